@@ -1,0 +1,100 @@
+"""Seeded synthetic workloads: shapes, seeds and input generators.
+
+This module holds no arithmetic of the method itself.  It only draws the
+inputs (q, k, v and the per-head decay values) that both the CUDA path and
+the CPU oracle consume, so the two sides always see the same numbers.
+
+Recipe: a CPU ``torch.Generator`` seeded per workload draws fp32 N(0, 1)
+samples in the order q, k, v; they are multiplied by the workload's scale and
+rounded once to the workload's dtype.  The oracle widens exactly those rounded
+values, the GPU reads them as they are.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    causal: bool
+    B: int
+    H: int
+    N: int
+    D: int
+    Dv: int
+    dtype: torch.dtype
+    scale: float
+    seed: int
+    decayed: bool = False
+    eps: float = 1e-6
+    # decode workloads: number of single-token steps after the prefill of N
+    steps: int = 0
+    step_seed0: int = 0
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.N
+
+    def gamma(self) -> Optional[torch.Tensor]:
+        return retnet_gammas(self.H) if self.decayed else None
+
+
+def retnet_gammas(H: int) -> torch.Tensor:
+    """Per-head fixed decays gamma_h = 1 - 2^(-5 - h/4), h = 0..H-1, computed
+    in fp64 and rounded once to fp32 (the value both sides use)."""
+    h = torch.arange(H, dtype=torch.float64)
+    return (1.0 - torch.pow(2.0, -5.0 - h / 4.0)).to(torch.float32)
+
+
+WORKLOADS = {
+    # causal, gamma = 1, fp32, B1 H1 N256 D=Dv=64, N(0,1), seed 0
+    "causal_f32_n256": Workload("causal_f32_n256", True, 1, 1, 256, 64, 64,
+                                torch.float32, 1.0, 0),
+    # causal, gamma = 1, bf16, B4 H8 N4096 D=Dv=64, N(0,1)*0.5, seed 1
+    "causal_bf16_n4096": Workload("causal_bf16_n4096", True, 4, 8, 4096, 64,
+                                  64, torch.bfloat16, 0.5, 1),
+    # causal with per-head RetNet decay, bf16, B2 H16 N16384 D=Dv=128, seed 2
+    "causal_decay_bf16_n16384": Workload("causal_decay_bf16_n16384", True, 2,
+                                         16, 16384, 128, 128, torch.bfloat16,
+                                         0.5, 2, decayed=True),
+    # non-causal, bf16, B8 H16 N65536 D=Dv=64, seed 3
+    "noncausal_bf16_n65536": Workload("noncausal_bf16_n65536", False, 8, 16,
+                                      65536, 64, 64, torch.bfloat16, 0.5, 3),
+    # decode: 256 sequences x H32, D=Dv=128; prefill of 512 tokens (seed 4),
+    # then 1024 single-token steps with fresh inputs from seed 1000 + t
+    "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
+                                128, torch.bfloat16, 0.5, 4, steps=1024,
+                                step_seed0=1000),
+}
+
+
+def make_qkv(B, H, N, D, Dv, dtype=torch.bfloat16, seed=0, scale=1.0,
+             device="cpu"):
+    """q, k: [B, H, N, D]; v: [B, H, N, Dv], drawn on the CPU in the order
+    q, k, v from one generator seeded with ``seed``, scaled, then rounded to
+    ``dtype`` and moved to ``device``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = []
+    for shape in ((B, H, N, D), (B, H, N, D), (B, H, N, Dv)):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if scale != 1.0:
+            x.mul_(scale)
+        out.append(x.to(dtype).to(device))
+    return tuple(out)
+
+
+def workload_inputs(w: Workload, device="cpu"):
+    """The q, k, v of workload ``w`` (for decode workloads: the prefill)."""
+    return make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, w.seed, w.scale, device)
+
+
+def decode_step_inputs(w: Workload, t: int, device="cpu"):
+    """Fresh q, k: [B, H, D] and v: [B, H, Dv] for decode step t."""
+    q, k, v = make_qkv(w.B, w.H, 1, w.D, w.Dv, w.dtype, w.step_seed0 + t,
+                       w.scale, device)
+    return q[:, :, 0], k[:, :, 0], v[:, :, 0]
