@@ -1,0 +1,396 @@
+"""Benchmark: causal linear-attention forward, tokens/s and roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step is one forward pass (one la_forward call) over the whole workload,
+inputs already resident in HBM.  The default workload is the causal,
+per-head-decayed one at N = 16384, D = Dv = 128, bf16 (B = 2, H = 16); its
+Q, K, V and O (537 MB) exceed the 129 MB L2, so no flush is needed between
+iterations.  Under torchrun each rank runs its own replica (independent
+batches, no collective on the data path: weak scaling); the time is the max
+over ranks and the value the tokens of all ranks over that time.
+
+Rank 0 prints one JSON line.  `--impl reference` times the fp64 CPU oracle
+instead (the one other place this script runs oracle/), on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("causal linear-attn fwd tokens/s and % roofline "
+          "(TFLOP/s or HBM GB/s), 1×GB300")
+DEFAULT_WORKLOAD = "causal_decay_bf16_n16384"
+FALLBACK_HBM_GBS = 6800.0  # profiling recipe fallback, used only if absent
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture, keyed by workload, with the hash of the kernel source the
+# capture was taken on; reported only while that source is unchanged.
+NCU_TRAFFIC = {}
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU multi-process tests)
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(ms_per_step_max: float, tokens_per_rank_step: int, world: int):
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step / (ms_per_step_max / 1e3)
+
+
+def algorithmic_work(w):
+    """Algorithmic bytes and flops of one forward pass over the workload.
+
+    Bytes: Q, K, V read and O written once, in their dtype (the state never
+    leaves the chip).  Flops per (b, h, token), recurrent form: 2 D Dv state
+    update + 2 D Dv read-out + 2 D denominator + D normaliser update + Dv
+    divides (the chunked kernel's extra intra-chunk work is not counted)."""
+    import torch
+    es = torch.tensor([], dtype=w.dtype).element_size()
+    units = w.B * w.H * w.N
+    byts = units * (2 * w.D + 2 * w.Dv) * es
+    flops = units * (4 * w.D * w.Dv + 3 * w.D + w.Dv)
+    return byts, flops
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kernelized_sequence_mixing_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+
+def oracle_sample(w, heads_per_pass):
+    """A bounded sample of the workload for the fp64 oracle: the first
+    `heads_per_pass` (b, h) units, every token."""
+    from kernelized_sequence_mixing_gb300.workloads import workload_inputs
+    import numpy as np
+    q, k, v = workload_inputs(w)
+    f = lambda t: t.float().reshape(-1, w.N, t.shape[-1])[:heads_per_pass].numpy()  # noqa: E731
+    g = w.gamma()
+    gu = None
+    if g is not None:
+        gu = np.tile(g.numpy(), w.B)[:heads_per_pass]
+    return f(q), f(k), f(v), gu
+
+
+def time_oracle(w, heads_per_pass, passes):
+    import oracle
+    qs, ks, vs, gu = oracle_sample(w, heads_per_pass)
+    threads = oracle.default_threads()
+    times = []
+    for _ in range(passes):
+        t0 = time.perf_counter()
+        if w.causal:
+            oracle.causal(qs, ks, vs, gamma=gu, eps=w.eps, nthreads=threads)
+        else:
+            oracle.noncausal(qs, ks, vs, eps=w.eps, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    # tokens/s of the workload's metric: a token is one position of one
+    # sequence across all H heads, so the sample covers heads/H of N tokens.
+    tokens = heads_per_pass / w.H * w.N
+    return tokens, times, threads
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    heads = min(8, w.B * w.H)
+    for _ in range(args.warmup):
+        time_oracle(w, heads, 1)
+    tokens, times, threads = time_oracle(w, heads, args.steps)
+    total = sum(times)
+    value = tokens * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{heads} of {w.B * w.H} (b,h) units, all "
+                                   f"{w.N} tokens, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+           "Dv": w.Dv, "causal": w.causal, "global_batch": w.B,
+           "seq_len": w.N, "parallelism": "replicas (independent batches)"}
+    if w.decayed:
+        cfg["gamma"] = "per head 1 - 2^(-5 - h/4)"
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def run_ours(args, w):
+    import torch
+    import kernelized_sequence_mixing_gb300 as la
+    from kernelized_sequence_mixing_gb300 import build as labuild
+    from kernelized_sequence_mixing_gb300.workloads import make_qkv
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        labuild.build()
+    barrier(ws)
+    la.load_library()
+
+    # this rank's replica: an independent batch of the same shape
+    q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, w.seed + 7919 * rank,
+                       w.scale)
+    g = w.gamma()
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 if w.causal else 4
+
+    def step():
+        la.forward(qd, kd, vd, causal=w.causal, gamma=g, eps=w.eps, out=od)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # keep the GPU under the same load before and after the timed region so
+    # the clock sampler sees it even when the timed region is short
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = ev[0].elapsed_time(ev[-1]) / args.steps
+
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+
+    ms_max = reduce_max(ms, ws)
+    tokens_rank = w.B * w.N
+    value = aggregate(ms_max, tokens_rank, ws)
+
+    # end to end through the public API with host buffers: pinned inputs
+    # copied in, result copied out, every step
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
+    la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+    e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, ws)
+    es = q.element_size()
+    h2d = (q.numel() + k.numel() + v.numel()) * es
+    d2h = od.numel() * es
+
+    if rank != 0:
+        return 0
+
+    hbm_peak, tc_peak, peak_src = measured_peaks()
+    byts, flops = algorithmic_work(w)
+    launch_ms = statistics.mean(per_launch)  # one kernel launch per step
+    achieved_gbs = byts / (launch_ms / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes"] if tr and tr.get("source") == src_hash else None
+
+    # CPU baseline: the fp64 oracle on the host cores, one pass over a bounded
+    # sample (all 32 heads of the default workload, ~20 s of CPU work)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        heads = min(w.B * w.H, 32)
+        tokens, times, threads = time_oracle(w, heads, 1)
+        cpu = {"value": tokens / times[0], "unit": "tokens/s",
+               "cores": threads, "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} (b,h) units, all {w.N} "
+                         f"tokens, one pass ({times[0]:.1f} s wall)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype.itemsize == 2 else "f32",
+        "data": "synthetic",
+        "config": dict(workload_config(w),
+                       l2="inputs larger than L2 (Q,K,V,O = "
+                          f"{byts / 1e6:.0f} MB), no flush"),
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs,
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                                    if peak_src == "measured" else "fallback",
+                     "algorithmic_bytes": byts,
+                     "tflops": flops / (launch_ms / 1e3) / 1e12,
+                     "tensor_peak_tflops": tc_peak},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens_rank * ws / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "kernel_source": src_hash,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    from kernelized_sequence_mixing_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

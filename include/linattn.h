@@ -1,0 +1,124 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) kernelized linear-attention
+ * library.
+ *
+ * The library computes linear attention with the Linear Transformer feature
+ * map phi(x) = elu(x) + 1 (x + 1 for x > 0, exp(x) otherwise):
+ *
+ *   o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i + eps)
+ *
+ * in the three forms described on "Linear Attention Mechanisms"
+ * (dileepadev.github.io) and "Attention-Free / Sub-Quadratic Architectures"
+ * (blog.vguerra.net):
+ *   - causal:     S_i = gamma S_{i-1} + phi(k_i) v_i^T, z_i = gamma z_{i-1} +
+ *                 phi(k_i) ("Recurrent Reformulation"; "The recurrent form
+ *                 (causal)"; fixed decay gamma from "Gating and Selective
+ *                 State Updates" / "Evolution: add decay/gating", applied to
+ *                 both S and z);
+ *   - non-causal: S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j) over every
+ *                 key, shared by every query ("The Kernel Trick for
+ *                 Attention"; "Linear Attention (the core trick)");
+ *   - decode:     one step of the causal recurrence on a caller-held state.
+ * eps is added to the denominator after the dot product, as in the NumPy
+ * listing on "Linear Attention Mechanisms" (sadullah.online), "The linear
+ * attention trick".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are dense, row-major, contiguous, in DEVICE memory:
+ *     q, k  [B][H][N][D]      v, o  [B][H][N][Dv]     (forward / prefill)
+ *     q, k  [B][H][D]         v, o  [B][H][Dv]        (decode step)
+ *     S     [B][H][D][Dv] fp32                        (state, caller-owned)
+ *     z     [B][H][D]     fp32
+ *   q, k, v and o all have the element type `dtype` (LA_F32 or LA_BF16).
+ *   Every device pointer must be 16-byte aligned.
+ * - gamma is a HOST array of H floats in [0, 1] (one decay per head), or
+ *   NULL meaning 1 for every head.  The library copies the values during the
+ *   call; the caller keeps ownership.
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call is asynchronous on that stream and never synchronises.  The
+ *   caller owns all buffers; the library keeps no state between calls.
+ * - Arguments are validated before any CUDA call, so a rejected call has no
+ *   side effect.  A launch failure returns LA_ERR_CUDA; an error raised while
+ *   a kernel runs surfaces at the caller's next synchronisation.
+ * - Supported sizes: D and Dv in {64, 128}; H <= 256; B*H*N < 2^31 tokens per
+ *   call.  B, H or N equal to 0 is an empty call that returns LA_OK (for
+ *   la_prefill_state with N = 0 the state is set to zero).
+ * - Arithmetic: fp32 state and accumulation.  For LA_BF16 the tensor-core
+ *   kernels round phi(q), phi(k), the decay-weighted values and the
+ *   intra-chunk weights to bf16 as matrix-multiply operands; o is rounded to
+ *   bf16 (round to nearest even).
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad eps or
+                             gamma, aliasing output, gamma != 1 when
+                             non-causal */
+  LA_ERR_UNSUPPORTED = 2, /* valid but not implemented: D or Dv not in
+                             {64, 128}, H > 256, too many tokens */
+  LA_ERR_CUDA = 3         /* a CUDA call or kernel launch failed */
+} la_status_t;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype_t;
+
+/*
+ * Forward pass over whole sequences.
+ *   causal != 0: o_i uses keys/values j <= i (inclusive), decayed by
+ *                gamma[h]^(i-j).
+ *   causal == 0: o_i uses every key/value of its (b, h); gamma must be NULL
+ *                or all 1 (otherwise LA_ERR_INVALID_ARG).  The non-causal
+ *                path needs a stream-ordered workspace of about
+ *                B*H*(D*Dv + D)*4*(1 + ceil(N/4096)) bytes, taken with
+ *                cudaMallocAsync on `stream` and released on it.
+ * q, k: [B][H][N][D]; v: [B][H][N][Dv]; o: [B][H][N][Dv] (written).  o must
+ * not overlap q, k or v.  eps must be finite and >= 0.
+ */
+LA_API la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
+                       int B, int H, int N, int D, int Dv, int causal,
+                       const float *gamma, float eps, la_dtype_t dtype,
+                       void *stream);
+
+/*
+ * State after a causal pass over N tokens (the prefill of the decode loop):
+ *   S = sum_j gamma^(N-1-j) phi(k_j) v_j^T,  z = sum_j gamma^(N-1-j) phi(k_j)
+ * k: [B][H][N][D]; v: [B][H][N][Dv] (dtype); S: [B][H][D][Dv] fp32 and
+ * z: [B][H][D] fp32 are overwritten.  S and z must not overlap k or v, nor
+ * each other.
+ */
+LA_API la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
+                             int B, int H, int N, int D, int Dv,
+                             const float *gamma, la_dtype_t dtype,
+                             void *stream);
+
+/*
+ * One recurrent decode step, in place: first
+ *   S <- gamma S + phi(k) v^T,  z <- gamma z + phi(k),
+ * then  o = phi(q)^T S / (phi(q) . z + eps)  with the updated state.
+ * q, k: [B][H][D]; v, o: [B][H][Dv] (dtype); S: [B][H][D][Dv] fp32 and
+ * z: [B][H][D] fp32 are read and rewritten.  No buffer may overlap another.
+ */
+LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
+                           float *S, float *z, void *o, int B, int H, int D,
+                           int Dv, const float *gamma, float eps,
+                           la_dtype_t dtype, void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+LA_API const char *la_status_string(la_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

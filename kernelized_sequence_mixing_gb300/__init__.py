@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) kernelized linear attention, phi(x) = elu(x) + 1.
+
+A thin ctypes binding over the C ABI in include/linattn.h (liblinattn.so,
+built in-tree by ``kernelized_sequence_mixing_gb300.build``).  This module
+only marshals arguments: shapes, dtypes, the current CUDA stream and, for host
+tensors, the host<->device copies around the call.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU fallback, and
+a missing library raises RuntimeError.
+
+Functions (same names as the C entry points, minus the ``la_`` prefix):
+  forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None)
+  prefill_state(k, v, gamma=None, S=None, z=None)
+  decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import workloads  # noqa: F401  (seeded input generators)
+
+__all__ = ["forward", "prefill_state", "decode_step", "status_string",
+           "load_library", "library_path", "LinAttnError", "workloads"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "liblinattn.so")
+_lib = None
+_lock = threading.Lock()
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA = 0, 1, 2, 3
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load liblinattn.so; raises RuntimeError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m kernelized_sequence_mixing_gb300.build` "
+                    "(or __graft_entry__.build()); there is no fallback path")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            FP = ctypes.POINTER(ctypes.c_float)
+            lib.la_forward.argtypes = [P, P, P, P, I, I, I, I, I, I, FP, F, I, P]
+            lib.la_forward.restype = I
+            lib.la_prefill_state.argtypes = [P, P, P, P, I, I, I, I, I, FP, I, P]
+            lib.la_prefill_state.restype = I
+            lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, FP, F,
+                                           I, P]
+            lib.la_decode_step.restype = I
+            lib.la_status_string.argtypes = [I]
+            lib.la_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load_library().la_status_string(int(code)).decode()
+
+
+def _gamma_arg(gamma, H):
+    if gamma is None:
+        return None
+    if isinstance(gamma, torch.Tensor):
+        vals = gamma.detach().to("cpu", torch.float32).reshape(-1).tolist()
+    elif isinstance(gamma, (int, float)):
+        vals = [float(gamma)] * H
+    else:
+        vals = [float(x) for x in gamma]
+    if len(vals) != H:
+        raise ValueError(f"gamma needs {H} values (one per head), got {len(vals)}")
+    return (ctypes.c_float * H)(*vals)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check(fn, code):
+    if code != LA_OK:
+        raise LinAttnError(fn, code)
+
+
+def _contig(name, t):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _to_device(t, dev):
+    if t.device.type == "cuda":
+        return t
+    if not t.is_pinned():
+        t = t.pin_memory()
+    return t.to(dev, non_blocking=True)
+
+
+def forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None,
+            device=None):
+    """Linear attention over whole sequences.
+
+    q, k: [B, H, N, D]; v: [B, H, N, Dv]; all float32 or all bfloat16,
+    contiguous.  CUDA tensors are used in place on the current stream; host
+    tensors are copied to ``device`` (default cuda:0), computed there and the
+    result copied back to host memory (pinned).  gamma: None, a float, or H
+    per-head decays in [0, 1] (causal only).  Returns o: [B, H, N, Dv].
+    """
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    host = q.device.type != "cuda"
+    dev = torch.device(device or "cuda:0") if host else q.device
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    dt = _dtype_code(q)
+    g = _gamma_arg(gamma, H)
+    with torch.cuda.device(dev):
+        qd, kd, vd = (_to_device(t, dev) for t in (q, k, v))
+        od = out if (out is not None and not host) else torch.empty(
+            (B, H, N, Dv), dtype=q.dtype, device=dev)
+        _contig("out", od)
+        _check("la_forward", lib.la_forward(
+            _ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), B, H, N, D, Dv,
+            1 if causal else 0, g, float(eps), dt, _stream(dev)))
+        if not host:
+            return od
+        res = out if out is not None else torch.empty(
+            od.shape, dtype=od.dtype, pin_memory=True)
+        res.copy_(od, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        return res
+
+
+def prefill_state(k, v, gamma=None, S=None, z=None):
+    """State after a causal pass: S = sum_j gamma^(N-1-j) phi(k_j) v_j^T,
+    z likewise.  k: [B, H, N, D], v: [B, H, N, Dv] CUDA tensors.  Returns
+    (S [B, H, D, Dv] fp32, z [B, H, D] fp32), written into S, z if given."""
+    lib = load_library()
+    _contig("k", k)
+    _contig("v", v)
+    B, H, N, D = k.shape
+    Dv = v.shape[-1]
+    if v.shape[:3] != k.shape[:3] or k.dtype != v.dtype:
+        raise ValueError("k, v shapes/dtypes disagree")
+    dev = k.device
+    with torch.cuda.device(dev):
+        if S is None:
+            S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
+        if z is None:
+            z = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+        _check("la_prefill_state", lib.la_prefill_state(
+            _ptr(k), _ptr(v), _ptr(S), _ptr(z), B, H, N, D, Dv,
+            _gamma_arg(gamma, H), _dtype_code(k), _stream(dev)))
+    return S, z
+
+
+def decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None):
+    """One recurrent step in place on (S, z): update with (k, v), then read
+    out with q.  q, k: [B, H, D]; v: [B, H, Dv]; S: [B, H, D, Dv] fp32;
+    z: [B, H, D] fp32 (all CUDA).  Returns o: [B, H, Dv]."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("S", S), ("z", z)):
+        _contig(n, t)
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty((B, H, Dv), dtype=q.dtype, device=dev)
+        _check("la_decode_step", lib.la_decode_step(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out), B, H, D,
+            Dv, _gamma_arg(gamma, H), float(eps), _dtype_code(q),
+            _stream(dev)))
+    return out

@@ -1,0 +1,58 @@
+// Host-side launchers of the library's kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace linattn {
+
+constexpr int kMaxHeads = 256;
+
+// Per-head decay values, passed to kernels by value.
+struct Gammas {
+  float g[kMaxHeads];
+};
+
+enum Dtype { kF32 = 0, kBF16 = 1 };
+
+struct Problem {
+  const void *q, *k, *v;
+  void *o;
+  int B, H, N, D, Dv;
+  bool decay;  // any gamma != 1
+  float eps;
+  Dtype dtype;
+};
+
+// Causal forward on CUDA cores (fp32 FFMA): any dtype.
+cudaError_t launch_causal_simt(const Problem &p, const Gammas &g,
+                               cudaStream_t s);
+
+// Causal forward on tcgen05 tensor cores (bf16 operands, fp32 state).
+// Returns cudaErrorNotSupported when the shape is outside its envelope.
+cudaError_t launch_causal_tc(const Problem &p, const Gammas &g,
+                             cudaStream_t s);
+
+// Split-N reduction of S = sum_j w_j phi(k_j) v_j^T and z = sum_j w_j
+// phi(k_j) with w_j = gamma^(N-1-j): partials [nsplit][BH][D*Dv + D] in
+// `partials` (fp32) unless nsplit == 1, in which case S, z are written
+// directly.  Then a fixed-order reduction into S [BH][D][Dv], z [BH][D].
+int kv_state_num_splits(int BH, int N);
+size_t kv_state_workspace_bytes(int BH, int N, int D, int Dv);
+cudaError_t launch_kv_state(const void *k, const void *v, float *S, float *z,
+                            float *partials, int B, int H, int N, int D,
+                            int Dv, bool decay, const Gammas &g, Dtype dt,
+                            cudaStream_t s);
+
+// o = phi(q) S / (phi(q) . z + eps) for every row, S and z per (b, h).
+cudaError_t launch_noncausal_apply(const void *q, const float *S,
+                                   const float *z, void *o, int BH, int N,
+                                   int D, int Dv, float eps, Dtype dt,
+                                   cudaStream_t s);
+
+// One decode step in place on S, z.
+cudaError_t launch_decode_step(const void *q, const void *k, const void *v,
+                               float *S, float *z, void *o, int B, int H,
+                               int D, int Dv, bool decay, const Gammas &g,
+                               float eps, Dtype dt, cudaStream_t s);
+
+}  // namespace linattn

@@ -1,0 +1,190 @@
+// C ABI of the library: argument validation, workspace and dispatch.
+//
+// Every check runs before the first CUDA call, so a rejected call has no side
+// effect on the device or the stream.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/linattn.h"
+#include "kernels.h"
+
+using namespace linattn;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+size_t elem_size(la_dtype_t dt) { return dt == LA_F32 ? 4 : 2; }
+
+bool supported_dim(int d) { return d == 64 || d == 128; }
+
+// Common size/type checks.  Returns LA_OK or the first failure.
+la_status_t check_sizes(int B, int H, int N, int D, int Dv, la_dtype_t dt) {
+  if (dt != LA_F32 && dt != LA_BF16) return LA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || D <= 0 || Dv <= 0) return LA_ERR_INVALID_ARG;
+  if (!supported_dim(D) || !supported_dim(Dv)) return LA_ERR_UNSUPPORTED;
+  if (H > kMaxHeads) return LA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H * (int64_t)(N > 0 ? N : 1) >= ((int64_t)1 << 31))
+    return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
+// gamma: NULL (all 1) or H values in [0, 1].  Fills g and reports whether any
+// value differs from 1.
+la_status_t load_gammas(const float *gamma, int H, Gammas *g, bool *decay) {
+  *decay = false;
+  for (int h = 0; h < kMaxHeads; ++h) g->g[h] = 1.f;
+  if (!gamma) return LA_OK;
+  for (int h = 0; h < H; ++h) {
+    const float x = gamma[h];
+    if (!(x >= 0.f && x <= 1.f)) return LA_ERR_INVALID_ARG;  // also NaN
+    g->g[h] = x;
+    if (x != 1.f) *decay = true;
+  }
+  return LA_OK;
+}
+
+la_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return LA_OK;
+  if (e == cudaErrorNotSupported) return LA_ERR_UNSUPPORTED;
+  return LA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *la_status_string(la_status_t s) {
+  switch (s) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARG: return "invalid argument";
+    case LA_ERR_UNSUPPORTED: return "unsupported shape or size";
+    case LA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
+                       int B, int H, int N, int D, int Dv, int causal,
+                       const float *gamma, float eps, la_dtype_t dtype,
+                       void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  if (!causal && decay) return LA_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)B * H * N;
+  if (rows == 0) return LA_OK;
+  if (!q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)rows * D * es, nv = (size_t)rows * Dv * es;
+  if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv))
+    return LA_ERR_INVALID_ARG;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Problem p{q, k, v, o, B, H, N, D, Dv, decay, eps,
+            dtype == LA_F32 ? kF32 : kBF16};
+  if (causal) {
+    if (p.dtype == kBF16) {
+      cudaError_t e = launch_causal_tc(p, g, s);
+      if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    return from_cuda(launch_causal_simt(p, g, s));
+  }
+  // Non-causal: reduce S, z per (b, h) into a stream-ordered workspace, then
+  // apply them to every query.
+  const int BH = B * H;
+  const size_t state_bytes = sizeof(float) * (size_t)BH * ((size_t)D * Dv + D);
+  const size_t part_bytes = kv_state_workspace_bytes(BH, N, D, Dv);
+  void *ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, state_bytes + part_bytes, s);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  float *S = static_cast<float *>(ws);
+  float *z = S + (size_t)BH * D * Dv;
+  float *part = part_bytes ? z + (size_t)BH * D : nullptr;
+  e = launch_kv_state(k, v, S, z, part, B, H, N, D, Dv, false, g, p.dtype, s);
+  if (e == cudaSuccess)
+    e = launch_noncausal_apply(q, S, z, o, BH, N, D, Dv, eps, p.dtype, s);
+  cudaError_t ef = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(ef);
+}
+
+la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
+                             int B, int H, int N, int D, int Dv,
+                             const float *gamma, la_dtype_t dtype,
+                             void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  const int BH = B * H;
+  if (BH == 0) return LA_OK;
+  if (!S || !z || !aligned16(S) || !aligned16(z)) return LA_ERR_INVALID_ARG;
+  const size_t nS = sizeof(float) * (size_t)BH * D * Dv, nz = sizeof(float) * (size_t)BH * D;
+  if (overlaps(S, nS, z, nz)) return LA_ERR_INVALID_ARG;
+  if (N > 0) {
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return LA_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    const size_t nk = (size_t)BH * N * D * es, nv = (size_t)BH * N * Dv * es;
+    if (overlaps(S, nS, k, nk) || overlaps(S, nS, v, nv) ||
+        overlaps(z, nz, k, nk) || overlaps(z, nz, v, nv))
+      return LA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t part_bytes = kv_state_workspace_bytes(BH, N, D, Dv);
+  void *ws = nullptr;
+  if (part_bytes) {
+    if (cudaMallocAsync(&ws, part_bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+  }
+  cudaError_t e = launch_kv_state(k, v, S, z, static_cast<float *>(ws), B, H,
+                                  N, D, Dv, decay, g,
+                                  dtype == LA_F32 ? kF32 : kBF16, s);
+  cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(ef);
+}
+
+la_status_t la_decode_step(const void *q, const void *k, const void *v,
+                           float *S, float *z, void *o, int B, int H, int D,
+                           int Dv, const float *gamma, float eps,
+                           la_dtype_t dtype, void *stream) {
+  la_status_t st = check_sizes(B, H, 1, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  const int BH = B * H;
+  if (BH == 0) return LA_OK;
+  if (!q || !k || !v || !S || !z || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) ||
+      !aligned16(z) || !aligned16(o))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const void *ptr[6] = {q, k, v, S, z, o};
+  const size_t len[6] = {(size_t)BH * D * es, (size_t)BH * D * es,
+                         (size_t)BH * Dv * es, sizeof(float) * (size_t)BH * D * Dv,
+                         sizeof(float) * (size_t)BH * D, (size_t)BH * Dv * es};
+  // the written buffers (S, z, o) may overlap nothing
+  for (int w = 3; w < 6; ++w)
+    for (int i = 0; i < 6; ++i)
+      if (i != w && overlaps(ptr[w], len[w], ptr[i], len[i])) return LA_ERR_INVALID_ARG;
+  return from_cuda(launch_decode_step(q, k, v, S, z, o, B, H, D, Dv, decay, g,
+                                      eps, dtype == LA_F32 ? kF32 : kBF16,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

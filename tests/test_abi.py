@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/*.h declares, and rejects bad arguments before any CUDA call (so
+these tests never touch a device)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, UNSUPPORTED, CUDA_ERR = 0, 1, 2, 3
+F32, BF16 = 0, 1
+A = 0x10000          # a 16-byte aligned fake device address (never touched)
+STEP = 0x10000000    # distance between fake buffers (no overlap)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kernelized_sequence_mixing_gb300 import build
+    build.build()
+    import kernelized_sequence_mixing_gb300 as la
+    return la.load_library()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names.update(re.findall(r"LA_API\s+[\w\s\*]*?\b(la_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    for s in ("la_forward", "la_prefill_state", "la_decode_step",
+              "la_status_string"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, text in ((OK, "ok"), (INVALID, "invalid argument"),
+                       (UNSUPPORTED, "unsupported"), (CUDA_ERR, "CUDA")):
+        assert text in lib.la_status_string(code).decode()
+
+
+def fwd(lib, q=A, k=A + STEP, v=A + 2 * STEP, o=A + 3 * STEP, B=1, H=2, N=8,
+        D=64, Dv=64, causal=1, gamma=None, eps=1e-6, dt=BF16):
+    g = None if gamma is None else (ctypes.c_float * len(gamma))(*gamma)
+    return lib.la_forward(q, k, v, o, B, H, N, D, Dv, causal, g, eps, dt, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, o=0) == INVALID
+    assert fwd(lib, q=A + 8) == INVALID          # misaligned
+    assert fwd(lib, v=A + 2 * STEP + 4) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, D=0) == INVALID
+    assert fwd(lib, eps=-1e-6) == INVALID
+    assert fwd(lib, eps=float("nan")) == INVALID
+    assert fwd(lib, eps=float("inf")) == INVALID
+    assert fwd(lib, gamma=[0.5, 1.5]) == INVALID
+    assert fwd(lib, gamma=[0.5, float("nan")]) == INVALID
+    assert fwd(lib, gamma=[-0.1, 1.0]) == INVALID
+    assert fwd(lib, causal=0, gamma=[0.5, 1.0]) == INVALID
+    assert fwd(lib, dt=7) == INVALID
+    # aliasing: o overlaps q (same start, or partial overlap)
+    assert fwd(lib, o=A) == INVALID
+    assert fwd(lib, o=A + 1024) == INVALID
+
+
+def test_forward_unsupported_shapes(lib):
+    assert fwd(lib, D=96) == UNSUPPORTED
+    assert fwd(lib, Dv=256) == UNSUPPORTED
+    assert fwd(lib, D=32, dt=F32) == UNSUPPORTED
+    g = [1.0] * 257
+    assert fwd(lib, H=257, gamma=g) == UNSUPPORTED
+    assert fwd(lib, B=1 << 16, H=256, N=1 << 16, gamma=[1.0] * 256) == UNSUPPORTED
+
+
+def test_forward_empty_calls_are_noops(lib):
+    assert fwd(lib, N=0, q=None, k=None, v=None, o=None) == OK
+    assert fwd(lib, B=0, q=None, k=None, v=None, o=None) == OK
+    assert fwd(lib, H=0, q=None, k=None, v=None, o=None) == OK
+    # gamma of 1 is accepted non-causally
+    assert fwd(lib, N=0, causal=0, gamma=[1.0, 1.0]) == OK
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    P = lib.la_prefill_state
+    assert P(A, A + STEP, None, A + 3 * STEP, 1, 2, 8, 64, 64, None, BF16, None) == INVALID
+    assert P(A, A + STEP, A + 2 * STEP, A + 2 * STEP, 1, 2, 8, 64, 64, None, BF16, None) == INVALID
+    assert P(A, A + STEP, A, A + 3 * STEP, 1, 2, 8, 64, 64, None, BF16, None) == INVALID
+    assert P(A, A + STEP, A + 2 * STEP + 4, A + 3 * STEP, 1, 2, 8, 64, 64, None, BF16, None) == INVALID
+    bad = (ctypes.c_float * 2)(2.0, 1.0)
+    assert P(A, A + STEP, A + 2 * STEP, A + 3 * STEP, 1, 2, 8, 64, 64, bad, BF16, None) == INVALID
+    assert P(A, A + STEP, A + 2 * STEP, A + 3 * STEP, 1, 2, 8, 48, 64, None, BF16, None) == UNSUPPORTED
+    assert P(None, None, None, None, 0, 2, 8, 64, 64, None, BF16, None) == OK
+
+
+def test_decode_rejects_bad_arguments(lib):
+    Dc = lib.la_decode_step
+    ptrs = [A + i * STEP for i in range(6)]
+
+    def call(p=ptrs, B=2, H=2, D=128, Dv=128, eps=1e-6, g=None, dt=BF16):
+        return Dc(*p, B, H, D, Dv, g, eps, dt, None)
+
+    assert call(p=[None] + ptrs[1:]) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(p=ptrs[:5] + [ptrs[3]]) == INVALID      # o aliases S
+    assert call(p=ptrs[:4] + [ptrs[3] + 64, ptrs[5]]) == INVALID  # z inside S
+    assert call(p=ptrs[:3] + [ptrs[0]] + ptrs[4:]) == INVALID     # S aliases q
+    assert call(p=ptrs[:5] + [ptrs[5] + 2]) == INVALID  # misaligned o
+    assert call(D=100) == UNSUPPORTED
+    assert call(g=(ctypes.c_float * 2)(1.0, -0.5)) == INVALID
+    assert call(B=0, p=[None] * 6) == OK

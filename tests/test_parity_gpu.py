@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Small cases are compared in full (several chunk tiles plus a ragged tail);
+the full-size workloads, run in the same launch configuration the benchmark
+times, are compared on whole sampled heads.  Errors are per-row normwise
+(see helpers.TOL): 1e-4 for fp32 inputs, 2e-2 for bf16 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+from helpers import TOL, max_row_error, state_error, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kernelized_sequence_mixing_gb300 import build
+    build.build()
+    import kernelized_sequence_mixing_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def ora(oracle_mod):
+    return oracle_mod
+
+
+def gen(B, H, N, D, Dv, dtype, seed, scale=0.5):
+    from kernelized_sequence_mixing_gb300.workloads import make_qkv
+    return make_qkv(B, H, N, D, Dv, dtype, seed, scale)
+
+
+def gammas_for(H, kind):
+    if kind is None:
+        return None
+    if kind == "mix":
+        base = [0.0, 0.5, 0.9, 0.96875, 0.999, 1.0]
+        return torch.tensor([base[h % len(base)] for h in range(H)],
+                            dtype=torch.float32)
+    if kind == "retnet":
+        from kernelized_sequence_mixing_gb300.workloads import retnet_gammas
+        return retnet_gammas(H)
+    return torch.full((H,), float(kind), dtype=torch.float32)
+
+
+# --------------------------------------------------------------------------
+# causal forward
+
+CAUSAL_SMALL = [
+    # (B, H, N, D, Dv)
+    (1, 1, 1, 64, 64),
+    (1, 2, 63, 64, 64),
+    (2, 1, 64, 64, 128),
+    (1, 3, 65, 128, 64),
+    (1, 2, 200, 128, 128),
+    (2, 2, 1000, 64, 64),
+    (1, 2, 1337, 128, 128),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16],
+                         ids=["f32", "bf16"])
+@pytest.mark.parametrize("gkind", [None, "mix"])
+@pytest.mark.parametrize("shape", CAUSAL_SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_causal_small(la, ora, dtype, gkind, shape):
+    B, H, N, D, Dv = shape
+    q, k, v = gen(B, H, N, D, Dv, dtype, seed=N + D + 7 * H)
+    g = gammas_for(H, gkind)
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = ora.causal(to_np(q), to_np(k), to_np(v),
+                     gamma=None if g is None else g.numpy(), eps=1e-6)
+    err = max_row_error(to_np(o), ref)
+    assert err < TOL[dtype], err
+
+
+def test_causal_f32_n256_full(la, ora):
+    """fp32, gamma = 1, B1 H1 N256 D=Dv=64, N(0,1) from seed 0."""
+    from kernelized_sequence_mixing_gb300.workloads import (WORKLOADS,
+                                                            workload_inputs)
+    w = WORKLOADS["causal_f32_n256"]
+    q, k, v = workload_inputs(w)
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, eps=w.eps)
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), eps=w.eps)
+    assert o.shape == (1, 1, 256, 64) and o.dtype == torch.float32
+    assert max_row_error(to_np(o), ref) < 1e-4
+
+
+def test_causal_bf16_n4096_full(la, ora):
+    """bf16, gamma = 1, B4 H8 N4096 D=Dv=64: every row of every head."""
+    from kernelized_sequence_mixing_gb300.workloads import (WORKLOADS,
+                                                            workload_inputs)
+    w = WORKLOADS["causal_bf16_n4096"]
+    q, k, v = workload_inputs(w)
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, eps=w.eps)
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), eps=w.eps)
+    assert max_row_error(to_np(o), ref) < 2e-2
+
+
+def test_causal_decay_bf16_n16384_sampled_heads(la, ora):
+    """The benchmarked workload (B2 H16 N16384 D=Dv=128, per-head RetNet
+    decay), one launch at full size; whole heads compared, including the
+    fastest (h = 0) and slowest (h = 15) decay."""
+    from kernelized_sequence_mixing_gb300.workloads import (WORKLOADS,
+                                                            workload_inputs)
+    w = WORKLOADS["causal_decay_bf16_n16384"]
+    q, k, v = workload_inputs(w)
+    g = w.gamma()
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g,
+                   eps=w.eps)
+    o = to_np(o)
+    assert np.isfinite(o).all()
+    for b, h in ((0, 0), (0, 15), (1, 7), (1, 3)):
+        ref = ora.causal(to_np(q[b, h]), to_np(k[b, h]), to_np(v[b, h]),
+                         gamma=float(g[h]), eps=w.eps)
+        err = max_row_error(o[b, h], ref)
+        assert err < 2e-2, (b, h, err)
+
+
+def test_causal_empty_and_host_buffers(la, ora):
+    q, k, v = gen(1, 2, 0, 64, 64, torch.bfloat16, 1)
+    o = la.forward(q.cuda(), k.cuda(), v.cuda())
+    assert o.shape == (1, 2, 0, 64)
+    # host tensors: copied in, computed on the GPU, copied back
+    q, k, v = gen(1, 2, 300, 64, 128, torch.bfloat16, 2)
+    o_host = la.forward(q, k, v, gamma=[0.9, 1.0])
+    o_dev = la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=[0.9, 1.0])
+    assert o_host.device.type == "cpu"
+    assert torch.equal(o_host, o_dev.cpu())
+
+
+def test_causal_repeatable(la):
+    q, k, v = (t.cuda() for t in gen(2, 2, 777, 128, 128, torch.bfloat16, 3))
+    a = la.forward(q, k, v, gamma=[0.95, 0.5])
+    b = la.forward(q, k, v, gamma=[0.95, 0.5])
+    assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# non-causal forward
+
+NONCAUSAL_SMALL = [
+    (1, 1, 1, 64, 64),
+    (1, 2, 100, 64, 128),
+    (2, 1, 4096, 128, 64),
+    (1, 2, 4097, 128, 128),
+    (1, 1, 10000, 64, 64),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16],
+                         ids=["f32", "bf16"])
+@pytest.mark.parametrize("shape", NONCAUSAL_SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_noncausal_small(la, ora, dtype, shape):
+    B, H, N, D, Dv = shape
+    q, k, v = gen(B, H, N, D, Dv, dtype, seed=3 * N + D)
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=False)
+    ref = ora.noncausal(to_np(q), to_np(k), to_np(v), eps=1e-6)
+    assert max_row_error(to_np(o), ref) < TOL[dtype]
+
+
+def test_noncausal_equals_last_causal_row(la):
+    q, k, v = (t.cuda() for t in gen(1, 2, 999, 64, 64, torch.float32, 5))
+    on = la.forward(q, k, v, causal=False)
+    oc = la.forward(q, k, v, causal=True)
+    err = max_row_error(to_np(on[:, :, -1]), to_np(oc[:, :, -1]))
+    assert err < 1e-4
+
+
+def test_noncausal_repeatable(la):
+    q, k, v = (t.cuda() for t in gen(2, 2, 9000, 64, 64, torch.bfloat16, 6))
+    assert torch.equal(la.forward(q, k, v, causal=False),
+                       la.forward(q, k, v, causal=False))
+
+
+def test_noncausal_bf16_n65536_sampled_heads(la, ora):
+    """Full-size non-causal workload (B8 H16 N65536 D=Dv=64), one launch;
+    three whole heads compared."""
+    from kernelized_sequence_mixing_gb300.workloads import (WORKLOADS,
+                                                            workload_inputs)
+    w = WORKLOADS["noncausal_bf16_n65536"]
+    q, k, v = workload_inputs(w)
+    o = to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), causal=False,
+                         eps=w.eps))
+    assert np.isfinite(o).all()
+    for b, h in ((0, 0), (3, 9), (7, 15)):
+        ref = ora.noncausal(to_np(q[b, h]), to_np(k[b, h]), to_np(v[b, h]),
+                            eps=w.eps)
+        assert max_row_error(o[b, h], ref) < 2e-2, (b, h)
+
+
+# --------------------------------------------------------------------------
+# prefill and decode
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16],
+                         ids=["f32", "bf16"])
+@pytest.mark.parametrize("gkind", [None, "mix"])
+@pytest.mark.parametrize("N,D,Dv", [(0, 64, 64), (1, 64, 128), (300, 128, 64),
+                                    (5000, 128, 128)])
+def test_prefill_state(la, ora, dtype, gkind, N, D, Dv):
+    B, H = 1, 3
+    q, k, v = gen(B, H, N, D, Dv, dtype, seed=N + 11)
+    g = gammas_for(H, gkind)
+    S, z = la.prefill_state(k.cuda(), v.cuda(), gamma=g)
+    S_ref, z_ref = ora.prefill(to_np(k), to_np(v),
+                               gamma=None if g is None else g.numpy())
+    if N == 0:
+        assert not S.any() and not z.any()
+        return
+    tol = 1e-4  # fp32 sums of up to 5000 terms
+    assert state_error(to_np(S), S_ref) < tol
+    assert state_error(to_np(z)[..., None], z_ref[..., None]) < tol
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16],
+                         ids=["f32", "bf16"])
+@pytest.mark.parametrize("gkind", [None, "mix"])
+@pytest.mark.parametrize("D,Dv", [(64, 64), (128, 64), (64, 128), (128, 128)])
+def test_prefill_then_decode_matches_causal(la, ora, dtype, gkind, D, Dv):
+    """prefill(N) then M decode steps reproduce causal rows N..N+M-1."""
+    B, H, N, M = 2, 6, 70, 12
+    q, k, v = gen(B, H, N + M, D, Dv, dtype, seed=D + Dv)
+    g = gammas_for(H, gkind)
+    gn = None if g is None else g.numpy()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    S, z = la.prefill_state(kd[:, :, :N].contiguous(), vd[:, :, :N].contiguous(),
+                            gamma=g)
+    ref_full, S_end, z_end = ora.causal(to_np(q), to_np(k), to_np(v), gamma=gn,
+                                        return_state=True)
+    for t in range(M):
+        o = la.decode_step(qd[:, :, N + t].contiguous(), kd[:, :, N + t].contiguous(),
+                           vd[:, :, N + t].contiguous(), S, z, gamma=g)
+        err = max_row_error(to_np(o), ref_full[:, :, N + t])
+        assert err < TOL[dtype], (t, err)
+    assert state_error(to_np(S), S_end) < 1e-4
+    assert state_error(to_np(z)[..., None], z_end[..., None]) < 1e-4
+    # the GPU's own causal forward agrees too
+    oc = la.forward(qd, kd, vd, gamma=g)
+    assert max_row_error(to_np(o), to_np(oc[:, :, -1])) < 2 * TOL[dtype]
+
+
+def test_decode_state_roundtrip(la):
+    """A state copied out and back in continues identically (resume)."""
+    B, H, D, Dv = 2, 4, 128, 128
+    q, k, v = gen(B, H, 2, D, Dv, torch.bfloat16, 9)
+    S = torch.rand(B, H, D, Dv, device="cuda")
+    z = torch.rand(B, H, D, device="cuda") + 1
+    S2, z2 = S.cpu().cuda(), z.cpu().cuda()
+    args = [t[:, :, 0].contiguous().cuda() for t in (q, k, v)]
+    o1 = la.decode_step(*args, S, z)
+    o2 = la.decode_step(*args, S2, z2)
+    assert torch.equal(o1, o2) and torch.equal(S, S2) and torch.equal(z, z2)
+
+
+def test_decode_bf16_h32_full(la, ora):
+    """The decode workload: 256 sequences x H32, D=Dv=128, fp32 state from a
+    512-token prefill, then 1024 steps with fresh seeded inputs.  Sampled
+    (sequence, head) units are followed by the oracle through every step;
+    outputs are gated at steps 0..7, every 128th and the last, and the final
+    states are compared."""
+    from kernelized_sequence_mixing_gb300.workloads import (
+        WORKLOADS, decode_step_inputs, workload_inputs)
+    w = WORKLOADS["decode_bf16_h32"]
+    q, k, v = workload_inputs(w)
+    S, z = la.prefill_state(k.cuda(), v.cuda())
+    units = [(0, 0), (17, 5), (128, 31), (255, 16)]
+    bs = [u[0] for u in units]
+    hs = [u[1] for u in units]
+    Sr, zr = ora.prefill(to_np(k[bs, hs]), to_np(v[bs, hs]))
+    assert state_error(to_np(S[bs, hs]), Sr) < 1e-4
+    gate = set(range(8)) | set(range(0, w.steps, 128)) | {w.steps - 1}
+    worst = 0.0
+    for t in range(w.steps):
+        qt, kt, vt = decode_step_inputs(w, t)
+        o = la.decode_step(qt.cuda(), kt.cuda(), vt.cuda(), S, z, eps=w.eps)
+        orf, Sr, zr = ora.decode_step(to_np(qt[bs, hs]), to_np(kt[bs, hs]),
+                                      to_np(vt[bs, hs]), Sr, zr, eps=w.eps)
+        if t in gate:
+            err = max_row_error(to_np(o[bs, hs]), orf)
+            worst = max(worst, err)
+            assert err < 2e-2, (t, err)
+    assert state_error(to_np(S[bs, hs]), Sr) < 1e-4
+    assert state_error(to_np(z[bs, hs])[..., None], zr[..., None]) < 1e-4
