@@ -115,6 +115,28 @@ LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
                            int Dv, const float *gamma, float eps,
                            la_dtype_t dtype, void *stream);
 
+/*
+ * Which kernel la_forward would run for a causal call with these arguments:
+ * 1 = the tcgen05 tensor-core kernel (bf16, D and Dv in {64, 128}, every
+ * gamma >= 0.35, B*H <= 65535), 0 = the fp32 CUDA-core kernel (fp32 inputs,
+ * or stronger decays, whose gamma^-63 operand scale would leave the bf16
+ * range), or a negative la_status_t (negated) if the arguments are invalid.
+ * Host-only; touches no device.
+ */
+LA_API int la_causal_kernel(int B, int H, int N, int D, int Dv,
+                            const float *gamma, la_dtype_t dtype);
+
+/*
+ * Number of bounded device-side waits that gave up on the current device since
+ * the library was loaded (or since the last reset).  The tensor-core kernels
+ * bound every wait on another warp's progress; a nonzero count means some
+ * kernel abandoned its work and the outputs of that call are invalid.  Reads
+ * device memory with a blocking copy, so call it after synchronising the
+ * streams that ran the kernels.  reset != 0 sets the counter back to zero.
+ * Returns -1 if the counter cannot be read.
+ */
+LA_API int la_device_wait_timeouts(int reset);
+
 /* Static, NUL-terminated description of a status code. */
 LA_API const char *la_status_string(la_status_t s);
 

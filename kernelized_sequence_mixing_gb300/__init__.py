@@ -23,6 +23,7 @@ import torch
 from . import workloads  # noqa: F401  (seeded input generators)
 
 __all__ = ["forward", "prefill_state", "decode_step", "status_string",
+           "device_wait_timeouts", "causal_kernel",
            "load_library", "library_path", "LinAttnError", "workloads"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -64,6 +65,10 @@ def load_library() -> ctypes.CDLL:
             lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, FP, F,
                                            I, P]
             lib.la_decode_step.restype = I
+            lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
+            lib.la_causal_kernel.restype = I
+            lib.la_device_wait_timeouts.argtypes = [I]
+            lib.la_device_wait_timeouts.restype = I
             lib.la_status_string.argtypes = [I]
             lib.la_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -72,6 +77,22 @@ def load_library() -> ctypes.CDLL:
 
 def status_string(code: int) -> str:
     return load_library().la_status_string(int(code)).decode()
+
+
+def causal_kernel(B, H, N, D, Dv, gamma=None, dtype=torch.bfloat16) -> str:
+    """Which kernel a causal forward with these sizes runs: "tensor-core" or
+    "cuda-core" (host-only query)."""
+    code = load_library().la_causal_kernel(B, H, N, D, Dv, _gamma_arg(gamma, H),
+                                           _DTYPES[dtype])
+    if code < 0:
+        raise LinAttnError("la_causal_kernel", -code)
+    return "tensor-core" if code == 1 else "cuda-core"
+
+
+def device_wait_timeouts(reset: bool = False) -> int:
+    """Count of device-side bounded waits that gave up on the current device
+    (nonzero: some kernel abandoned its work).  Synchronise first."""
+    return int(load_library().la_device_wait_timeouts(1 if reset else 0))
 
 
 def _gamma_arg(gamma, H):

@@ -8,6 +8,7 @@
 
 #include "../../include/linattn.h"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 using namespace linattn;
 
@@ -60,6 +61,30 @@ la_status_t from_cuda(cudaError_t e) {
 }  // namespace
 
 extern "C" {
+
+int la_causal_kernel(int B, int H, int N, int D, int Dv, const float *gamma,
+                     la_dtype_t dtype) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return -static_cast<int>(st);
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return -static_cast<int>(st);
+  Problem p{nullptr, nullptr, nullptr, nullptr, B, H, N, D, Dv, decay, 0.f,
+            dtype == LA_F32 ? kF32 : kBF16};
+  return causal_tc_supported(p, g) ? 1 : 0;
+}
+
+int la_device_wait_timeouts(int reset) {
+  unsigned int *ctr = wait_timeout_counter();
+  if (!ctr) return -1;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, ctr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (reset) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(ctr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+  }
+  return static_cast<int>(v);
+}
 
 const char *la_status_string(la_status_t s) {
   switch (s) {

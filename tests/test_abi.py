@@ -35,7 +35,8 @@ def declared_symbols():
 def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_prefill_state", "la_decode_step",
-              "la_status_string"):
+              "la_status_string", "la_causal_kernel",
+              "la_device_wait_timeouts"):
         assert s in syms
 
 
@@ -121,3 +122,17 @@ def test_decode_rejects_bad_arguments(lib):
     assert call(D=100) == UNSUPPORTED
     assert call(g=(ctypes.c_float * 2)(1.0, -0.5)) == INVALID
     assert call(B=0, p=[None] * 6) == OK
+
+
+def test_causal_kernel_dispatch(lib):
+    K = lib.la_causal_kernel
+    g = lambda *x: (ctypes.c_float * len(x))(*x)  # noqa: E731
+    assert K(2, 16, 16384, 128, 128, None, BF16) == 1
+    assert K(4, 8, 4096, 64, 64, None, BF16) == 1
+    assert K(1, 2, 100, 64, 128, g(0.35, 1.0), BF16) == 1
+    assert K(1, 2, 100, 64, 128, g(0.34, 1.0), BF16) == 0   # strong decay
+    assert K(1, 2, 100, 64, 128, g(0.0, 1.0), BF16) == 0
+    assert K(1, 1, 256, 64, 64, None, F32) == 0             # fp32 inputs
+    assert K(1, 1, 256, 96, 64, None, BF16) == -UNSUPPORTED
+    assert K(1, 2, 256, 64, 64, g(1.5, 1.0), BF16) == -INVALID
+    assert K(256, 256, 1, 64, 64, None, BF16) == 0          # B*H > 65535

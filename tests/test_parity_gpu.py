@@ -38,8 +38,12 @@ def gen(B, H, N, D, Dv, dtype, seed, scale=0.5):
 def gammas_for(H, kind):
     if kind is None:
         return None
-    if kind == "mix":
+    if kind == "mix":    # includes decays too strong for the tensor-core path
         base = [0.0, 0.5, 0.9, 0.96875, 0.999, 1.0]
+        return torch.tensor([base[h % len(base)] for h in range(H)],
+                            dtype=torch.float32)
+    if kind == "mild":   # every decay inside the tensor-core envelope
+        base = [0.35, 0.75, 0.96875, 0.999, 1.0, 0.5]
         return torch.tensor([base[h % len(base)] for h in range(H)],
                             dtype=torch.float32)
     if kind == "retnet":
@@ -65,12 +69,16 @@ CAUSAL_SMALL = [
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16],
                          ids=["f32", "bf16"])
-@pytest.mark.parametrize("gkind", [None, "mix"])
+@pytest.mark.parametrize("gkind", [None, "mix", "mild"])
 @pytest.mark.parametrize("shape", CAUSAL_SMALL, ids=lambda s: "x".join(map(str, s)))
 def test_causal_small(la, ora, dtype, gkind, shape):
     B, H, N, D, Dv = shape
     q, k, v = gen(B, H, N, D, Dv, dtype, seed=N + D + 7 * H)
     g = gammas_for(H, gkind)
+    path = la.causal_kernel(B, H, N, D, Dv, gamma=g, dtype=dtype)
+    # "mix" always holds 0.0 for head 0, which sends the call to the CUDA cores
+    tc_expected = dtype == torch.bfloat16 and gkind != "mix"
+    assert path == ("tensor-core" if tc_expected else "cuda-core"), path
     o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
     torch.cuda.synchronize()
     ref = ora.causal(to_np(q), to_np(k), to_np(v),
@@ -286,3 +294,27 @@ def test_decode_bf16_h32_full(la, ora):
             assert err < 2e-2, (t, err)
     assert state_error(to_np(S[bs, hs]), Sr) < 1e-4
     assert state_error(to_np(z[bs, hs])[..., None], zr[..., None]) < 1e-4
+
+
+def test_tensor_core_and_cuda_core_paths_agree(la, ora):
+    """The same bf16 problem through both causal kernels (a strong decay on a
+    spare head forces the CUDA-core kernel) against the oracle."""
+    B, H, N, D, Dv = 1, 3, 777, 128, 128
+    q, k, v = gen(B, H, N, D, Dv, torch.bfloat16, 77)
+    g_tc = torch.tensor([0.9, 0.99, 1.0])
+    g_cc = torch.tensor([0.9, 0.99, 0.1])
+    assert la.causal_kernel(B, H, N, D, Dv, g_tc) == "tensor-core"
+    assert la.causal_kernel(B, H, N, D, Dv, g_cc) == "cuda-core"
+    o_tc = to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=g_tc))
+    o_cc = to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=g_cc))
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=g_tc.numpy())
+    for h in range(2):
+        assert max_row_error(o_tc[0, h], ref[0, h]) < 2e-2
+        assert max_row_error(o_cc[0, h], ref[0, h]) < 2e-2
+        assert max_row_error(o_tc[0, h], o_cc[0, h]) < 2e-2
+
+
+def test_zz_no_device_wait_timeouts(la):
+    """No tensor-core kernel gave up a bounded wait during this module."""
+    torch.cuda.synchronize()
+    assert la.device_wait_timeouts() == 0
