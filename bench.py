@@ -40,7 +40,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by workload, with the hash of the kernel source the
 # capture was taken on; reported only while that source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/causal_tc_decay_bf16_n16384.md: 402.853632 MB read + 111.215360
+    # MB written in one launch of the full workload
+    "causal_decay_bf16_n16384": {"bytes": 514068992, "source": "e9730703a2c826db"},
+}
 
 
 # ---------------------------------------------------------------------------
@@ -100,13 +104,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# sources the causal tensor-core kernel is compiled from
+KERNEL_SOURCES = ("causal_tc.cu", "tc_common.cuh", "common.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kernelized_sequence_mixing_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
