@@ -52,6 +52,8 @@
 #ifndef LINATTN_H
 #define LINATTN_H
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define LA_API __attribute__((visibility("default")))
 #else
@@ -136,6 +138,38 @@ LA_API int la_causal_kernel(int B, int H, int N, int D, int Dv,
  * Returns -1 if the counter cannot be read.
  */
 LA_API int la_device_wait_timeouts(int reset);
+
+/*
+ * Non-causal forward without any device allocation.  No counterpart on the
+ * pages: it computes exactly what la_forward(..., causal = 0, gamma = NULL,
+ * ...) computes, but keeps its scratch (per-head S, z and the partial sums of
+ * the split reduction) in a fixed array inside the library instead of taking
+ * a workspace with cudaMallocAsync.  For callers that cannot let a library
+ * allocate: applications that reserve device memory up front in their own
+ * allocator and forbid third-party allocations, and latency-critical loops
+ * where an allocation could stall or fail on a full memory pool.
+ *   - The scratch is la_forward_noncausal_static_limit() bytes (32 MiB) on
+ *     every GPU that loads the library, held until the process exits.  Calls
+ *     whose per-head state alone, B*H*(D*Dv + D)*4 bytes, exceeds it return
+ *     LA_ERR_UNSUPPORTED; below that the reduction uses as many sequence
+ *     splits as fit.
+ *   - The first call on each device queries the device address of the
+ *     scratch (one runtime call, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one scratch array.  Calls whose work
+ *     overlaps on the GPU (for example on two streams with no ordering
+ *     between them) race on it and corrupt each other's results: order them.
+ *     Each call writes every scratch word before reading it, so nothing needs
+ *     clearing between calls.
+ * Arguments, layouts and errors otherwise as la_forward (gamma is implicitly
+ * 1; D, Dv in {64, 128}).
+ */
+LA_API la_status_t la_forward_noncausal_static(const void *q, const void *k, const void *v,
+                                               void *o, int B, int H, int N, int D, int Dv,
+                                               float eps, la_dtype_t dtype, void *stream);
+
+/* Size in bytes of the per-device scratch used by la_forward_noncausal_static. */
+LA_API size_t la_forward_noncausal_static_limit(void);
 
 /* Static, NUL-terminated description of a status code. */
 LA_API const char *la_status_string(la_status_t s);

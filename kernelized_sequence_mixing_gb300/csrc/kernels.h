@@ -46,6 +46,12 @@ cudaError_t launch_kv_state(const void *k, const void *v, float *S, float *z,
                             int Dv, bool decay, const Gammas &g, Dtype dt,
                             cudaStream_t s);
 
+// The same reduction (no decay) with a caller-chosen number of splits
+// (partials [nsplit][BH][D*Dv + D] in `partials` when nsplit > 1).
+cudaError_t launch_kv_state_splits(const void *k, const void *v, float *S, float *z,
+                                   float *partials, int B, int H, int N, int D, int Dv,
+                                   int nsplit, const Gammas &g, Dtype dt, cudaStream_t s);
+
 // o = phi(q) S / (phi(q) . z + eps) for every row, S and z per (b, h).
 cudaError_t launch_noncausal_apply(const void *q, const float *S,
                                    const float *z, void *o, int BH, int N,

@@ -230,7 +230,48 @@ cudaError_t apply_shape(const void *q, const float *S, const float *z, void *o,
   return cudaErrorNotSupported;
 }
 
+template <int D, int DV, bool DECAY, typename T>
+cudaError_t kv_typed_n(const void *k, const void *v, float *S, float *z, float *part,
+                       int BH, int H, int N, int nsplit, int split_len, const Gammas &g,
+                       cudaStream_t s) {
+  const int64_t nS = (int64_t)BH * D * DV, nz = (int64_t)BH * D;
+  float *So = nsplit == 1 ? S : part;
+  float *zo = nsplit == 1 ? z : part + (int64_t)nsplit * nS;
+  dim3 grid((unsigned)BH, (unsigned)nsplit);
+  kv_partial_kernel<D, DV, DECAY, T><<<grid, kThreads, 0, s>>>(
+      static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N, split_len, g);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || nsplit == 1) return err;
+  kv_reduce_kernel<<<(unsigned)((nS + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+      part, S, nS, nsplit);
+  kv_reduce_kernel<<<(unsigned)((nz + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+      part + (int64_t)nsplit * nS, z, nz, nsplit);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t kv_shape_n(const void *k, const void *v, float *S, float *z, float *part,
+                       int BH, int H, int N, int D, int Dv, int nsplit, int split_len,
+                       const Gammas &g, cudaStream_t s) {
+  if (D == 64 && Dv == 64) return kv_typed_n<64, 64, false, T>(k, v, S, z, part, BH, H, N, nsplit, split_len, g, s);
+  if (D == 64 && Dv == 128) return kv_typed_n<64, 128, false, T>(k, v, S, z, part, BH, H, N, nsplit, split_len, g, s);
+  if (D == 128 && Dv == 64) return kv_typed_n<128, 64, false, T>(k, v, S, z, part, BH, H, N, nsplit, split_len, g, s);
+  if (D == 128 && Dv == 128) return kv_typed_n<128, 128, false, T>(k, v, S, z, part, BH, H, N, nsplit, split_len, g, s);
+  return cudaErrorNotSupported;
+}
+
 }  // namespace
+
+cudaError_t launch_kv_state_splits(const void *k, const void *v, float *S, float *z,
+                                   float *partials, int B, int H, int N, int D, int Dv,
+                                   int nsplit, const Gammas &g, Dtype dt, cudaStream_t s) {
+  const int BH = B * H;
+  if (nsplit < 1) return cudaErrorInvalidValue;
+  const int split_len = N > 0 ? (N + nsplit - 1) / nsplit : 1;
+  return dt == kF32
+             ? kv_shape_n<float>(k, v, S, z, partials, BH, H, N, D, Dv, nsplit, split_len, g, s)
+             : kv_shape_n<__nv_bfloat16>(k, v, S, z, partials, BH, H, N, D, Dv, nsplit, split_len, g, s);
+}
 
 int kv_state_num_splits(int BH, int N) {
   (void)BH;
