@@ -1,0 +1,863 @@
+// Sequence-parallel linear attention on tcgen05 tensor cores (sm_103a).
+//
+// Method: the recurrence of "Linear Attention Mechanisms" (dileepadev.github.io),
+// "Recurrent Reformulation", S_i = gamma S_(i-1) + phi(k_i) v_i^T,
+// z_i = gamma z_(i-1) + phi(k_i), o_i = phi(q_i)^T S_i / (phi(q_i) . z_i + eps),
+// with the fixed per-head decay gamma of its "Gating and Selective State
+// Updates" (RetNet) on both S and z, and phi = elu + 1.  The non-causal form
+// ("The Kernel Trick for Attention") is the same read-out with the sums taken
+// once over all tokens and gamma = 1.
+//
+// Work split.  The tokens of each (batch, head) are cut into P parts of whole
+// 64-token chunks; one CTA owns one part with the full D x Dv state, so the
+// grid has B*H*P CTAs and every SM gets work even when B*H is small.
+//
+//   phase A  (every part but the last): the part's own contribution
+//            T_p = sum_(s in part) gamma^(E_A - s) phi(k_s) [v_s | 1]^T,
+//            E_A = the part's last chunk-aligned position, accumulated in
+//            tensor memory by the MMA (M = D, N = Dv + 16, K = tokens).
+//   chain    the state before the part is the inclusive state of part p-1,
+//            published by the CTA that owns it; this CTA publishes
+//            incl_p = gamma^(e_p - E_A) T_p + gamma^len_p incl_(p-1).
+//            Parts are handed out in part-major order by an atomic ticket, so
+//            the owner of part p-1 has already started: every wait ends.
+//   phase C  the chunks of the part in order.  For a chunk at c0 inside a
+//            decay window ending at E (windows of W tokens from the part's
+//            start, W chosen so gamma^W stays far above the bf16 range limit):
+//              qh_t = gamma^(c0+t-E) phi(q_t),  kh_s = gamma^(E-c0-s) phi(k_s)
+//              A'   = qh kh^T                 (= gamma^(t-s) phi(q_t).phi(k_s))
+//              P    = A' masked to s <= t
+//              O    = qh [T | z] + P [V | 1]  (numerators and the normaliser)
+//              T   += kh^T [V | 1]
+//            where T (fp32, tensor memory) is the state scaled to the window
+//            end: T = sum_(s < c0) gamma^(E - s) phi(k_s) [v_s | 1].  Scaling
+//            q and k to the same reference point makes O exact without
+//            rescaling T per chunk; T is multiplied by gamma^W once per window.
+//            o_t = O[t, :Dv] / (O[t, Dv] + eps).
+//
+// Every term of the token-by-token recurrence appears once; the regrouping
+// changes only the order of summation and the rounding of the MMA operands
+// to bf16.  The same kernel also computes, by mode, the final state of a
+// prefill (phase A and chain only), the per-part sums of the non-causal form
+// (phase A only) and the non-causal read-out (phase C with the inter-chunk
+// product only).
+//
+// Warp roles (18 warps):
+//   0-3   P: A' -> masked bf16 P in shared memory
+//   4-7   state: chain, T initialisation, bf16 copy of [T | z] for the MMA,
+//         window rescaling (thread = row d of T)
+//   8-11  output: O -> o rows (divide by the normaliser)
+//   12-15 feature map: phi and the decay scale in place on the q, k tiles
+//   16    TMA producer (q, k, v tiles into a ring of stages)
+//   17    TMEM owner and MMA issuer
+// Every wait is bounded; a CTA that gives up counts the failure in device
+// memory, still publishes its chain flag (so no other CTA waits on it),
+// drains its in-flight copies and MMAs, frees tensor memory and exits.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace linattn {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;          // tokens per chunk
+constexpr int kThreads = 576;   // 18 warps
+constexpr int kSmemMax = 227 * 1024;
+constexpr int kBox = 8192;      // one TMA box: 64 rows x 128 bytes (64 bf16)
+constexpr float kGammaMin = 0.35f;
+constexpr float kLog2Floor = -93.0139f;  // log2(1e-28): smallest factor in a window
+
+constexpr int kWarpS = 4;
+constexpr int kWarpO = 8;
+constexpr int kWarpPhi = 12;
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;
+
+enum Mode : int { kCausal = 0, kPrefill = 1, kKvSum = 2, kApply = 3 };
+
+template <int D, int DV>
+struct Lay {
+  static constexpr int KB = D / 64, VB = DV / 64;
+  static constexpr int NA = DV + 16;  // columns of [V | 1], [T | z] and O
+  // stage: q boxes | k boxes (and a zero box when D = 64) | v boxes | ones box
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = KB * kBox;
+  static constexpr int kOffV = kOffK + 2 * kBox;
+  static constexpr int kOffOnes = kOffV + VB * kBox;
+  static constexpr int kStageBytes = kOffOnes + kBox;
+  static constexpr int kPBytes = kC * 128;
+  static constexpr int kSopAtom = D * 64;  // 32 columns of [T | z], 64-byte swizzle
+  static constexpr int kSopBytes = (DV / 32 + 1) * kSopAtom;
+  static constexpr int kNumBars = 3 * 4 + 12;
+  static constexpr int kFixed = kPBytes + kSopBytes + kNumBars * 8 + 64 + 1024;
+  static constexpr int kStages = (kSmemMax - kFixed) / kStageBytes >= 4 ? 4 : 3;
+  static constexpr int kOffP = kStages * kStageBytes;
+  static constexpr int kOffSop = kOffP + kPBytes;
+  static constexpr int kOffBar = kOffSop + kSopBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  // tensor memory columns (fp32): A' (M = 64), T (M = 128), O double buffer (M = 64)
+  static constexpr uint32_t kColA = 0, kColT = 64, kColO = 64 + NA;
+  static_assert(kColO + 2 * NA <= 512, "tensor memory");
+  static_assert(kAlloc <= kSmemMax, "shared memory");
+  static_assert(kStageBytes % 1024 == 0 && kOffP % 1024 == 0 && kOffSop % 1024 == 0, "align");
+};
+
+struct ChunkParams {
+  CUtensorMap tmQ, tmK, tmV;
+  __nv_bfloat16 *o;
+  float *ws_state;   // [B*H][P][D*Dv + D]: per-part states (S rows, then z)
+  int *ws_flag;      // [B*H][P]: 1 once the part's state is published
+  int *ws_ticket;    // part-major work counter (P > 1)
+  float *S_out, *z_out;  // prefill: final state
+  unsigned int *timeouts;
+  int BH, H, N, P, Psum;
+  float eps;
+  Gammas lg;         // log2(gamma) per head
+};
+
+// phi(x) = elu(x) + 1 on a pair of bf16 values, times a per-row scale:
+// exp(min(x, 0)) + max(x, 0), with exp(y) = 2^(y log2 e) on the packed bf16
+// exp2 unit.  log2 e is split into a bf16 head and tail so that the argument
+// carries one rounding only.
+__device__ __forceinline__ uint32_t phi_scale_bf16x2(uint32_t w, uint32_t scale2) {
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 l2e_hi = __float2bfloat162_rn(1.4453125f);
+  const __nv_bfloat162 l2e_lo = __float2bfloat162_rn(1.4426950408889634f - 1.4453125f);
+  const __nv_bfloat162 m = __hmin2(x, zero);
+  const __nv_bfloat162 a = __hfma2(m, l2e_hi, __hmul2(m, l2e_lo));
+  uint32_t au = *reinterpret_cast<const uint32_t *>(&a), eu;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(eu) : "r"(au));
+  const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162 *>(&eu);
+  __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+  r = __hmul2(r, *reinterpret_cast<const __nv_bfloat162 *>(&scale2));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// phi and the row scales in place on NB boxes of 64 rows x 128 bytes.  Thread
+// tp (0..127) handles the 16-byte chunks tp + 128 m of every box, which lie in
+// rows (tp / 8) + 16 m, m = 0..3.
+template <int NB>
+__device__ __forceinline__ void map_boxes(uint8_t *box0, const uint32_t sc[4], int tp) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    uint4 x[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) x[m] = reinterpret_cast<const uint4 *>(box0 + b * kBox)[tp + 128 * m];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      x[m].x = phi_scale_bf16x2(x[m].x, sc[m]);
+      x[m].y = phi_scale_bf16x2(x[m].y, sc[m]);
+      x[m].z = phi_scale_bf16x2(x[m].z, sc[m]);
+      x[m].w = phi_scale_bf16x2(x[m].w, sc[m]);
+      reinterpret_cast<uint4 *>(box0 + b * kBox)[tp + 128 * m] = x[m];
+    }
+  }
+}
+
+// Row d of [T | z] (fp32 values of 32 consecutive columns starting at column
+// 32 * atom) into the MN-major, 64-byte-swizzled bf16 operand.
+__device__ __forceinline__ void put_sop32(uint8_t *sop, int atom_bytes, int atom, int d,
+                                          const float *x) {
+  uint8_t *a = sop + atom * atom_bytes;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
+        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+}
+__device__ __forceinline__ void put_sop16(uint8_t *sop, int atom_bytes, int atom, int d,
+                                          const float *x) {
+  uint8_t *a = sop + atom * atom_bytes;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
+        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+}
+
+template <int D, int DV, int MODE, bool DECAY>
+__global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ ChunkParams p) {
+  using L = Lay<D, DV>;
+  constexpr int S = L::kStages;
+  constexpr int NA = L::NA;
+  constexpr bool kPhaseC = MODE == kCausal || MODE == kApply;
+  constexpr bool kChain = MODE == kCausal || MODE == kPrefill;
+  constexpr size_t kRec = static_cast<size_t>(D) * DV + D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+  uint64_t *full = bars, *mapped = bars + 4, *empty = bars + 8;
+  uint64_t *A_full = bars + 12, *A_free = bars + 13, *P_full = bars + 14;
+  uint64_t *T_ready = bars + 15, *T_free = bars + 16, *S_full = bars + 17, *S_free = bars + 18;
+  uint64_t *O_full = bars + 19, *O_free = bars + 21, *drain = bars + 23;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
+  int *item = reinterpret_cast<int *>(sm + L::kOffMisc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.BH, N = p.N, P = p.P;
+
+  // ---- set-up: work item, constant operand blocks, barriers, TMEM ----
+  if (tid == 0) {
+    int t = blockIdx.x;
+    if (kChain && P > 1) t = atomicAdd(p.ws_ticket, 1);
+    item[0] = t / BH;  // part (part-major order)
+    item[1] = t % BH;  // batch * head
+  }
+  {
+    // ones box of every stage: column 0 = 1 in each of the 64 rows; zero box
+    // after k when D = 64; P and [T | z] buffers zero.
+    for (int i = tid; i < S * kBox / 16; i += kThreads) {
+      const int st = i / (kBox / 16), j = i % (kBox / 16);
+      uint8_t *ones = sm + st * L::kStageBytes + L::kOffOnes;
+      reinterpret_cast<uint4 *>(ones)[j] = make_uint4(0, 0, 0, 0);
+      if (D == 64)
+        reinterpret_cast<uint4 *>(sm + st * L::kStageBytes + L::kOffK + kBox)[j] =
+            make_uint4(0, 0, 0, 0);
+    }
+    uint4 *z4 = reinterpret_cast<uint4 *>(sm + L::kOffP);
+    for (int i = tid; i < (L::kPBytes + L::kSopBytes) / 16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  if (tid < S * kC) {
+    const int st = tid / kC, r = tid % kC;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + st * L::kStageBytes + L::kOffOnes + sw128_off(r, 0)) =
+        __float2bfloat16_rn(1.f);
+  }
+  if (tid == 32 * kWarpTma) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&mapped[i], 4);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(A_full, 1);
+    mbar_init(A_free, 4);
+    mbar_init(P_full, 4);
+    mbar_init(T_ready, 1);
+    mbar_init(T_free, 4);
+    mbar_init(S_full, 4);
+    mbar_init(S_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&O_full[b], 1);
+      mbar_init(&O_free[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int part = item[0], bh = item[1];
+
+  // the part: chunks [cb, cb + nch) of this (batch, head)
+  const int nch_all = (N + kC - 1) / kC;
+  const int pbase = nch_all / P, prem = nch_all % P;
+  const int cb = part * pbase + min(part, prem);
+  const int nch = pbase + (part < prem ? 1 : 0);
+  const int len = min(N, (cb + nch) * kC) - cb * kC;
+  const bool hasA = MODE == kPrefill || MODE == kKvSum || (MODE == kCausal && part < P - 1);
+  const bool needPrev = kChain && part > 0;
+  const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
+  int WC = 64;  // chunks per decay window
+  if (DECAY && lg < 0.f) {
+    const float c = kLog2Floor / lg / 64.f;
+    WC = c < 1.f ? 1 : (c > 64.f ? 64 : static_cast<int>(c));
+  }
+  const int W = kC * WC;
+
+  if (warp == kWarpTma) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&p.tmK);
+      prefetch_tmap(&p.tmV);
+      if (kPhaseC) prefetch_tmap(&p.tmQ);
+    }
+    const int nA = hasA ? nch : 0, nC = kPhaseC ? nch : 0;
+    int s = 0, issued = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nA + nC; ++it) {
+      if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.timeouts)) break;
+      if (lane == 0) {
+        const bool phaseA = it < nA;
+        const int row = (cb + (phaseA ? it : it - nA)) * kC;
+        const bool wq = !phaseA, wkv = phaseA || MODE != kApply;
+        uint8_t *st = sm + s * L::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], (wq ? L::KB * kBox : 0) + (wkv ? (L::KB + L::VB) * kBox : 0));
+        if (wq)
+#pragma unroll
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(st + L::kOffQ + kb * kBox, &p.tmQ, kb * 64, row, bh, &full[s]);
+        if (wkv) {
+#pragma unroll
+          for (int kb = 0; kb < L::KB; ++kb)
+            tma_load_3d(st + L::kOffK + kb * kBox, &p.tmK, kb * 64, row, bh, &full[s]);
+#pragma unroll
+          for (int vb = 0; vb < L::VB; ++vb)
+            tma_load_3d(st + L::kOffV + vb * kBox, &p.tmV, vb * 64, row, bh, &full[s]);
+        }
+      }
+      __syncwarp();
+      issued = it + 1;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    if (*abort_flag && lane == 0) {  // let every issued copy land before the CTA exits
+      for (int c = issued > S ? issued - S : 0; c < issued; ++c)
+        mbar_wait_drain(&full[c % S], (c / S) & 1);
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer (warp-wide loop, lane 0 issues) ----------------
+    const bool leader = lane == 0;
+    constexpr uint32_t ID_A = idesc_bf16(64, 64, false, false);
+    constexpr uint32_t ID_DS = idesc_bf16(128, NA, true, true);
+    constexpr uint32_t ID_O = idesc_bf16(64, NA, false, true);
+    constexpr uint64_t kStageU = L::kStageBytes >> 4;
+    const uint32_t base = smem_u32(sm);
+    // q, k: K-major (K = d); kh^T: MN-major (M = d, K = tokens); [V | 1]:
+    // MN-major (N = value column, K = tokens); P: K-major; [T | z]: MN-major
+    // (N = value column, K = d).  Variants differ in the start address only.
+    const uint64_t dq0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
+    const uint64_t dk0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
+    const uint64_t dkt0 = smem_desc(base + L::kOffK, kBox, 1024, kSw128);
+    const uint64_t dv0 = smem_desc(base + L::kOffV, kBox, 1024, kSw128);
+    const uint64_t dp0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
+    const uint64_t dsop0 = smem_desc(base + L::kOffSop, L::kSopAtom, 512, kSw64);
+    const uint32_t tA = tmem + L::kColA, tT = tmem + L::kColT;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    // phase A: T = kh^T [V | 1] over the part
+    for (int i = 0; hasA && i < nch; ++i) {
+      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t so = static_cast<uint64_t>(s) * kStageU;
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    if (ok && hasA) {
+      if (leader) mma_commit(T_ready);
+      __syncwarp();
+    }
+    // phase C
+    for (int i = 0; ok && kPhaseC && i < nch; ++i) {
+      const int b = i & 1;
+      const uint32_t u = static_cast<uint32_t>(i >> 1);
+      const uint64_t so = static_cast<uint64_t>(s) * kStageU;
+      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) break;
+      if (MODE == kCausal) {
+        // A' = qh kh^T  (M 64 tokens t, N 64 tokens s, K = D)
+        if (!warp_wait(A_free, (i & 1) ^ 1, abort_flag, p.timeouts)) break;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = so + (kk >> 2) * (kBox >> 4) + (kk & 3) * 2;
+            mma_bf16(tA, dq0 + off, dk0 + off, ID_A, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(A_full);
+        }
+        __syncwarp();
+        // T += kh^T [V | 1]: not needed after the last chunk
+        if (i + 1 < nch) {
+          if (!warp_wait(T_free, i & 1, abort_flag, p.timeouts)) break;
+          tc_fence_after();
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk)
+              mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, 1u);
+            mma_commit(T_ready);
+          }
+          __syncwarp();
+        }
+      }
+      // O = qh [T | z]  (M 64, N Dv + 16, K = D)
+      if (!warp_wait(&O_free[b], (u & 1) ^ 1, abort_flag, p.timeouts)) break;
+      if (!warp_wait(S_full, MODE == kApply ? 0u : static_cast<uint32_t>(i & 1), abort_flag,
+                     p.timeouts))
+        break;
+      tc_fence_after();
+      const uint32_t tO = tmem + L::kColO + b * NA;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(tO, dq0 + so + (kk >> 2) * (kBox >> 4) + (kk & 3) * 2, dsop0 + kk * 64, ID_O,
+                   kk > 0 ? 1u : 0u);
+        if (MODE == kCausal) mma_commit(S_free);
+      }
+      __syncwarp();
+      if (MODE == kCausal) {
+        // O += P [V | 1]  (M 64, N Dv + 16, K 64 tokens)
+        if (!warp_wait(P_full, i & 1, abort_flag, p.timeouts)) break;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk) mma_bf16(tO, dp0 + kk * 2, dv0 + so + kk * 128, ID_O, 1u);
+        }
+      }
+      if (leader) {
+        mma_commit(&O_full[b]);
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    // every MMA issued has completed before TMEM is released
+    if (leader) {
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kWarpPhi) {
+    // ---------------- feature map and decay scales, in place ----------------
+    const int tp = tid - kWarpPhi * 32;
+    const int r0 = tp >> 3;
+    const int nA = hasA ? nch : 0, nC = kPhaseC ? nch : 0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nA + nC; ++it) {
+      if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
+      const bool phaseA = it < nA;
+      const int i = phaseA ? it : it - nA;
+      const int nv = min(kC, N - (cb + i) * kC);
+      uint8_t *st = sm + s * L::kStageBytes;
+      if (phaseA || MODE != kApply) {
+        // kh_s = gamma^(E - s) phi(k_s); rows past the sequence end are zero
+        const int e0 = phaseA ? kC * nch - 1 - kC * i : W - 1 - kC * (i % WC);
+        uint32_t sc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int t = r0 + 16 * m;
+          float f = DECAY ? exp2f(static_cast<float>(e0 - t) * lg) : 1.f;
+          if (t >= nv) f = 0.f;
+          sc[m] = pack_bf16x2(f, f);
+        }
+        map_boxes<L::KB>(st + L::kOffK, sc, tp);
+      }
+      if (!phaseA) {
+        // qh_t = gamma^(t - E) phi(q_t)
+        const int e0 = kC * (i % WC) - (W - 1);
+        uint32_t sc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float f = DECAY ? exp2f(static_cast<float>(e0 + r0 + 16 * m) * lg) : 1.f;
+          sc[m] = pack_bf16x2(f, f);
+        }
+        map_boxes<L::KB>(st + L::kOffQ, sc, tp);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mapped[s]);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  } else if (warp >= kWarpO) {
+    // ---------------- output rows ----------------
+    const int w = warp - kWarpO;  // TMEM lane quadrant
+    const int t = 16 * w + lane;  // M = 64 layout: rows 16w..16w+15 in lanes 0..15
+    for (int i = 0; kPhaseC && i < nch; ++i) {
+      const int b = i & 1;
+      const uint32_t u = static_cast<uint32_t>(i >> 1);
+      if (!warp_wait(&O_full[b], u & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      const uint32_t tO = tmem_addr(tmem, 32 * w, L::kColO + b * NA);
+      const int nv = min(kC, N - (cb + i) * kC);
+      const bool row_ok = lane < 16 && t < nv;
+      __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + (cb + i) * kC + t) * DV;
+      float x[64], dz[16];
+      tmem_ld16(tO + DV, dz);
+      tmem_ld32(tO, x);
+      tmem_ld32(tO + 32, x + 32);
+      tmem_wait_ld();
+      const float inv = 1.f / (dz[0] + p.eps);
+      if (DV == 64) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&O_free[b]);
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<uint4 *>(orow)[q] = make_uint4(
+              pack_bf16x2(x[8 * q + 0] * inv, x[8 * q + 1] * inv), pack_bf16x2(x[8 * q + 2] * inv, x[8 * q + 3] * inv),
+              pack_bf16x2(x[8 * q + 4] * inv, x[8 * q + 5] * inv), pack_bf16x2(x[8 * q + 6] * inv, x[8 * q + 7] * inv));
+      }
+      if (DV == 128) {
+        tmem_ld32(tO + 64, x);
+        tmem_ld32(tO + 96, x + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&O_free[b]);
+        if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<uint4 *>(orow + 64)[q] = make_uint4(
+                pack_bf16x2(x[8 * q + 0] * inv, x[8 * q + 1] * inv), pack_bf16x2(x[8 * q + 2] * inv, x[8 * q + 3] * inv),
+                pack_bf16x2(x[8 * q + 4] * inv, x[8 * q + 5] * inv), pack_bf16x2(x[8 * q + 6] * inv, x[8 * q + 7] * inv));
+        }
+      }
+    }
+  } else if (warp >= kWarpS) {
+    // ---------------- state: thread d owns row d of T ----------------
+    const int w = warp - kWarpS;
+    const int ts = tid - kWarpS * 32;  // 0..127
+    const int d = 32 * w + lane;
+    const bool act = d < D;
+    const uint32_t tT = tmem_addr(tmem, 32 * w, L::kColT);
+    uint8_t *sop = sm + L::kOffSop;
+    constexpr int kAtom = L::kSopAtom;
+    if (MODE == kApply) {
+      // [S | z] = sum of the per-part sums, as the bf16 operand
+      const float *rec0 = p.ws_state + static_cast<size_t>(bh) * p.Psum * kRec;
+      if (act) {
+#pragma unroll 1
+        for (int cc = 0; cc < DV / 32; ++cc) {
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          for (int j = 0; j < p.Psum; ++j) {
+            const float4 *src = reinterpret_cast<const float4 *>(rec0 + j * kRec + d * DV + 32 * cc);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 v4 = __ldcg(src + q);
+              acc[4 * q] += v4.x;
+              acc[4 * q + 1] += v4.y;
+              acc[4 * q + 2] += v4.z;
+              acc[4 * q + 3] += v4.w;
+            }
+          }
+          put_sop32(sop, kAtom, cc, d, acc);
+        }
+        float zz[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zz[e] = 0.f;
+        for (int j = 0; j < p.Psum; ++j) zz[0] += __ldcg(rec0 + j * kRec + D * DV + d);
+        put_sop16(sop, kAtom, DV / 32, d, zz);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(S_full);
+    } else {
+      // chain: incl_p = corr T_p + gamma^len incl_(p-1); T = gamma^W incl_(p-1)
+      const bool publish = MODE == kKvSum || MODE == kPrefill || (MODE == kCausal && part < P - 1);
+      const bool last_prefill = MODE == kPrefill && part == P - 1;
+      if (hasA) {
+        warp_wait(T_ready, 0, abort_flag, p.timeouts);
+        tc_fence_after();
+      }
+      const float *prev = needPrev ? p.ws_state + (static_cast<size_t>(bh) * P + part - 1) * kRec : nullptr;
+      float *dstS = last_prefill ? p.S_out + static_cast<size_t>(bh) * D * DV
+                                 : p.ws_state + (static_cast<size_t>(bh) * P + part) * kRec;
+      float *dstz = last_prefill ? p.z_out + static_cast<size_t>(bh) * D : dstS + D * DV;
+      if (needPrev) {
+        if (ts == 0) {
+          const int *f = p.ws_flag + bh * P + part - 1;
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(f) == 0) {
+            if (*abort_flag) break;
+            if (clock64() - t0 > kWaitCycles) {
+              *abort_flag = 1;
+              atomicAdd(p.timeouts, 1u);
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        named_sync(1, 128);
+      }
+      const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+      const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
+      const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+#pragma unroll 1
+      for (int cc = 0; cc < DV / 32; ++cc) {
+        float tv[32], sp[32];
+        if (hasA) tmem_ld32(tT + 32 * cc, tv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (needPrev && act) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * DV + 32 * cc) + q);
+          sp[4 * q] = v4.x;
+          sp[4 * q + 1] = v4.y;
+          sp[4 * q + 2] = v4.z;
+          sp[4 * q + 3] = v4.w;
+        }
+        if (hasA) tmem_wait_ld();
+        if (publish && act) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 r;
+            r.x = hasA ? fmaf(corr, tv[4 * q], gLen * sp[4 * q]) : gLen * sp[4 * q];
+            r.y = hasA ? fmaf(corr, tv[4 * q + 1], gLen * sp[4 * q + 1]) : gLen * sp[4 * q + 1];
+            r.z = hasA ? fmaf(corr, tv[4 * q + 2], gLen * sp[4 * q + 2]) : gLen * sp[4 * q + 2];
+            r.w = hasA ? fmaf(corr, tv[4 * q + 3], gLen * sp[4 * q + 3]) : gLen * sp[4 * q + 3];
+            reinterpret_cast<float4 *>(dstS + d * DV + 32 * cc)[q] = r;
+          }
+        }
+        if (kPhaseC) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sp[e] *= gW;
+          tmem_st32(tT + 32 * cc, sp);
+          if (act) put_sop32(sop, kAtom, cc, d, sp);
+        }
+      }
+      {
+        float tv[16], sp[16];
+        if (hasA) {
+          tmem_ld16(tT + DV, tv);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sp[e] = 0.f;
+        if (needPrev && act) sp[0] = __ldcg(prev + D * DV + d);
+        if (publish && act) dstz[d] = hasA ? fmaf(corr, tv[0], gLen * sp[0]) : gLen * sp[0];
+        if (kPhaseC) {
+          sp[0] *= gW;
+          tmem_st16(tT + DV, sp);
+          if (act) put_sop16(sop, kAtom, DV / 32, d, sp);
+        }
+      }
+      if (publish && !last_prefill && MODE != kKvSum) {
+        // the state is visible device-wide before the flag
+        named_sync(1, 128);
+        if (ts == 0) {
+          __threadfence();
+          st_release_gpu(p.ws_flag + bh * P + part, 1);
+        }
+      }
+      if (kPhaseC) {
+        tmem_wait_st();
+        tc_fence_before();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(T_free);
+          mbar_arrive(S_full);
+        }
+        // per chunk: after T += kh^T [V | 1] of chunk i-1, publish bf16 [T | z]
+        // for chunk i (rescaled when chunk i opens a new decay window)
+        for (int i = 1; i < nch; ++i) {
+          if (!warp_wait(T_ready, static_cast<uint32_t>((i - 1 + (hasA ? 1 : 0)) & 1), abort_flag,
+                         p.timeouts))
+            break;
+          tc_fence_after();
+          const bool rebase = DECAY && (i % WC == 0);
+          if (!warp_wait(S_free, static_cast<uint32_t>((i - 1) & 1), abort_flag, p.timeouts)) break;
+#pragma unroll 1
+          for (int cc = 0; cc < DV / 32; cc += 2) {
+            float x0[32], x1[32];
+            tmem_ld32(tT + 32 * cc, x0);
+            tmem_ld32(tT + 32 * cc + 32, x1);
+            tmem_wait_ld();
+            if (rebase) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                x0[e] *= gW;
+                x1[e] *= gW;
+              }
+              tmem_st32(tT + 32 * cc, x0);
+              tmem_st32(tT + 32 * cc + 32, x1);
+            }
+            if (act) {
+              put_sop32(sop, kAtom, cc, d, x0);
+              put_sop32(sop, kAtom, cc + 1, d, x1);
+            }
+          }
+          {
+            float x0[16];
+            tmem_ld16(tT + DV, x0);
+            tmem_wait_ld();
+            if (rebase) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) x0[e] *= gW;
+              tmem_st16(tT + DV, x0);
+            }
+            if (act) put_sop16(sop, kAtom, DV / 32, d, x0);
+          }
+          if (rebase) tmem_wait_st();
+          tc_fence_before();
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(T_free);
+            mbar_arrive(S_full);
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------- P = A' masked to s <= t, bf16, 128-byte swizzled ----------------
+    const int w = warp;  // TMEM lane quadrant
+    const int t = 16 * w + lane;
+    for (int i = 0; MODE == kCausal && i < nch; ++i) {
+      if (!warp_wait(A_full, i & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      float a[64];
+      tmem_ld32(tmem_addr(tmem, 32 * w, L::kColA), a);
+      if (w >= 2) tmem_ld32(tmem_addr(tmem, 32 * w, L::kColA + 32), a + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(A_free);
+      // P of the previous chunk has been consumed by its MMA
+      if (i > 0 && !warp_wait(&O_full[(i - 1) & 1], static_cast<uint32_t>(((i - 1) >> 1) & 1),
+                              abort_flag, p.timeouts))
+        break;
+      if (lane < 16) {
+        uint8_t *prow = sm + L::kOffP;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (8 * j <= t) {  // chunks wholly above the diagonal stay zero
+            uint32_t wv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int s0 = 8 * j + 2 * q;
+              wv[q] = pack_bf16x2(s0 <= t ? a[s0] : 0.f, s0 + 1 <= t ? a[s0 + 1] : 0.f);
+            }
+            *reinterpret_cast<uint4 *>(prow + sw128_off(t, 16 * j)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(P_full);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+template <int D, int DV, int MODE, bool DECAY>
+cudaError_t launch_typed(const ChunkParams &prm, int grid, cudaStream_t s) {
+  auto kern = chunk_tc_kernel<D, DV, MODE, DECAY>;
+  const int smem = Lay<D, DV>::kAlloc;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kThreads, smem, s>>>(prm);
+  return cudaGetLastError();
+}
+
+template <int MODE, bool DECAY>
+cudaError_t launch_dims(const ChunkParams &prm, int D, int DV, int grid, cudaStream_t s) {
+  if (D == 64)
+    return DV == 64 ? launch_typed<64, 64, MODE, DECAY>(prm, grid, s)
+                    : launch_typed<64, 128, MODE, DECAY>(prm, grid, s);
+  return DV == 64 ? launch_typed<128, 64, MODE, DECAY>(prm, grid, s)
+                  : launch_typed<128, 128, MODE, DECAY>(prm, grid, s);
+}
+
+int num_sms() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
+}
+
+bool dims_ok(int D, int Dv) { return (D == 64 || D == 128) && (Dv == 64 || Dv == 128); }
+
+bool setup_params(ChunkParams *prm, const void *q, const void *k, const void *v, int BH, int N,
+                  int D, int Dv, int H, const Gammas &g, bool decay) {
+  if (q && !make_tmap_3d_bf16(&prm->tmQ, q, D, N, BH, 64, kC, 128)) return false;
+  if (k && !make_tmap_3d_bf16(&prm->tmK, k, D, N, BH, 64, kC, 128)) return false;
+  if (v && !make_tmap_3d_bf16(&prm->tmV, v, Dv, N, BH, 64, kC, 128)) return false;
+  if (!q) prm->tmQ = prm->tmK;
+  prm->timeouts = wait_timeout_counter();
+  if (!prm->timeouts) return false;
+  prm->BH = BH;
+  prm->H = H;
+  prm->N = N;
+  for (int h = 0; h < kMaxHeads; ++h)
+    prm->lg.g[h] = (decay && h < H) ? static_cast<float>(log2(static_cast<double>(g.g[h]))) : 0.f;
+  return true;
+}
+
+}  // namespace
+
+int chunk_parts(int BH, int N) {
+  const int nch = (N + kC - 1) / kC;
+  if (BH <= 0 || nch <= 0) return 1;
+  const int target = 4 * num_sms();
+  int P = (target + BH - 1) / BH;
+  if (P > nch) P = nch;
+  return P < 1 ? 1 : P;
+}
+
+size_t chunk_workspace_bytes(int BH, int P, int D, int Dv) {
+  if (P <= 1) return 0;
+  const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
+  const size_t flags16 = (flags + 255) & ~static_cast<size_t>(255);
+  return flags16 + sizeof(float) * static_cast<size_t>(BH) * P * (static_cast<size_t>(D) * Dv + D);
+}
+
+bool chunk_tc_supported(const Problem &p, const Gammas &g) {
+  if (p.dtype != kBF16 || !dims_ok(p.D, p.Dv) || p.N <= 0) return false;
+  const long long rows = static_cast<long long>(p.B) * p.H;
+  if (rows <= 0 || rows * chunk_parts(static_cast<int>(rows), p.N) >= (1LL << 31)) return false;
+  if (p.decay)
+    for (int h = 0; h < p.H; ++h)
+      if (!(g.g[h] >= kGammaMin)) return false;
+  return true;
+}
+
+cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int P, cudaStream_t s) {
+  if (!chunk_tc_supported(p, g)) return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  ChunkParams prm = {};
+  if (!setup_params(&prm, p.q, p.k, p.v, BH, p.N, p.D, p.Dv, p.H, g, p.decay))
+    return cudaErrorNotSupported;
+  prm.o = static_cast<__nv_bfloat16 *>(p.o);
+  prm.P = P;
+  prm.Psum = 1;
+  prm.eps = p.eps;
+  if (P > 1) {
+    if (!ws) return cudaErrorInvalidValue;
+    const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
+    prm.ws_flag = static_cast<int *>(ws);
+    prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;
+    prm.ws_state = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((flags + 255) & ~static_cast<size_t>(255)));
+    cudaError_t e = cudaMemsetAsync(ws, 0, flags, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = BH * P;
+  return p.decay ? launch_dims<kCausal, true>(prm, p.D, p.Dv, grid, s)
+                 : launch_dims<kCausal, false>(prm, p.D, p.Dv, grid, s);
+}
+
+}  // namespace linattn

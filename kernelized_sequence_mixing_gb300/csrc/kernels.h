@@ -35,6 +35,17 @@ bool causal_tc_supported(const Problem &p, const Gammas &g);
 cudaError_t launch_causal_tc(const Problem &p, const Gammas &g,
                              cudaStream_t s);
 
+// Sequence-parallel chunked kernels on tcgen05 tensor cores (bf16 operands,
+// fp32 state).  chunk_tc_supported() gives the envelope (bf16, D and Dv in
+// {64, 128}, every decay >= 0.35); chunk_parts() the number of parts per
+// (batch, head) and chunk_workspace_bytes() the device workspace the causal
+// launcher needs for that many parts (0 for one part).
+bool chunk_tc_supported(const Problem &p, const Gammas &g);
+int chunk_parts(int BH, int N);
+size_t chunk_workspace_bytes(int BH, int P, int D, int Dv);
+cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int P,
+                                cudaStream_t s);
+
 // Split-N reduction of S = sum_j w_j phi(k_j) v_j^T and z = sum_j w_j
 // phi(k_j) with w_j = gamma^(N-1-j): partials [nsplit][BH][D*Dv + D] in
 // `partials` (fp32) unless nsplit == 1, in which case S, z are written

@@ -71,7 +71,7 @@ int la_causal_kernel(int B, int H, int N, int D, int Dv, const float *gamma,
   if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return -static_cast<int>(st);
   Problem p{nullptr, nullptr, nullptr, nullptr, B, H, N, D, Dv, decay, 0.f,
             dtype == LA_F32 ? kF32 : kBF16};
-  return causal_tc_supported(p, g) ? 1 : 0;
+  return chunk_tc_supported(p, g) ? 1 : 0;
 }
 
 int la_device_wait_timeouts(int reset) {
@@ -120,16 +120,24 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Problem p{q, k, v, o, B, H, N, D, Dv, decay, eps,
             dtype == LA_F32 ? kF32 : kBF16};
+  const int BH = B * H;
   if (causal) {
-    if (p.dtype == kBF16) {
-      cudaError_t e = launch_causal_tc(p, g, s);
-      if (e != cudaErrorNotSupported) return from_cuda(e);
+    if (chunk_tc_supported(p, g)) {
+      // parts of the sequence run on separate SMs; the workspace carries the
+      // state from one part to the next
+      const int P = chunk_parts(BH, N);
+      const size_t wsb = chunk_workspace_bytes(BH, P, D, Dv);
+      void *ws = nullptr;
+      if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
+      cudaError_t e = launch_causal_chunk(p, g, ws, P, s);
+      cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+      if (e != cudaSuccess) return from_cuda(e);
+      return from_cuda(ef);
     }
     return from_cuda(launch_causal_simt(p, g, s));
   }
   // Non-causal: reduce S, z per (b, h) into a stream-ordered workspace, then
   // apply them to every query.
-  const int BH = B * H;
   const size_t state_bytes = sizeof(float) * (size_t)BH * ((size_t)D * Dv + D);
   const size_t part_bytes = kv_state_workspace_bytes(BH, N, D, Dv);
   void *ws = nullptr;

@@ -135,4 +135,4 @@ def test_causal_kernel_dispatch(lib):
     assert K(1, 1, 256, 64, 64, None, F32) == 0             # fp32 inputs
     assert K(1, 1, 256, 96, 64, None, BF16) == -UNSUPPORTED
     assert K(1, 2, 256, 64, 64, g(1.5, 1.0), BF16) == -INVALID
-    assert K(256, 256, 1, 64, 64, None, BF16) == 0          # B*H > 65535
+    assert K(256, 256, 1, 64, 64, None, BF16) == 1          # one-dimensional grid

@@ -87,6 +87,31 @@ def test_causal_small(la, ora, dtype, gkind, shape):
     assert err < TOL[dtype], err
 
 
+# The tensor-core path cuts each (batch, head) into parts and rescales its
+# state once per decay window.  Many heads give one part per head and windows
+# of one chunk (gamma = 0.35 / 0.5) or several chunks (0.9, 0.99); 200 heads
+# give four parts of ten chunks each, so the state crosses parts and windows.
+CAUSAL_PARTS = [
+    # (B, H, N, D, Dv, gammas)
+    (8, 76, 700, 64, 64, [0.35, 0.5, 0.9, 0.99]),
+    (2, 100, 2560, 64, 64, [0.5, 0.9, 0.99, 1.0]),
+    (1, 40, 1500, 128, 128, [0.6, 0.97, 1.0, 0.85]),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL_PARTS, ids=lambda c: "x".join(map(str, c[:5])))
+def test_causal_parts_and_windows(la, ora, case):
+    B, H, N, D, Dv, gl = case
+    q, k, v = gen(B, H, N, D, Dv, torch.bfloat16, seed=H + N)
+    g = torch.tensor([gl[h % len(gl)] for h in range(H)], dtype=torch.float32)
+    assert la.causal_kernel(B, H, N, D, Dv, gamma=g, dtype=torch.bfloat16) == "tensor-core"
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=g.numpy(), eps=1e-6)
+    err = max_row_error(to_np(o), ref)
+    assert err < 2e-2, err
+
+
 def test_causal_f32_n256_full(la, ora):
     """fp32, gamma = 1, B1 H1 N256 D=Dv=64, N(0,1) from seed 0."""
     from kernelized_sequence_mixing_gb300.workloads import (WORKLOADS,
