@@ -9,21 +9,25 @@
 // once over all tokens and gamma = 1.
 //
 // Work split.  The tokens of each (batch, head) are cut into P parts of whole
-// 64-token chunks; one CTA owns one part with the full D x Dv state, so the
-// grid has B*H*P CTAs and every SM gets work even when B*H is small.
+// 64-token chunks so that B*H*P CTAs keep every SM busy even when B*H is
+// small; one CTA owns one part with the full D x Dv state.
 //
-//   phase A  (every part but the last): the part's own contribution
-//            T_p = sum_(s in part) gamma^(E_A - s) phi(k_s) [v_s | 1]^T,
-//            E_A = the part's last chunk-aligned position, accumulated in
-//            tensor memory by the MMA (M = D, N = Dv + 16, K = tokens).
-//   chain    the state before the part is the inclusive state of part p-1,
-//            published by the CTA that owns it; this CTA publishes
-//            incl_p = gamma^(e_p - E_A) T_p + gamma^len_p incl_(p-1).
-//            Parts are handed out in part-major order by an atomic ticket, so
-//            the owner of part p-1 has already started: every wait ends.
-//   phase C  the chunks of the part in order.  For a chunk at c0 inside a
-//            decay window ending at E (windows of W tokens from the part's
-//            start, W chosen so gamma^W stays far above the bf16 range limit):
+//   phase A  the part's own contribution to the state, summed in tensor
+//            memory (M = D, N = Dv + 16, K = tokens; the operand phi(k) times
+//            its decay factor is split into two bf16 numbers, so the sum
+//            carries about 16 significant bits),
+//              A_p = sum_(s in part) gamma^(e_p - s) phi(k_s) [v_s | 1]^T,
+//            e_p = the part's last token.
+//   causal mode (one kernel): every part but the last runs phase A, then
+//            takes the inclusive state of part p-1 from the CTA that owns it
+//            (a flag in device memory) and publishes its own,
+//              incl_p = A_p + gamma^len_p incl_(p-1);
+//            parts are handed out in part-major order by an atomic ticket, so
+//            the owner of part p-1 has already started and every wait ends.
+//            Then phase C runs the part's chunks in order from incl_(p-1).
+//            For a chunk at c0 inside a decay window ending at E (windows of
+//            W tokens from the part's start, W chosen so gamma^W stays far
+//            above the bf16 range limit):
 //              qh_t = gamma^(c0+t-E) phi(q_t),  kh_s = gamma^(E-c0-s) phi(k_s)
 //              A'   = qh kh^T                 (= gamma^(t-s) phi(q_t).phi(k_s))
 //              P    = A' masked to s <= t
@@ -32,27 +36,30 @@
 //            where T (fp32, tensor memory) is the state scaled to the window
 //            end: T = sum_(s < c0) gamma^(E - s) phi(k_s) [v_s | 1].  Scaling
 //            q and k to the same reference point makes O exact without
-//            rescaling T per chunk; T is multiplied by gamma^W once per window.
-//            o_t = O[t, :Dv] / (O[t, Dv] + eps).
+//            rescaling T per chunk; T is multiplied by gamma^W once per
+//            window.  o_t = O[t, :Dv] / (O[t, Dv] + eps).
+//   state mode: phase A only, A_p stored for a scan over the parts
+//            (part_scan.cu): the final state of a prefill, or (gamma = 1) the
+//            sums of the non-causal form.
+//   apply mode: phase C with the inter-chunk product only, O = phi(q) [S | z],
+//            for the non-causal read-out.
 //
 // Every term of the token-by-token recurrence appears once; the regrouping
 // changes only the order of summation and the rounding of the MMA operands
-// to bf16.  The same kernel also computes, by mode, the final state of a
-// prefill (phase A and chain only), the per-part sums of the non-causal form
-// (phase A only) and the non-causal read-out (phase C with the inter-chunk
-// product only).
+// to bf16.
 //
 // Warp roles (18 warps):
 //   0-3   P: A' -> masked bf16 P in shared memory
-//   4-7   state: chain, T initialisation, bf16 copy of [T | z] for the MMA,
-//         window rescaling (thread = row d of T)
+//   4-7   state: the chain, T from the previous part's state, bf16 copy of
+//         [T | z] for the MMA, window rescaling, the part's sum in state mode
+//         (thread = row d of T)
 //   8-11  output: O -> o rows (divide by the normaliser)
 //   12-15 feature map: phi and the decay scale in place on the q, k tiles
+//         (in phase A, warps 0-15 share this work)
 //   16    TMA producer (q, k, v tiles into a ring of stages)
 //   17    TMEM owner and MMA issuer
 // Every wait is bounded; a CTA that gives up counts the failure in device
-// memory, still publishes its chain flag (so no other CTA waits on it),
-// drains its in-flight copies and MMAs, frees tensor memory and exits.
+// memory, drains its in-flight copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -75,33 +82,43 @@ constexpr int kWarpPhi = 12;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 
-enum Mode : int { kCausal = 0, kPrefill = 1, kKvSum = 2, kApply = 3 };
+enum Mode : int { kCausal = 0, kState = 1, kApply = 2 };
+constexpr int kMaxStages = 6;
 
-template <int D, int DV>
+template <int D, int DV, bool STATE>
 struct Lay {
   static constexpr int KB = D / 64, VB = DV / 64;
   static constexpr int NA = DV + 16;  // columns of [V | 1], [T | z] and O
-  // stage: q boxes | k boxes (and a zero box when D = 64) | v boxes | ones box
+  // stage: q boxes (not in state mode) | k boxes (and a zero box when
+  // D = 64) | state mode: the low bf16 parts of kh, same shape | v boxes |
+  // ones box
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = KB * kBox;
-  static constexpr int kOffV = kOffK + 2 * kBox;
+  static constexpr int kOffK = STATE ? 0 : KB * kBox;
+  // low parts of kh in the state sums: own boxes in state mode, the (then
+  // unused) q boxes in the first phase of the causal mode; the second
+  // 64-row atom of that operand is a zero box when D = 64
+  static constexpr int kOffKlo = STATE ? 2 * kBox : kOffQ;
+  static constexpr int kLboLo = (!STATE && D == 64) ? 2 * kBox : kBox;
+  static constexpr int kOffV = kOffK + (STATE ? 4 : 2) * kBox;
   static constexpr int kOffOnes = kOffV + VB * kBox;
   static constexpr int kStageBytes = kOffOnes + kBox;
-  static constexpr int kPBytes = kC * 128;
+  static constexpr int kPBytes = STATE ? 0 : kC * 128;
   static constexpr int kSopAtom = D * 64;  // 32 columns of [T | z], 64-byte swizzle
-  static constexpr int kSopBytes = (DV / 32 + 1) * kSopAtom;
-  static constexpr int kNumBars = 3 * 4 + 12;
+  static constexpr int kSopBytes = STATE ? 0 : (DV / 32 + 1) * kSopAtom;
+  static constexpr int kNumBars = 3 * kMaxStages + 12;
   static constexpr int kFixed = kPBytes + kSopBytes + kNumBars * 8 + 64 + 1024;
-  static constexpr int kStages = (kSmemMax - kFixed) / kStageBytes >= 4 ? 4 : 3;
+  static constexpr int kFit = (kSmemMax - kFixed) / kStageBytes;
+  static constexpr int kStages = kFit > kMaxStages ? kMaxStages : kFit;
   static constexpr int kOffP = kStages * kStageBytes;
   static constexpr int kOffSop = kOffP + kPBytes;
   static constexpr int kOffBar = kOffSop + kSopBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 64;
+  static constexpr int kBytes = kOffMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   // tensor memory columns (fp32): A' (M = 64), T (M = 128), O double buffer (M = 64)
   static constexpr uint32_t kColA = 0, kColT = 64, kColO = 64 + NA;
   static_assert(kColO + 2 * NA <= 512, "tensor memory");
+  static_assert(kStages >= 3, "stages");
   static_assert(kAlloc <= kSmemMax, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kOffP % 1024 == 0 && kOffSop % 1024 == 0, "align");
 };
@@ -109,14 +126,16 @@ struct Lay {
 struct ChunkParams {
   CUtensorMap tmQ, tmK, tmV;
   __nv_bfloat16 *o;
-  float *ws_state;   // [B*H][P][D*Dv + D]: per-part states (S rows, then z)
-  int *ws_flag;      // [B*H][P]: 1 once the part's state is published
-  int *ws_ticket;    // part-major work counter (P > 1)
-  float *S_out, *z_out;  // prefill: final state
+  // per-part records [B*H][rec_parts][D*Dv + D] (S rows, then z): state mode
+  // writes A_p; causal mode the inclusive states incl_p; apply mode reads
+  // the sum in slot 0 of its (batch, head)
+  float *rec;
+  int *ws_flag;    // causal, P > 1: [B*H][P], 1 once incl_p is published
+  int *ws_ticket;  // causal, P > 1: part-major work counter
   unsigned int *timeouts;
-  int BH, H, N, P, Psum;
+  int BH, H, N, P, rec_parts;
   float eps;
-  Gammas lg;         // log2(gamma) per head
+  Gammas lg;  // log2(gamma) per head
 };
 
 // phi(x) = elu(x) + 1 on a pair of bf16 values, times a per-row scale:
@@ -159,6 +178,38 @@ __device__ __forceinline__ void map_boxes(uint8_t *box0, const uint32_t sc[4], i
   }
 }
 
+// The same in fp32, leaving each value as the sum of two bf16 numbers: the
+// rounded value in place and the rounding error in the matching position of
+// lo0, so that an MMA pair over both carries about 16 significant bits.  Here
+// 512 threads share the boxes: thread tp handles chunk tp of every box, all
+// in row tp / 8, with the row scale sc.
+template <int NB>
+__device__ __forceinline__ void map_boxes_split(uint8_t *box0, uint8_t *lo0, float sc, int tp) {
+  uint4 x[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) x[b] = reinterpret_cast<const uint4 *>(box0 + b * kBox)[tp];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    {
+      uint32_t w[4] = {x[b].x, x[b].y, x[b].z, x[b].w}, hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float a = __uint_as_float(h ? (w[k] & 0xffff0000u) : (w[k] << 16));
+          v[h] = (__expf(fminf(a, 0.f)) + fmaxf(a, 0.f)) * sc;
+        }
+        hi[k] = pack_bf16x2(v[0], v[1]);
+        const float h0 = __uint_as_float(hi[k] << 16), h1 = __uint_as_float(hi[k] & 0xffff0000u);
+        lo[k] = pack_bf16x2(v[0] - h0, v[1] - h1);
+      }
+      reinterpret_cast<uint4 *>(box0 + b * kBox)[tp] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      reinterpret_cast<uint4 *>(lo0 + b * kBox)[tp] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+}
+
 // Row d of [T | z] (fp32 values of 32 consecutive columns starting at column
 // 32 * atom) into the MN-major, 64-byte-swizzled bf16 operand.
 __device__ __forceinline__ void put_sop32(uint8_t *sop, int atom_bytes, int atom, int d,
@@ -182,20 +233,19 @@ __device__ __forceinline__ void put_sop16(uint8_t *sop, int atom_bytes, int atom
 
 template <int D, int DV, int MODE, bool DECAY>
 __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ ChunkParams p) {
-  using L = Lay<D, DV>;
+  using L = Lay<D, DV, MODE == kState>;
   constexpr int S = L::kStages;
   constexpr int NA = L::NA;
   constexpr bool kPhaseC = MODE == kCausal || MODE == kApply;
-  constexpr bool kChain = MODE == kCausal || MODE == kPrefill;
   constexpr size_t kRec = static_cast<size_t>(D) * DV + D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-  uint64_t *full = bars, *mapped = bars + 4, *empty = bars + 8;
-  uint64_t *A_full = bars + 12, *A_free = bars + 13, *P_full = bars + 14;
-  uint64_t *T_ready = bars + 15, *T_free = bars + 16, *S_full = bars + 17, *S_free = bars + 18;
-  uint64_t *O_full = bars + 19, *O_free = bars + 21, *drain = bars + 23;
+  uint64_t *full = bars, *mapped = bars + kMaxStages, *empty = bars + 2 * kMaxStages;
+  uint64_t *A_full = bars + 3 * kMaxStages, *A_free = A_full + 1, *P_full = A_full + 2;
+  uint64_t *T_ready = A_full + 3, *T_free = A_full + 4, *S_full = A_full + 5, *S_free = A_full + 6;
+  uint64_t *O_full = A_full + 7, *O_free = A_full + 9, *drain = A_full + 11;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
   int *item = reinterpret_cast<int *>(sm + L::kOffMisc + 8);
@@ -204,9 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   const int BH = p.BH, N = p.N, P = p.P;
 
   // ---- set-up: work item, constant operand blocks, barriers, TMEM ----
+  const int prun = static_cast<int>(gridDim.x) / BH;  // parts run per (batch, head)
   if (tid == 0) {
-    int t = blockIdx.x;
-    if (kChain && P > 1) t = atomicAdd(p.ws_ticket, 1);
+    int t = static_cast<int>(blockIdx.x);
+    if (MODE == kCausal && P > 1) t = atomicAdd(p.ws_ticket, 1);
     item[0] = t / BH;  // part (part-major order)
     item[1] = t % BH;  // batch * head
   }
@@ -217,9 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       const int st = i / (kBox / 16), j = i % (kBox / 16);
       uint8_t *ones = sm + st * L::kStageBytes + L::kOffOnes;
       reinterpret_cast<uint4 *>(ones)[j] = make_uint4(0, 0, 0, 0);
-      if (D == 64)
+      if (D == 64) {
         reinterpret_cast<uint4 *>(sm + st * L::kStageBytes + L::kOffK + kBox)[j] =
             make_uint4(0, 0, 0, 0);
+        if (MODE == kState)
+          reinterpret_cast<uint4 *>(sm + st * L::kStageBytes + L::kOffKlo + kBox)[j] =
+              make_uint4(0, 0, 0, 0);
+      }
     }
     uint4 *z4 = reinterpret_cast<uint4 *>(sm + L::kOffP);
     for (int i = tid; i < (L::kPBytes + L::kSopBytes) / 16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
@@ -231,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         __float2bfloat16_rn(1.f);
   }
   if (tid == 32 * kWarpTma) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&mapped[i], 4);
+      mbar_init(&mapped[i], 16);
       mbar_init(&empty[i], 1);
     }
     mbar_init(A_full, 1);
@@ -265,8 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   const int cb = part * pbase + min(part, prem);
   const int nch = pbase + (part < prem ? 1 : 0);
   const int len = min(N, (cb + nch) * kC) - cb * kC;
-  const bool hasA = MODE == kPrefill || MODE == kKvSum || (MODE == kCausal && part < P - 1);
-  const bool needPrev = kChain && part > 0;
+  const bool hasA = MODE == kState || (MODE == kCausal && part < P - 1);
+  const bool needPrev = MODE == kCausal && part > 0;
+  (void)prun;
   const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
   int WC = 64;  // chunks per decay window
   if (DECAY && lg < 0.f) {
@@ -274,6 +330,134 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     WC = c < 1.f ? 1 : (c > 64.f ? 64 : static_cast<int>(c));
   }
   const int W = kC * WC;
+
+  // phase A feature map, kh_s = gamma^(e_p - s) phi(k_s).  State mode: warps
+  // 0-15, thread tp maps row tp / 8 of every k box in fp32, split into bf16
+  // high and low parts (low parts to the boxes at kOffKlo).  Causal mode: the
+  // four feature-map warps, bf16 (tp = 0..127, rows tp / 8 + 16 m).
+  auto phase_a_map = [&](int tp) {
+    int s = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < nch; ++i) {
+      if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
+      const int nv = min(kC, N - (cb + i) * kC);
+      uint8_t *st = sm + s * L::kStageBytes;
+      const int e0 = kC * nch - 1 - kC * i;
+      if (MODE == kState) {
+        const int row = tp >> 3;
+        float f = DECAY ? exp2f(static_cast<float>(e0 - row) * lg) : 1.f;
+        if (row >= nv) f = 0.f;
+        map_boxes_split<L::KB>(st + L::kOffK, st + L::kOffKlo, f, tp);
+      } else {
+        uint32_t sc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int t = (tp >> 3) + 16 * m;
+          float f = DECAY ? exp2f(static_cast<float>(e0 - t) * lg) : 1.f;
+          if (t >= nv) f = 0.f;
+          sc[m] = pack_bf16x2(f, f);
+        }
+        map_boxes<L::KB>(st + L::kOffK, sc, tp);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(&mapped[s], MODE == kState ? 1 : 4);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  };
+
+  // Causal mode, before phase C, run by the state warps (columns
+  // [0, Dv/2)) and the output warps (columns [Dv/2, Dv) and z) together:
+  // S0 = incl_(p-1) (0 for the first part); incl_p = A_p + gamma^len_p S0 is
+  // published for the next part unless this is the last; T = gamma^W S0 goes
+  // to tensor memory and, in bf16, to the [T | z] operand.  Thread c of the
+  // 256 handles row d = 32 w + lane.
+  auto chain_part = [&](int w, int cc0, int cc1, bool with_z, int c) {
+    const int d = 32 * w + lane;
+    const bool act = d < D;
+    const uint32_t tT = tmem_addr(tmem, 32 * w, L::kColT);
+    uint8_t *sop = sm + L::kOffSop;
+    const bool pub = part < P - 1;
+    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+    const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
+    const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+    if (hasA) {
+      warp_wait(T_ready, 0, abort_flag, p.timeouts);
+      tc_fence_after();
+    }
+    if (needPrev) {
+      if (c == 0) {
+        const int *f = p.ws_flag + bh * P + part - 1;
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(f) == 0) {
+          if (*abort_flag) break;
+          if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicAdd(p.timeouts, 1u);
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      named_sync(1, 256);
+    }
+    const float *prev = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
+    float *dst = p.rec + (static_cast<size_t>(bh) * P + part) * kRec;
+#pragma unroll 1
+    for (int cc = cc0; cc < cc1; ++cc) {
+      float x[32], t[32];
+      if (hasA) tmem_ld32(tT + 32 * cc, t);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (needPrev && act) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * DV + 32 * cc) + q);
+        x[4 * q] = v4.x;
+        x[4 * q + 1] = v4.y;
+        x[4 * q + 2] = v4.z;
+        x[4 * q + 3] = v4.w;
+      }
+      if (hasA) tmem_wait_ld();
+      if (pub && act) {
+        float4 *o4 = reinterpret_cast<float4 *>(dst + d * DV + 32 * cc);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o4[q] = make_float4(fmaf(gLen, x[4 * q], hasA ? corr * t[4 * q] : 0.f),
+                              fmaf(gLen, x[4 * q + 1], hasA ? corr * t[4 * q + 1] : 0.f),
+                              fmaf(gLen, x[4 * q + 2], hasA ? corr * t[4 * q + 2] : 0.f),
+                              fmaf(gLen, x[4 * q + 3], hasA ? corr * t[4 * q + 3] : 0.f));
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] *= gW;
+      tmem_st32(tT + 32 * cc, x);
+      if (act) put_sop32(sop, L::kSopAtom, cc, d, x);
+    }
+    if (with_z) {
+      float sp[16], tz[16];
+      if (hasA) {
+        tmem_ld16(tT + DV, tz);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sp[e] = 0.f;
+      if (needPrev && act) sp[0] = __ldcg(prev + D * DV + d);
+      if (pub && act) dst[D * DV + d] = fmaf(gLen, sp[0], hasA ? corr * tz[0] : 0.f);
+      sp[0] *= gW;
+      tmem_st16(tT + DV, sp);
+      if (act) put_sop16(sop, L::kSopAtom, DV / 32, d, sp);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    fence_async_smem();
+    named_sync(1, 256);
+    if (pub && c == 0) {
+      // the state is visible device-wide before the flag
+      __threadfence();
+      st_release_gpu(p.ws_flag + bh * P + part, 1);
+    }
+  };
 
   if (warp == kWarpTma) {
     // ---------------- TMA producer ----------------
@@ -331,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     const uint64_t dq0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
     const uint64_t dk0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
     const uint64_t dkt0 = smem_desc(base + L::kOffK, kBox, 1024, kSw128);
+    const uint64_t dktlo0 = smem_desc(base + L::kOffKlo, L::kLboLo, 1024, kSw128);
     const uint64_t dv0 = smem_desc(base + L::kOffV, kBox, 1024, kSw128);
     const uint64_t dp0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
     const uint64_t dsop0 = smem_desc(base + L::kOffSop, L::kSopAtom, 512, kSw64);
@@ -348,8 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (leader) {
         const uint64_t so = static_cast<uint64_t>(s) * kStageU;
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk)
+        for (int kk = 0; kk < kC / 16; ++kk) {
           mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
+          if (MODE == kState) mma_bf16(tT, dktlo0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, 1u);
+        }
         mma_commit(&empty[s]);
       }
       __syncwarp();
@@ -362,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (leader) mma_commit(T_ready);
       __syncwarp();
     }
-    // phase C
+    // phase C: per chunk A', [dS | dz], inter-chunk and, once P is ready,
+    // intra-chunk MMAs
     for (int i = 0; ok && kPhaseC && i < nch; ++i) {
       const int b = i & 1;
       const uint32_t u = static_cast<uint32_t>(i >> 1);
@@ -436,20 +624,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     __syncwarp();
   } else if (warp >= kWarpPhi) {
     // ---------------- feature map and decay scales, in place ----------------
+    // phase A (warps 0-15, see below) comes first; this loop is phase C
     const int tp = tid - kWarpPhi * 32;
     const int r0 = tp >> 3;
-    const int nA = hasA ? nch : 0, nC = kPhaseC ? nch : 0;
-    int s = 0;
-    uint32_t ph = 0;
-    for (int it = 0; it < nA + nC; ++it) {
+    if (hasA) phase_a_map(MODE == kState ? tid : tp);
+    int s = (hasA ? nch : 0) % S;
+    uint32_t ph = static_cast<uint32_t>(((hasA ? nch : 0) / S) & 1);
+    for (int i = 0; kPhaseC && i < nch; ++i) {
       if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
-      const bool phaseA = it < nA;
-      const int i = phaseA ? it : it - nA;
       const int nv = min(kC, N - (cb + i) * kC);
       uint8_t *st = sm + s * L::kStageBytes;
-      if (phaseA || MODE != kApply) {
+      if (MODE != kApply) {
         // kh_s = gamma^(E - s) phi(k_s); rows past the sequence end are zero
-        const int e0 = phaseA ? kC * nch - 1 - kC * i : W - 1 - kC * (i % WC);
+        const int e0 = W - 1 - kC * (i % WC);
         uint32_t sc[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -460,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         }
         map_boxes<L::KB>(st + L::kOffK, sc, tp);
       }
-      if (!phaseA) {
+      {
         // qh_t = gamma^(t - E) phi(q_t)
         const int e0 = kC * (i % WC) - (W - 1);
         uint32_t sc[4];
@@ -473,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&mapped[s]);
+      if (lane == 0) mbar_arrive_cnt(&mapped[s], 4);
       if (++s == S) {
         s = 0;
         ph ^= 1;
@@ -481,7 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     }
   } else if (warp >= kWarpO) {
     // ---------------- output rows ----------------
+    if (MODE == kState) phase_a_map(tid);
     const int w = warp - kWarpO;  // TMEM lane quadrant
+    if (MODE == kCausal) chain_part(w, DV / 64, DV / 32, true, 128 + tid - kWarpO * 32);
     const int t = 16 * w + lane;  // M = 64 layout: rows 16w..16w+15 in lanes 0..15
     for (int i = 0; kPhaseC && i < nch; ++i) {
       const int b = i & 1;
@@ -501,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (DV == 64) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&O_free[b]);
+        if (lane == 0) mbar_arrive_relaxed(&O_free[b]);
       }
       if (row_ok) {
 #pragma unroll
@@ -516,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&O_free[b]);
+        if (lane == 0) mbar_arrive_relaxed(&O_free[b]);
         if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -529,136 +718,70 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   } else if (warp >= kWarpS) {
     // ---------------- state: thread d owns row d of T ----------------
     const int w = warp - kWarpS;
-    const int ts = tid - kWarpS * 32;  // 0..127
     const int d = 32 * w + lane;
     const bool act = d < D;
     const uint32_t tT = tmem_addr(tmem, 32 * w, L::kColT);
     uint8_t *sop = sm + L::kOffSop;
     constexpr int kAtom = L::kSopAtom;
+    if (MODE == kState) phase_a_map(tid);
     if (MODE == kApply) {
-      // [S | z] = sum of the per-part sums, as the bf16 operand
-      const float *rec0 = p.ws_state + static_cast<size_t>(bh) * p.Psum * kRec;
+      // [S | z] (the sum over all tokens, slot 0 of this (batch, head)) as the bf16 operand
+      const float *r0 = p.rec + static_cast<size_t>(bh) * p.rec_parts * kRec;
       if (act) {
 #pragma unroll 1
         for (int cc = 0; cc < DV / 32; ++cc) {
-          float acc[32];
+          float x[32];
+          const float4 *src = reinterpret_cast<const float4 *>(r0 + d * DV + 32 * cc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-          for (int j = 0; j < p.Psum; ++j) {
-            const float4 *src = reinterpret_cast<const float4 *>(rec0 + j * kRec + d * DV + 32 * cc);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 v4 = __ldcg(src + q);
-              acc[4 * q] += v4.x;
-              acc[4 * q + 1] += v4.y;
-              acc[4 * q + 2] += v4.z;
-              acc[4 * q + 3] += v4.w;
-            }
+          for (int q = 0; q < 8; ++q) {
+            const float4 v4 = __ldcg(src + q);
+            x[4 * q] = v4.x;
+            x[4 * q + 1] = v4.y;
+            x[4 * q + 2] = v4.z;
+            x[4 * q + 3] = v4.w;
           }
-          put_sop32(sop, kAtom, cc, d, acc);
+          put_sop32(sop, kAtom, cc, d, x);
         }
         float zz[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) zz[e] = 0.f;
-        for (int j = 0; j < p.Psum; ++j) zz[0] += __ldcg(rec0 + j * kRec + D * DV + d);
+        zz[0] = __ldcg(r0 + D * DV + d);
         put_sop16(sop, kAtom, DV / 32, d, zz);
       }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(S_full);
-    } else {
-      // chain: incl_p = corr T_p + gamma^len incl_(p-1); T = gamma^W incl_(p-1)
-      const bool publish = MODE == kKvSum || MODE == kPrefill || (MODE == kCausal && part < P - 1);
-      const bool last_prefill = MODE == kPrefill && part == P - 1;
-      if (hasA) {
-        warp_wait(T_ready, 0, abort_flag, p.timeouts);
-        tc_fence_after();
-      }
-      const float *prev = needPrev ? p.ws_state + (static_cast<size_t>(bh) * P + part - 1) * kRec : nullptr;
-      float *dstS = last_prefill ? p.S_out + static_cast<size_t>(bh) * D * DV
-                                 : p.ws_state + (static_cast<size_t>(bh) * P + part) * kRec;
-      float *dstz = last_prefill ? p.z_out + static_cast<size_t>(bh) * D : dstS + D * DV;
-      if (needPrev) {
-        if (ts == 0) {
-          const int *f = p.ws_flag + bh * P + part - 1;
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(f) == 0) {
-            if (*abort_flag) break;
-            if (clock64() - t0 > kWaitCycles) {
-              *abort_flag = 1;
-              atomicAdd(p.timeouts, 1u);
-              break;
-            }
-            __nanosleep(64);
-          }
-        }
-        named_sync(1, 128);
-      }
-      const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
-      const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
+    } else if (MODE == kState) {
+      // A_p = gamma^(e_p - E) T: T is scaled to the chunk-aligned end E of
+      // the part; e_p = its last token (they differ only for a ragged end)
       const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+      warp_wait(T_ready, 0, abort_flag, p.timeouts);
+      tc_fence_after();
+      float *aS = p.rec + (static_cast<size_t>(bh) * p.rec_parts + part) * kRec;
 #pragma unroll 1
-      for (int cc = 0; cc < DV / 32; ++cc) {
-        float tv[32], sp[32];
-        if (hasA) tmem_ld32(tT + 32 * cc, tv);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (needPrev && act) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * DV + 32 * cc) + q);
-          sp[4 * q] = v4.x;
-          sp[4 * q + 1] = v4.y;
-          sp[4 * q + 2] = v4.z;
-          sp[4 * q + 3] = v4.w;
-        }
-        if (hasA) tmem_wait_ld();
-        if (publish && act) {
+      for (int cc = 0; cc < DV / 32; cc += 2) {
+        float x0[32], x1[32];
+        tmem_ld32(tT + 32 * cc, x0);
+        tmem_ld32(tT + 32 * cc + 32, x1);
+        tmem_wait_ld();
+        if (act) {
+          float4 *dst = reinterpret_cast<float4 *>(aS + d * DV + 32 * cc);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            float4 r;
-            r.x = hasA ? fmaf(corr, tv[4 * q], gLen * sp[4 * q]) : gLen * sp[4 * q];
-            r.y = hasA ? fmaf(corr, tv[4 * q + 1], gLen * sp[4 * q + 1]) : gLen * sp[4 * q + 1];
-            r.z = hasA ? fmaf(corr, tv[4 * q + 2], gLen * sp[4 * q + 2]) : gLen * sp[4 * q + 2];
-            r.w = hasA ? fmaf(corr, tv[4 * q + 3], gLen * sp[4 * q + 3]) : gLen * sp[4 * q + 3];
-            reinterpret_cast<float4 *>(dstS + d * DV + 32 * cc)[q] = r;
+            dst[q] = make_float4(corr * x0[4 * q], corr * x0[4 * q + 1], corr * x0[4 * q + 2], corr * x0[4 * q + 3]);
+            dst[8 + q] = make_float4(corr * x1[4 * q], corr * x1[4 * q + 1], corr * x1[4 * q + 2], corr * x1[4 * q + 3]);
           }
         }
-        if (kPhaseC) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sp[e] *= gW;
-          tmem_st32(tT + 32 * cc, sp);
-          if (act) put_sop32(sop, kAtom, cc, d, sp);
-        }
       }
-      {
-        float tv[16], sp[16];
-        if (hasA) {
-          tmem_ld16(tT + DV, tv);
-          tmem_wait_ld();
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sp[e] = 0.f;
-        if (needPrev && act) sp[0] = __ldcg(prev + D * DV + d);
-        if (publish && act) dstz[d] = hasA ? fmaf(corr, tv[0], gLen * sp[0]) : gLen * sp[0];
-        if (kPhaseC) {
-          sp[0] *= gW;
-          tmem_st16(tT + DV, sp);
-          if (act) put_sop16(sop, kAtom, DV / 32, d, sp);
-        }
-      }
-      if (publish && !last_prefill && MODE != kKvSum) {
-        // the state is visible device-wide before the flag
-        named_sync(1, 128);
-        if (ts == 0) {
-          __threadfence();
-          st_release_gpu(p.ws_flag + bh * P + part, 1);
-        }
-      }
+      float tz[16];
+      tmem_ld16(tT + DV, tz);
+      tmem_wait_ld();
+      if (act) aS[D * DV + d] = corr * tz[0];
+    } else {
+      chain_part(w, 0, DV / 64, false, tid - kWarpS * 32);
+      const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
       if (kPhaseC) {
-        tmem_wait_st();
-        tc_fence_before();
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        if (lane == 0) {  // both warp groups of the chain are done (chain_part)
           mbar_arrive(T_free);
           mbar_arrive(S_full);
         }
@@ -715,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     }
   } else {
     // ---------------- P = A' masked to s <= t, bf16, 128-byte swizzled ----------------
+    if (MODE == kState) phase_a_map(tid);
     const int w = warp;  // TMEM lane quadrant
     const int t = 16 * w + lane;
     for (int i = 0; MODE == kCausal && i < nch; ++i) {
@@ -726,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(A_free);
+      if (lane == 0) mbar_arrive_relaxed(A_free);
       // P of the previous chunk has been consumed by its MMA
       if (i > 0 && !warp_wait(&O_full[(i - 1) & 1], static_cast<uint32_t>(((i - 1) >> 1) & 1),
                               abort_flag, p.timeouts))
@@ -762,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
 template <int D, int DV, int MODE, bool DECAY>
 cudaError_t launch_typed(const ChunkParams &prm, int grid, cudaStream_t s) {
   auto kern = chunk_tc_kernel<D, DV, MODE, DECAY>;
-  const int smem = Lay<D, DV>::kAlloc;
+  const int smem = Lay<D, DV, MODE == kState>::kAlloc;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, smem, s>>>(prm);
@@ -776,6 +900,12 @@ cudaError_t launch_dims(const ChunkParams &prm, int D, int DV, int grid, cudaStr
                     : launch_typed<64, 128, MODE, DECAY>(prm, grid, s);
   return DV == 64 ? launch_typed<128, 64, MODE, DECAY>(prm, grid, s)
                   : launch_typed<128, 128, MODE, DECAY>(prm, grid, s);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const ChunkParams &prm, bool decay, int D, int DV, int grid, cudaStream_t s) {
+  return decay ? launch_dims<MODE, true>(prm, D, DV, grid, s)
+               : launch_dims<MODE, false>(prm, D, DV, grid, s);
 }
 
 int num_sms() {
@@ -795,20 +925,26 @@ bool dims_ok(int D, int Dv) { return (D == 64 || D == 128) && (Dv == 64 || Dv ==
 bool setup_params(ChunkParams *prm, const void *q, const void *k, const void *v, int BH, int N,
                   int D, int Dv, int H, const Gammas &g, bool decay) {
   if (q && !make_tmap_3d_bf16(&prm->tmQ, q, D, N, BH, 64, kC, 128)) return false;
-  if (k && !make_tmap_3d_bf16(&prm->tmK, k, D, N, BH, 64, kC, 128)) return false;
-  if (v && !make_tmap_3d_bf16(&prm->tmV, v, Dv, N, BH, 64, kC, 128)) return false;
+  if (!make_tmap_3d_bf16(&prm->tmK, k, D, N, BH, 64, kC, 128)) return false;
+  if (!make_tmap_3d_bf16(&prm->tmV, v, Dv, N, BH, 64, kC, 128)) return false;
   if (!q) prm->tmQ = prm->tmK;
   prm->timeouts = wait_timeout_counter();
   if (!prm->timeouts) return false;
   prm->BH = BH;
   prm->H = H;
   prm->N = N;
-  for (int h = 0; h < kMaxHeads; ++h)
-    prm->lg.g[h] = (decay && h < H) ? static_cast<float>(log2(static_cast<double>(g.g[h]))) : 0.f;
+  prm->lg = log2_gammas(g, H, decay);
   return true;
 }
 
 }  // namespace
+
+Gammas log2_gammas(const Gammas &g, int H, bool decay) {
+  Gammas lg;
+  for (int h = 0; h < kMaxHeads; ++h)
+    lg.g[h] = (decay && h < H) ? static_cast<float>(log2(static_cast<double>(g.g[h]))) : 0.f;
+  return lg;
+}
 
 int chunk_parts(int BH, int N) {
   const int nch = (N + kC - 1) / kC;
@@ -820,10 +956,18 @@ int chunk_parts(int BH, int N) {
 }
 
 size_t chunk_workspace_bytes(int BH, int P, int D, int Dv) {
-  if (P <= 1) return 0;
+  return sizeof(float) * static_cast<size_t>(BH) * P * (static_cast<size_t>(D) * Dv + D);
+}
+
+namespace {
+size_t causal_flag_bytes(int BH, int P) {
   const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
-  const size_t flags16 = (flags + 255) & ~static_cast<size_t>(255);
-  return flags16 + sizeof(float) * static_cast<size_t>(BH) * P * (static_cast<size_t>(D) * Dv + D);
+  return (flags + 255) & ~static_cast<size_t>(255);
+}
+}  // namespace
+
+size_t chunk_causal_workspace_bytes(int BH, int P, int D, int Dv) {
+  return P <= 1 ? 0 : causal_flag_bytes(BH, P) + chunk_workspace_bytes(BH, P, D, Dv);
 }
 
 bool chunk_tc_supported(const Problem &p, const Gammas &g) {
@@ -844,20 +988,56 @@ cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int
     return cudaErrorNotSupported;
   prm.o = static_cast<__nv_bfloat16 *>(p.o);
   prm.P = P;
-  prm.Psum = 1;
+  prm.rec_parts = P;
   prm.eps = p.eps;
   if (P > 1) {
     if (!ws) return cudaErrorInvalidValue;
-    const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
+    // flags and ticket start at zero; the records need no initialisation
+    const size_t fb = causal_flag_bytes(BH, P);
     prm.ws_flag = static_cast<int *>(ws);
     prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;
-    prm.ws_state = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ((flags + 255) & ~static_cast<size_t>(255)));
-    cudaError_t e = cudaMemsetAsync(ws, 0, flags, s);
+    prm.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + fb);
+    cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  const int grid = BH * P;
-  return p.decay ? launch_dims<kCausal, true>(prm, p.D, p.Dv, grid, s)
-                 : launch_dims<kCausal, false>(prm, p.D, p.Dv, grid, s);
+  return launch_mode<kCausal>(prm, p.decay, p.D, p.Dv, BH * P, s);
+}
+
+cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
+                                 int N, int D, int Dv, bool decay, const Gammas &g, void *ws,
+                                 int P, cudaStream_t s) {
+  const Problem pr{nullptr, k, v, nullptr, B, H, N, D, Dv, decay, 0.f, kBF16};
+  if (!chunk_tc_supported(pr, g) || !ws) return cudaErrorNotSupported;
+  const int BH = B * H;
+  ChunkParams prm = {};
+  if (!setup_params(&prm, nullptr, k, v, BH, N, D, Dv, H, g, decay)) return cudaErrorNotSupported;
+  prm.P = P;
+  prm.rec_parts = P;
+  prm.rec = static_cast<float *>(ws);
+  cudaError_t e = launch_mode<kState>(prm, decay, D, Dv, BH * P, s);
+  if (e != cudaSuccess) return e;
+  return launch_part_scan(prm.rec, BH, H, P, N, D, Dv, prm.lg, kScanFinal, S, z, s);
+}
+
+cudaError_t launch_noncausal_chunk(const Problem &p, void *ws, int Ps, int Pa, cudaStream_t s) {
+  Gammas ones;
+  for (int h = 0; h < kMaxHeads; ++h) ones.g[h] = 1.f;
+  if (p.decay || !chunk_tc_supported(p, ones) || !ws) return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  ChunkParams prm = {};
+  if (!setup_params(&prm, p.q, p.k, p.v, BH, p.N, p.D, p.Dv, p.H, ones, false))
+    return cudaErrorNotSupported;
+  prm.o = static_cast<__nv_bfloat16 *>(p.o);
+  prm.eps = p.eps;
+  prm.rec = static_cast<float *>(ws);
+  prm.rec_parts = Ps;
+  prm.P = Ps;
+  cudaError_t e = launch_mode<kState>(prm, false, p.D, p.Dv, BH * Ps, s);
+  if (e == cudaSuccess)
+    e = launch_part_scan(prm.rec, BH, p.H, Ps, p.N, p.D, p.Dv, prm.lg, kScanSum, nullptr, nullptr, s);
+  if (e != cudaSuccess) return e;
+  prm.P = Pa;
+  return launch_mode<kApply>(prm, false, p.D, p.Dv, BH * Pa, s);
 }
 
 }  // namespace linattn

@@ -38,13 +38,30 @@ cudaError_t launch_causal_tc(const Problem &p, const Gammas &g,
 // Sequence-parallel chunked kernels on tcgen05 tensor cores (bf16 operands,
 // fp32 state).  chunk_tc_supported() gives the envelope (bf16, D and Dv in
 // {64, 128}, every decay >= 0.35); chunk_parts() the number of parts per
-// (batch, head) and chunk_workspace_bytes() the device workspace the causal
-// launcher needs for that many parts (0 for one part).
+// (batch, head); chunk_workspace_bytes() the fp32 per-part records for that
+// many parts (prefill, non-causal) and chunk_causal_workspace_bytes() the
+// causal launcher's workspace (flags and inclusive states; 0 for one part).
 bool chunk_tc_supported(const Problem &p, const Gammas &g);
 int chunk_parts(int BH, int N);
 size_t chunk_workspace_bytes(int BH, int P, int D, int Dv);
+size_t chunk_causal_workspace_bytes(int BH, int P, int D, int Dv);
+Gammas log2_gammas(const Gammas &g, int H, bool decay);
 cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int P,
                                 cudaStream_t s);
+// Final state S [BH][D][Dv], z [BH][D] of the causal recurrence over N tokens.
+cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
+                                 int N, int D, int Dv, bool decay, const Gammas &g, void *ws,
+                                 int P, cudaStream_t s);
+// Non-causal forward: sums over Ps parts, read-out over Pa parts.
+cudaError_t launch_noncausal_chunk(const Problem &p, void *ws, int Ps, int Pa, cudaStream_t s);
+
+// Scan over per-part records [BH][P][D*Dv + D] (part_scan.cu): kScanStarts
+// turns A_p into the state before part p in place; kScanFinal writes the
+// state after all parts to S_out, z_out; kScanSum writes sum_p A_p to slot 0.
+enum ScanMode { kScanStarts = 0, kScanFinal = 1, kScanSum = 2 };
+cudaError_t launch_part_scan(float *rec, int BH, int H, int P, int N, int D, int Dv,
+                             const Gammas &lg, int mode, float *S_out, float *z_out,
+                             cudaStream_t s);
 
 // Split-N reduction of S = sum_j w_j phi(k_j) v_j^T and z = sum_j w_j
 // phi(k_j) with w_j = gamma^(N-1-j): partials [nsplit][BH][D*Dv + D] in

@@ -126,7 +126,7 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
       // parts of the sequence run on separate SMs; the workspace carries the
       // state from one part to the next
       const int P = chunk_parts(BH, N);
-      const size_t wsb = chunk_workspace_bytes(BH, P, D, Dv);
+      const size_t wsb = chunk_causal_workspace_bytes(BH, P, D, Dv);
       void *ws = nullptr;
       if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
       cudaError_t e = launch_causal_chunk(p, g, ws, P, s);
@@ -138,6 +138,16 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
   }
   // Non-causal: reduce S, z per (b, h) into a stream-ordered workspace, then
   // apply them to every query.
+  if (chunk_tc_supported(p, g)) {
+    const int P = chunk_parts(BH, N);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, chunk_workspace_bytes(BH, P, D, Dv), s) != cudaSuccess)
+      return LA_ERR_CUDA;
+    cudaError_t e = launch_noncausal_chunk(p, ws, P, P, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(ef);
+  }
   const size_t state_bytes = sizeof(float) * (size_t)BH * ((size_t)D * Dv + D);
   const size_t part_bytes = kv_state_workspace_bytes(BH, N, D, Dv);
   void *ws = nullptr;
@@ -177,6 +187,19 @@ la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
       return LA_ERR_INVALID_ARG;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Problem pr{nullptr, k, v, nullptr, B, H, N, D, Dv, decay, 0.f,
+                   dtype == LA_F32 ? kF32 : kBF16};
+  if (N > 0 && chunk_tc_supported(pr, g)) {
+    // tensor cores: per-part sums, then a scan over the parts
+    const int P = chunk_parts(BH, N);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, chunk_workspace_bytes(BH, P, D, Dv), s) != cudaSuccess)
+      return LA_ERR_CUDA;
+    cudaError_t e = launch_prefill_chunk(k, v, S, z, B, H, N, D, Dv, decay, g, ws, P, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(ef);
+  }
   const size_t part_bytes = kv_state_workspace_bytes(BH, N, D, Dv);
   void *ws = nullptr;
   if (part_bytes) {
