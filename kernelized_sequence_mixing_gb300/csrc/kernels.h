@@ -27,14 +27,6 @@ struct Problem {
 cudaError_t launch_causal_simt(const Problem &p, const Gammas &g,
                                cudaStream_t s);
 
-// Causal forward on tcgen05 tensor cores (bf16 operands, fp32 state).
-// causal_tc_supported() tells whether a problem is inside its envelope
-// (bf16, D and Dv in {64, 128}, every decay >= 0.35, B*H <= 65535); the
-// launcher returns cudaErrorNotSupported outside it.
-bool causal_tc_supported(const Problem &p, const Gammas &g);
-cudaError_t launch_causal_tc(const Problem &p, const Gammas &g,
-                             cudaStream_t s);
-
 // Sequence-parallel chunked kernels on tcgen05 tensor cores (bf16 operands,
 // fp32 state).  chunk_tc_supported() gives the envelope (bf16, D and Dv in
 // {64, 128}, every decay >= 0.35); chunk_parts() the number of parts per
