@@ -33,6 +33,17 @@ if ROOT not in sys.path:
 
 METRIC = ("causal linear-attn fwd tokens/s and % roofline "
           "(TFLOP/s or HBM GB/s), 1×GB300")
+# metrics of the other workloads (same unit, their own roofline)
+METRICS = {
+    "noncausal": "non-causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
+    "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
+}
+
+
+def workload_metric(w):
+    if w.steps:
+        return METRICS["decode"]
+    return METRIC if w.causal else METRICS["noncausal"]
 DEFAULT_WORKLOAD = "causal_decay_bf16_n16384"
 FALLBACK_HBM_GBS = 6800.0  # profiling recipe fallback, used only if absent
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -77,6 +88,18 @@ def barrier(world: int):
 def aggregate(ms_per_step_max: float, tokens_per_rank_step: int, world: int):
     """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
     return world * tokens_per_rank_step / (ms_per_step_max / 1e3)
+
+
+def decode_work(w):
+    """Algorithmic bytes and flops of one decode step over all B*H units:
+    the fp32 state (S and z) read and written once, q, k, v read and o
+    written once; flops per unit 4 D Dv + 3 D + Dv as in the forward."""
+    import torch
+    es = torch.tensor([], dtype=w.dtype).element_size()
+    units = w.B * w.H
+    byts = units * (2 * 4 * (w.D * w.Dv + w.D) + (2 * w.D + 2 * w.Dv) * es)
+    flops = units * (4 * w.D * w.Dv + 3 * w.D + w.Dv)
+    return byts, flops
 
 
 def algorithmic_work(w):
@@ -213,18 +236,45 @@ def time_oracle(w, heads_per_pass, passes):
     return tokens, times, threads
 
 
+def time_oracle_decode(w, units, passes):
+    """The oracle's decode step on the first `units` (sequence, head) units,
+    from a zero state (the work per step does not depend on the state)."""
+    import numpy as np
+    import oracle
+    from kernelized_sequence_mixing_gb300.workloads import decode_step_inputs
+    qt, kt, vt = decode_step_inputs(w, 0)
+    f = lambda t: t.float().reshape(-1, t.shape[-1])[:units].numpy()  # noqa: E731
+    q, k, v = f(qt), f(kt), f(vt)
+    S = np.zeros((units, w.D, w.Dv))
+    z = np.zeros((units, w.D))
+    threads = oracle.default_threads()
+    times = []
+    for _ in range(passes):
+        t0 = time.perf_counter()
+        oracle.decode_step(q, k, v, S, z, eps=w.eps, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    # a token is one position of one sequence across all H heads
+    return units / w.H, times, threads
+
+
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    heads = min(8, w.B * w.H)
-    for _ in range(args.warmup):
-        time_oracle(w, heads, 1)
-    tokens, times, threads = time_oracle(w, heads, args.steps)
+    if w.steps:
+        heads = min(1024, w.B * w.H)
+        for _ in range(args.warmup):
+            time_oracle_decode(w, heads, 1)
+        tokens, times, threads = time_oracle_decode(w, heads, args.steps)
+    else:
+        heads = min(8, w.B * w.H)
+        for _ in range(args.warmup):
+            time_oracle(w, heads, 1)
+        tokens, times, threads = time_oracle(w, heads, args.steps)
     total = sum(times)
     value = tokens * len(times) / total
     line = {
-        "impl": "reference", "metric": METRIC, "value": value,
+        "impl": "reference", "metric": workload_metric(w), "value": value,
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -232,8 +282,10 @@ def run_reference(args, w):
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": f"{heads} of {w.B * w.H} (b,h) units, all "
-                                   f"{w.N} tokens, per step"},
+                         "sample": (f"{heads} of {w.B * w.H} (b,h) units, one "
+                                    "decode step per step") if w.steps else
+                                   (f"{heads} of {w.B * w.H} (b,h) units, all "
+                                    f"{w.N} tokens, per step")},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -247,6 +299,10 @@ def workload_config(w):
            "seq_len": w.N, "parallelism": "replicas (independent batches)"}
     if w.decayed:
         cfg["gamma"] = "per head 1 - 2^(-5 - h/4)"
+    if w.steps:
+        cfg.update(seq_len=1, prefill_len=w.N, state="fp32 S [D][Dv] and z [D] "
+                   "per (sequence, head), from the prefill",
+                   step="one la_decode_step over all B*H units")
     return cfg
 
 
@@ -271,16 +327,45 @@ def run_ours(args, w):
     la.load_library()
 
     # this rank's replica: an independent batch of the same shape
-    q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, w.seed + 7919 * rank,
-                       w.scale)
     g = w.gamma()
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1 if w.causal else 4
+    seed = w.seed + 7919 * rank
+    if w.steps:
+        # decode: the state comes from a prefill of N tokens (not timed);
+        # every timed step is one la_decode_step over all B*H units
+        from kernelized_sequence_mixing_gb300.workloads import decode_step_inputs
+        _, kp, vp = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
+        S, z = la.prefill_state(kp.to(dev), vp.to(dev), gamma=g)
+        del kp, vp
+        q, k, v = decode_step_inputs(w, 7919 * rank)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty((w.B, w.H, w.Dv), dtype=w.dtype, device=dev)
+        launches_per_step = 1
 
-    def step():
-        la.forward(qd, kd, vd, causal=w.causal, gamma=g, eps=w.eps, out=od)
+        def step():
+            la.decode_step(qd, kd, vd, S, z, gamma=g, eps=w.eps, out=od)
+
+        def e2e_step(qh, kh, vh, oh):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            step()
+            oh.copy_(od, non_blocking=True)
+        tokens_rank = w.B
+    else:
+        q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
+        # causal: one chunk kernel (after a small memset of its flags);
+        # non-causal: state pass, scan, apply
+        launches_per_step = 1 if w.causal else 3
+
+        def step():
+            la.forward(qd, kd, vd, causal=w.causal, gamma=g, eps=w.eps, out=od)
+
+        def e2e_step(qh, kh, vh, oh):
+            la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+        tokens_rank = w.B * w.N
+    stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
         step()
@@ -316,7 +401,6 @@ def run_ours(args, w):
     clocks = sampler.stop() if not args.quick else None
 
     ms_max = reduce_max(ms, ws)
-    tokens_rank = w.B * w.N
     value = aggregate(ms_max, tokens_rank, ws)
 
     # end to end through the public API with host buffers: pinned inputs
@@ -325,12 +409,14 @@ def run_ours(args, w):
     if not args.quick:
         qh, kh, vh = (t.pin_memory() for t in (q, k, v))
         oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-        la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+        e2e_step(qh, kh, vh, oh)
+        torch.cuda.synchronize(dev)
         e2e_steps = max(1, min(args.steps, 10))
         barrier(ws)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+            e2e_step(qh, kh, vh, oh)
+        torch.cuda.synchronize(dev)
         e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, ws)
     es = q.element_size()
     h2d = (q.numel() + k.numel() + v.numel()) * es
@@ -340,7 +426,7 @@ def run_ours(args, w):
         return 0
 
     hbm_peak, tc_peak, peak_src = measured_peaks()
-    byts, flops = algorithmic_work(w)
+    byts, flops = decode_work(w) if w.steps else algorithmic_work(w)
     launch_ms = statistics.mean(per_launch)  # one kernel launch per step
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
@@ -351,22 +437,30 @@ def run_ours(args, w):
     # sample (all 32 heads of the default workload, ~20 s of CPU work)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        heads = min(w.B * w.H, 32)
-        tokens, times, threads = time_oracle(w, heads, 1)
-        cpu = {"value": tokens / times[0], "unit": "tokens/s",
-               "cores": threads, "kind": "oracle",
-               "sample": f"{heads} of {w.B * w.H} (b,h) units, all {w.N} "
-                         f"tokens, one pass ({times[0]:.1f} s wall)"}
+        if w.steps:
+            heads = min(w.B * w.H, 2048)
+            tokens, times, threads = time_oracle_decode(w, heads, 3)
+            t = min(times)
+            sample = (f"{heads} of {w.B * w.H} (sequence, head) units, one decode "
+                      f"step, best of 3 ({t:.2f} s wall)")
+        else:
+            heads = min(w.B * w.H, 32)
+            tokens, times, threads = time_oracle(w, heads, 1)
+            t = times[0]
+            sample = (f"{heads} of {w.B * w.H} (b,h) units, all {w.N} "
+                      f"tokens, one pass ({t:.1f} s wall)")
+        cpu = {"value": tokens / t, "unit": "tokens/s", "cores": threads,
+               "kind": "oracle", "sample": sample}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "metric": workload_metric(w), "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype.itemsize == 2 else "f32",
         "data": "synthetic",
         "config": dict(workload_config(w),
-                       l2="inputs larger than L2 (Q,K,V,O = "
-                          f"{byts / 1e6:.0f} MB), no flush"),
+                       l2=f"working set larger than L2 ({byts / 1e6:.0f} MB "
+                          "read and written per step), no flush"),
         "roofline": {"bound": "hbm", "achieved": achieved_gbs,
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak, "traffic": traffic,

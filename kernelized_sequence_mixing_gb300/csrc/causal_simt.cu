@@ -46,7 +46,7 @@ template <int D, int DV, bool DECAY, typename T>
 __global__ void __launch_bounds__(kThreads)
     causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                        const T *__restrict__ v, T *__restrict__ o, int H,
-                       int N, float eps, Gammas gam) {
+                       int N, float eps, const __grid_constant__ Gammas gam) {
   extern __shared__ float4 smem4[];
   using L = SimtLayout<D>;
   float *fqT = reinterpret_cast<float *>(smem4);  // [D][kLd]  phi(q)^T

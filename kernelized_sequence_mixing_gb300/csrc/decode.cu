@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kThreads)
     decode_kernel(const T *__restrict__ q, const T *__restrict__ k,
                   const T *__restrict__ v, float *__restrict__ S,
                   float *__restrict__ z, T *__restrict__ o, int H, float eps,
-                  Gammas gam) {
+                  const __grid_constant__ Gammas gam) {
   constexpr int EPL = DV / 32;         // columns per lane
   constexpr int RPW = D / kWarps;      // rows per warp
   using V = typename vec<EPL>::type;

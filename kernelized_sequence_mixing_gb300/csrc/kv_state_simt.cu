@@ -26,7 +26,7 @@ template <int D, int DV, bool DECAY, typename T>
 __global__ void __launch_bounds__(kThreads)
     kv_partial_kernel(const T *__restrict__ k, const T *__restrict__ v,
                       float *__restrict__ S_out, float *__restrict__ z_out,
-                      int H, int N, int split_len, Gammas gam) {
+                      int H, int N, int split_len, const __grid_constant__ Gammas gam) {
   constexpr int RD = D / 16, RE = DV / 16;
   __shared__ __align__(16) float fk[kTok][D];
   __shared__ __align__(16) float vs[kTok][DV];
