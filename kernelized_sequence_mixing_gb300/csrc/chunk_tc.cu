@@ -947,10 +947,25 @@ Gammas log2_gammas(const Gammas &g, int H, bool decay) {
 }
 
 int chunk_parts(int BH, int N) {
+  // A CTA's time is about its phase A (0.3 of its phase C per chunk) plus the
+  // chain links before it plus its phase C, and a second wave of CTAs
+  // repeats the whole critical path.  So: at most one wave, and no more
+  // parts than minimise phase C + chain, P ~ sqrt(nch * 3 / 7) with a chain
+  // link worth about 3 chunks of phase C.
   const int nch = (N + kC - 1) / kC;
   if (BH <= 0 || nch <= 0) return 1;
-  const int target = 4 * num_sms();
-  int P = (target + BH - 1) / BH;
+  int P = num_sms() / BH;
+  const int pmax = static_cast<int>(sqrt(0.43 * nch));
+  if (P > pmax) P = pmax;
+  if (P > nch) P = nch;
+  return P < 1 ? 1 : P;
+}
+
+int chunk_state_parts(int BH, int N) {
+  // state and apply passes: no chain, about two waves of CTAs
+  const int nch = (N + kC - 1) / kC;
+  if (BH <= 0 || nch <= 0) return 1;
+  int P = (2 * num_sms() + BH - 1) / BH;
   if (P > nch) P = nch;
   return P < 1 ? 1 : P;
 }
