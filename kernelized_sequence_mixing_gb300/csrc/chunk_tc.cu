@@ -83,41 +83,54 @@ constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 
 enum Mode : int { kCausal = 0, kState = 1, kApply = 2 };
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
 
-template <int D, int DV, bool STATE>
+template <int D, int DV, int MODE>
 struct Lay {
+  static constexpr bool STATE = MODE == kState, APPLY = MODE == kApply;
   static constexpr int KB = D / 64, VB = DV / 64;
   static constexpr int NA = DV + 16;  // columns of [V | 1], [T | z] and O
-  // stage: q boxes (not in state mode) | k boxes (and a zero box when
-  // D = 64) | state mode: the low bf16 parts of kh, same shape | v boxes |
-  // ones box
+  // Stage layout by mode:
+  //   causal: q boxes | k boxes (and a zero box when D = 64) | v boxes | ones box
+  //   state:  k boxes | low bf16 parts of kh | v boxes | ones box (Dv = 128)
+  //   apply:  q boxes
+  // In state mode the zero box (D = 64) and the ones box (Dv = 64) are one
+  // shared copy after the stages, reached through per-stage descriptor
+  // offsets, so that more stages fit.  The causal mode's first phase keeps
+  // the low parts in the (then unused) q boxes.
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = STATE ? 0 : KB * kBox;
-  // low parts of kh in the state sums: own boxes in state mode, the (then
-  // unused) q boxes in the first phase of the causal mode; the second
-  // 64-row atom of that operand is a zero box when D = 64
-  static constexpr int kOffKlo = STATE ? 2 * kBox : kOffQ;
-  static constexpr int kLboLo = (!STATE && D == 64) ? 2 * kBox : kBox;
-  static constexpr int kOffV = kOffK + (STATE ? 4 : 2) * kBox;
-  static constexpr int kOffOnes = kOffV + VB * kBox;
-  static constexpr int kStageBytes = kOffOnes + kBox;
-  static constexpr int kPBytes = STATE ? 0 : kC * 128;
+  static constexpr int kOffKlo = STATE ? KB * kBox : kOffQ;
+  static constexpr int kOffV = STATE ? 2 * KB * kBox : kOffK + 2 * kBox;
+  static constexpr bool kOnesInStage = !APPLY && !(STATE && DV == 64);
+  static constexpr int kOffOnes = kOffV + VB * kBox;  // in-stage ones box
+  static constexpr int kStageBytes =
+      APPLY ? KB * kBox : (STATE ? kOffOnes + (kOnesInStage ? kBox : 0) : kOffOnes + kBox);
+  static constexpr int kSharedBytes = STATE ? ((D == 64 ? kBox : 0) + (DV == 64 ? kBox : 0)) : 0;
+  static constexpr int kPBytes = MODE == kCausal ? kC * 128 : 0;
   static constexpr int kSopAtom = D * 64;  // 32 columns of [T | z], 64-byte swizzle
   static constexpr int kSopBytes = STATE ? 0 : (DV / 32 + 1) * kSopAtom;
   static constexpr int kNumBars = 3 * kMaxStages + 12;
-  static constexpr int kFixed = kPBytes + kSopBytes + kNumBars * 8 + 64 + 1024;
+  static constexpr int kFixed =
+      kSharedBytes + kPBytes + kSopBytes + kNumBars * 8 + 64 + 1024;
   static constexpr int kFit = (kSmemMax - kFixed) / kStageBytes;
   static constexpr int kStages = kFit > kMaxStages ? kMaxStages : kFit;
-  static constexpr int kOffP = kStages * kStageBytes;
+  static constexpr int kOffShared = kStages * kStageBytes;   // state: zero box, then ones box
+  static constexpr int kOffZero = kOffShared;
+  static constexpr int kOffSharedOnes = kOffShared + (D == 64 ? kBox : 0);
+  static constexpr int kOffP = kOffShared + kSharedBytes;
   static constexpr int kOffSop = kOffP + kPBytes;
   static constexpr int kOffBar = kOffSop + kSopBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-  // tensor memory columns (fp32): A' (M = 64), T (M = 128), O double buffer (M = 64)
-  static constexpr uint32_t kColA = 0, kColT = 64, kColO = 64 + NA;
-  static_assert(kColO + 2 * NA <= 512, "tensor memory");
+  // tensor memory columns (fp32): A' (M = 64), T (M = 128), O double buffer
+  // (M = 64); state mode uses only T, apply mode only O, and allocates no more
+  // than it uses (two apply CTAs can then share an SM)
+  static constexpr uint32_t kColA = 0, kColT = STATE ? 0 : 64, kColO = APPLY ? 0 : 64 + NA;
+  static constexpr uint32_t kTmemUsed = STATE ? NA : (APPLY ? 2 * NA : kColO + 2 * NA);
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
+  static_assert(kTmemUsed <= 512, "tensor memory");
   static_assert(kStages >= 3, "stages");
   static_assert(kAlloc <= kSmemMax, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kOffP % 1024 == 0 && kOffSop % 1024 == 0, "align");
@@ -233,7 +246,7 @@ __device__ __forceinline__ void put_sop16(uint8_t *sop, int atom_bytes, int atom
 
 template <int D, int DV, int MODE, bool DECAY>
 __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ ChunkParams p) {
-  using L = Lay<D, DV, MODE == kState>;
+  using L = Lay<D, DV, MODE>;
   constexpr int S = L::kStages;
   constexpr int NA = L::NA;
   constexpr bool kPhaseC = MODE == kCausal || MODE == kApply;
@@ -262,29 +275,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     item[1] = t % BH;  // batch * head
   }
   {
-    // ones box of every stage: column 0 = 1 in each of the 64 rows; zero box
-    // after k when D = 64; P and [T | z] buffers zero.
-    for (int i = tid; i < S * kBox / 16; i += kThreads) {
-      const int st = i / (kBox / 16), j = i % (kBox / 16);
-      uint8_t *ones = sm + st * L::kStageBytes + L::kOffOnes;
-      reinterpret_cast<uint4 *>(ones)[j] = make_uint4(0, 0, 0, 0);
-      if (D == 64) {
-        reinterpret_cast<uint4 *>(sm + st * L::kStageBytes + L::kOffK + kBox)[j] =
-            make_uint4(0, 0, 0, 0);
-        if (MODE == kState)
-          reinterpret_cast<uint4 *>(sm + st * L::kStageBytes + L::kOffKlo + kBox)[j] =
-              make_uint4(0, 0, 0, 0);
-      }
+    // ones boxes (column 0 = 1 in each of the 64 rows), zero boxes (the
+    // second 64-row atom of kh^T when D = 64), P and [T | z] buffers: zero
+    constexpr int kBoxU4 = kBox / 16;
+    for (int i = tid; i < S * kBoxU4; i += kThreads) {
+      const int st = i / kBoxU4, j = i % kBoxU4;
+      uint8_t *stg = sm + st * L::kStageBytes;
+      if (L::kOnesInStage) reinterpret_cast<uint4 *>(stg + L::kOffOnes)[j] = make_uint4(0, 0, 0, 0);
+      if (D == 64 && MODE == kCausal) reinterpret_cast<uint4 *>(stg + L::kOffK + kBox)[j] = make_uint4(0, 0, 0, 0);
     }
-    uint4 *z4 = reinterpret_cast<uint4 *>(sm + L::kOffP);
-    for (int i = tid; i < (L::kPBytes + L::kSopBytes) / 16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
+    uint4 *z4 = reinterpret_cast<uint4 *>(sm + L::kOffShared);
+    for (int i = tid; i < (L::kSharedBytes + L::kPBytes + L::kSopBytes) / 16; i += kThreads)
+      z4[i] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  if (tid < S * kC) {
+  if (L::kOnesInStage && tid < S * kC) {
     const int st = tid / kC, r = tid % kC;
     *reinterpret_cast<__nv_bfloat16 *>(sm + st * L::kStageBytes + L::kOffOnes + sw128_off(r, 0)) =
         __float2bfloat16_rn(1.f);
   }
+  if (MODE == kState && DV == 64 && tid < kC)
+    *reinterpret_cast<__nv_bfloat16 *>(sm + L::kOffSharedOnes + sw128_off(tid, 0)) =
+        __float2bfloat16_rn(1.f);
   if (tid == 32 * kWarpTma) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, L::kTmemCols);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -514,9 +526,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     // (N = value column, K = d).  Variants differ in the start address only.
     const uint64_t dq0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
     const uint64_t dk0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
+    // kh^T (its low parts) and [V | 1]: the second atom (zero box, ones box)
+    // is in the stage at the next box, except where it is a shared copy
     const uint64_t dkt0 = smem_desc(base + L::kOffK, kBox, 1024, kSw128);
-    const uint64_t dktlo0 = smem_desc(base + L::kOffKlo, L::kLboLo, 1024, kSw128);
+    const uint64_t dktlo0 = smem_desc(base + L::kOffKlo, (MODE == kCausal && D == 64) ? 2 * kBox : kBox, 1024, kSw128);
     const uint64_t dv0 = smem_desc(base + L::kOffV, kBox, 1024, kSw128);
+    // state mode, per stage: start address field as usual, LBO to the shared box
+    auto desc_state = [&](int st, int off, bool shared, int shared_off) {
+      const uint32_t a = base + st * L::kStageBytes + off;
+      return smem_desc(a, shared ? base + shared_off - a : kBox, 1024, kSw128);
+    };
     const uint64_t dp0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
     const uint64_t dsop0 = smem_desc(base + L::kOffSop, L::kSopAtom, 512, kSw64);
     const uint32_t tA = tmem + L::kColA, tT = tmem + L::kColT;
@@ -532,10 +551,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       tc_fence_after();
       if (leader) {
         const uint64_t so = static_cast<uint64_t>(s) * kStageU;
+        if (MODE == kState) {
+          const uint64_t dk = desc_state(s, L::kOffK, D == 64, L::kOffZero);
+          const uint64_t dl = desc_state(s, L::kOffKlo, D == 64, L::kOffZero);
+          const uint64_t dv = desc_state(s, L::kOffV, DV == 64, L::kOffSharedOnes);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
-          if (MODE == kState) mma_bf16(tT, dktlo0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, 1u);
+          for (int kk = 0; kk < kC / 16; ++kk) {
+            mma_bf16(tT, dk + kk * 128, dv + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tT, dl + kk * 128, dv + kk * 128, ID_DS, 1u);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk)
+            mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&empty[s]);
       }
@@ -549,28 +577,45 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (leader) mma_commit(T_ready);
       __syncwarp();
     }
-    // phase C: per chunk A', [dS | dz], inter-chunk and, once P is ready,
-    // intra-chunk MMAs
+    // phase C.  Iteration i issues chunk i+1's A' first, then chunk i's
+    // [dS | dz], inter- and intra-chunk MMAs, so the P warps turn A'_(i+1)
+    // into P while the tensor pipe works on chunk i: every wait below has
+    // about a chunk of queued work in front of it.  (A' has one buffer: the
+    // P warps have read A'_i long before A'_(i+1) is issued.)
+    auto issue_a = [&](int j, int st) -> bool {  // A'_j = qh kh^T (M 64 t, N 64 s, K = D)
+      if (!warp_wait(A_free, (j & 1) ^ 1, abort_flag, p.timeouts)) return false;
+      tc_fence_after();
+      if (leader) {
+        const uint64_t so = static_cast<uint64_t>(st) * kStageU;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = so + (kk >> 2) * (kBox >> 4) + (kk & 3) * 2;
+          mma_bf16(tA, dq0 + off, dk0 + off, ID_A, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(A_full);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && kPhaseC && nch > 0 && MODE == kCausal) {
+      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts) || !issue_a(0, s)) ok = false;
+    }
     for (int i = 0; ok && kPhaseC && i < nch; ++i) {
       const int b = i & 1;
       const uint32_t u = static_cast<uint32_t>(i >> 1);
       const uint64_t so = static_cast<uint64_t>(s) * kStageU;
-      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) break;
+      int s1 = s + 1;
+      uint32_t ph1 = ph;
+      if (s1 == S) {
+        s1 = 0;
+        ph1 ^= 1;
+      }
+      if (MODE == kApply && !warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) break;
       if (MODE == kCausal) {
-        // A' = qh kh^T  (M 64 tokens t, N 64 tokens s, K = D)
-        if (!warp_wait(A_free, (i & 1) ^ 1, abort_flag, p.timeouts)) break;
-        tc_fence_after();
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t off = so + (kk >> 2) * (kBox >> 4) + (kk & 3) * 2;
-            mma_bf16(tA, dq0 + off, dk0 + off, ID_A, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(A_full);
-        }
-        __syncwarp();
-        // T += kh^T [V | 1]: not needed after the last chunk
         if (i + 1 < nch) {
+          if (!warp_wait(&mapped[s1], ph1, abort_flag, p.timeouts)) break;
+          if (!issue_a(i + 1, s1)) break;
+          // T += kh^T [V | 1]: not needed after the last chunk
           if (!warp_wait(T_free, i & 1, abort_flag, p.timeouts)) break;
           tc_fence_after();
           if (leader) {
@@ -611,10 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         mma_commit(&empty[s]);
       }
       __syncwarp();
-      if (++s == S) {
-        s = 0;
-        ph ^= 1;
-      }
+      s = s1;
+      ph = ph1;
     }
     // every MMA issued has completed before TMEM is released
     if (leader) {
@@ -880,13 +923,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 template <int D, int DV, int MODE, bool DECAY>
 cudaError_t launch_typed(const ChunkParams &prm, int grid, cudaStream_t s) {
   auto kern = chunk_tc_kernel<D, DV, MODE, DECAY>;
-  const int smem = Lay<D, DV, MODE == kState>::kAlloc;
+  const int smem = Lay<D, DV, MODE>::kAlloc;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, smem, s>>>(prm);
