@@ -129,7 +129,7 @@ def measured_peaks():
 
 
 # sources the causal tensor-core kernel is compiled from
-KERNEL_SOURCES = ("chunk_tc.cu", "tc_common.cuh", "common.cuh")
+KERNEL_SOURCES = ("chunk128.cu", "chunk_tc.cu", "tc_common.cuh", "common.cuh")
 
 
 def kernel_source_hash():

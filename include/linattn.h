@@ -119,10 +119,12 @@ LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
 
 /*
  * Which kernel la_forward would run for a causal call with these arguments:
- * 1 = the tcgen05 tensor-core kernel (bf16, D and Dv in {64, 128}, every
- * gamma >= 0.35, B*H <= 65535), 0 = the fp32 CUDA-core kernel (fp32 inputs,
- * or stronger decays, whose gamma^-63 operand scale would leave the bf16
- * range), or a negative la_status_t (negated) if the arguments are invalid.
+ * 2 = the tcgen05 tensor-core kernel with 128-token chunks (bf16,
+ * D = Dv = 128, every gamma >= 0.61), 1 = the tcgen05 tensor-core kernel with
+ * 64-token chunks (bf16, D and Dv in {64, 128}, every gamma >= 0.35),
+ * 0 = the fp32 CUDA-core kernel (fp32 inputs, or stronger decays, whose
+ * gamma^-63 operand scale would leave the bf16 range), or a negative
+ * la_status_t (negated) if the arguments are invalid.
  * Host-only; touches no device.
  */
 LA_API int la_causal_kernel(int B, int H, int N, int D, int Dv,

@@ -80,13 +80,14 @@ def status_string(code: int) -> str:
 
 
 def causal_kernel(B, H, N, D, Dv, gamma=None, dtype=torch.bfloat16) -> str:
-    """Which kernel a causal forward with these sizes runs: "tensor-core" or
-    "cuda-core" (host-only query)."""
+    """Which kernel a causal forward with these sizes runs: "tensor-core-128"
+    (128-token chunks), "tensor-core" (64-token chunks) or "cuda-core"
+    (host-only query)."""
     code = load_library().la_causal_kernel(B, H, N, D, Dv, _gamma_arg(gamma, H),
                                            _DTYPES[dtype])
     if code < 0:
         raise LinAttnError("la_causal_kernel", -code)
-    return "tensor-core" if code == 1 else "cuda-core"
+    return {2: "tensor-core-128", 1: "tensor-core"}.get(code, "cuda-core")
 
 
 def device_wait_timeouts(reset: bool = False) -> int:

@@ -1,0 +1,802 @@
+// Causal linear attention with 128-token chunks, D = Dv = 128, on tcgen05
+// tensor cores (sm_103a).
+//
+// Method: the recurrence of "Linear Attention Mechanisms" (dileepadev.github.io),
+// "Recurrent Reformulation", S_i = gamma S_(i-1) + phi(k_i) v_i^T,
+// z_i = gamma z_(i-1) + phi(k_i), o_i = phi(q_i)^T S_i / (phi(q_i) . z_i + eps),
+// phi = elu + 1, with the fixed per-head decay gamma of its "Gating and
+// Selective State Updates" (RetNet) on both S and z.
+//
+// The same chunkwise regrouping and sequence split as the 64-token kernel
+// (chunk_tc.cu): parts of whole chunks per (batch, head), phase A (the
+// part's own sum A_p), a chain of inclusive states between the CTAs of one
+// (batch, head), then phase C over the part's chunks:
+//   qh_t = gamma^(c0+t-E) phi(q_t),  kh_s = gamma^(E-c0-s) phi(k_s)
+//   A'   = qh kh^T,  P = A' masked to s <= t
+//   O    = qh [T | z] + P [V | 1],  T += kh^T [V | 1]
+//   o_t  = O[t, :Dv] / (O[t, Dv] + eps)
+// with T the state scaled to the end E of the current decay window.
+//
+// What differs: chunks of 128 tokens, so every product of phase C is an
+// M = 128 MMA (twice the work per instruction of the M = 64 products, and
+// half the hand-offs per token), and the A operands qh and P live in tensor
+// memory: the feature-map warps write qh there (no shared-memory tile for
+// the mapped q), and the P warps overwrite A' in place with bf16 P.  That
+// leaves shared memory for double-buffered k and v tiles of 128 tokens.
+//
+// Warp roles (18 warps):
+//   0-3   P: A' -> masked bf16 P in tensor memory
+//   4-7   state and output: the chain, the bf16 copy of [T | z] for the MMA
+//         and window rescaling (thread = row d of T), then O -> o rows
+//         (divide by the normaliser; thread = token row)
+//   8-15  feature map: kh in place, qh into tensor memory; warp 8 + j maps
+//         the rows of TMEM lane quadrant j % 4, dims [64 (j / 4), + 64)
+//   (warps 0-15 share the phase A feature map)
+//   16    TMA: lane 0 the k ring, lane 1 the v ring, lane 2 the q tile
+//   17    TMEM owner and MMA issuer
+// Every wait is bounded; a CTA that gives up counts the failure in device
+// memory, drains its in-flight copies and MMAs, frees tensor memory and exits.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace linattn {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 128;      // tokens per chunk
+constexpr int kD = 128;      // key / query width
+constexpr int kDV = 128;     // value width
+constexpr int kNA = kDV + 16;  // columns of [V | 1], [T | z] and O
+constexpr int kThreads = 576;
+constexpr int kWarpS = 4;
+constexpr int kWarpPhi = 8;
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;
+constexpr float kGammaMin = 0.61f;       // gamma^128 stays above 1e-28
+constexpr float kLog2Floor = -93.0139f;  // log2(1e-28): smallest factor in a window
+
+// Shared memory, from a 1024-byte aligned base.
+//   k ring: 2 slots x 2 boxes of 128 rows x 128 bytes (64 dims), 128-byte swizzle
+//   v ring: 2 slots x (4 atoms of 128 rows x 64 bytes (32 columns), 64-byte
+//           swizzle, then the ones atom: column 0 = 1) = [V | 1]
+//   q tile: one slot, 2 boxes like k
+//   [T | z]: bf16, 5 atoms of 128 rows (d) x 64 bytes, 64-byte swizzle
+constexpr int kKBox = 128 * 128;
+constexpr int kVAtom = 128 * 64;
+constexpr int kKSlot = 2 * kKBox;
+constexpr int kVSlot = 5 * kVAtom;
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + 2 * kKSlot;
+constexpr int kOffQ = kOffV + 2 * kVSlot;
+constexpr int kSopAtom = kD * 64;
+constexpr int kOffSop = kOffQ + kKSlot;
+constexpr int kNumBars = 24;
+constexpr int kOffBar = kOffSop + 5 * kSopAtom;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kBytes = kOffMisc + 32;
+constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
+static_assert(kAlloc <= 227 * 1024, "shared memory");
+static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffSop % 1024 == 0, "align");
+
+// Tensor memory (512 columns): qh as bf16 pairs, A' (fp32; P as bf16 pairs
+// in its first 64 columns), T = [S | z] (fp32), O (fp32).
+constexpr uint32_t kColQ = 0;
+constexpr uint32_t kColA = 64;
+constexpr uint32_t kColT = 192;
+constexpr uint32_t kColO = kColT + kNA;
+static_assert(kColO + kNA <= 512, "tensor memory");
+
+// barrier slots
+enum Bar : int {
+  kKFull = 0,      // [2] TMA k tile landed
+  kKEmpty = 2,     // [2] k slot free (MMA commit)
+  kVFull = 4,      // [2]
+  kVEmpty = 6,     // [2]
+  kQFull = 8,      // q tile landed
+  kQEmpty = 9,     // q tile read by the feature-map warps
+  kKMapped = 10,   // [2] kh in place
+  kQReady = 12,    // qh in tensor memory
+  kAFull = 13,     // A' computed
+  kPFull = 14,     // P in tensor memory
+  kTReady = 15,    // T updated
+  kTFree = 16,     // T read (and rescaled) by the state warps
+  kSFull = 17,     // bf16 [T | z] written
+  kInterDone = 18, // O = qh [T | z] done: [T | z] and qh may be replaced
+  kOFull = 19,     // O complete
+  kOFree = 20,     // O read by the output warps
+  kDrain = 21,
+};
+
+struct Chunk128Params {
+  CUtensorMap tmQ, tmK, tmV;
+  __nv_bfloat16 *o;
+  float *rec;      // P > 1: inclusive states [B*H][P][D*Dv + D]
+  int *ws_flag;    // P > 1: [B*H][P], 1 once incl_p is published
+  int *ws_ticket;  // P > 1: part-major work counter
+  unsigned int *timeouts;
+  int BH, H, N, P;
+  int o_v8;  // o is 32-byte aligned: 256-bit stores
+  float eps;
+  Gammas lg;  // log2(gamma) per head
+};
+
+// phi and the row scale in place on one box row: 8 chunks of 16 bytes of
+// row r of a 128-byte-swizzled box.
+__device__ __forceinline__ void map_row(uint8_t *box, int r, uint32_t sc) {
+  uint4 x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = *reinterpret_cast<const uint4 *>(box + sw128_off(r, 16 * c));
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    x[c].x = phi_scale_bf16x2(x[c].x, sc);
+    x[c].y = phi_scale_bf16x2(x[c].y, sc);
+    x[c].z = phi_scale_bf16x2(x[c].z, sc);
+    x[c].w = phi_scale_bf16x2(x[c].w, sc);
+    *reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * c)) = x[c];
+  }
+}
+
+// The same on chunks [c0, c0 + 4) of the row.
+__device__ __forceinline__ void map_row4(uint8_t *box, int r, int c0, uint32_t sc) {
+  uint4 x[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) x[c] = *reinterpret_cast<const uint4 *>(box + sw128_off(r, 16 * (c0 + c)));
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    x[c].x = phi_scale_bf16x2(x[c].x, sc);
+    x[c].y = phi_scale_bf16x2(x[c].y, sc);
+    x[c].z = phi_scale_bf16x2(x[c].z, sc);
+    x[c].w = phi_scale_bf16x2(x[c].w, sc);
+    *reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * (c0 + c))) = x[c];
+  }
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  tmem_st32(taddr, f);
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+  tmem_st16(taddr, f);
+}
+
+// 64 bf16 (32 pairs) to global memory: 256-bit stores when the row is
+// 32-byte aligned, else 128-bit.
+__device__ __forceinline__ void store_row_half(__nv_bfloat16 *dst, const uint32_t *pk, int v8) {
+  if (v8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * q),
+                   "r"(pk[8 * q]), "r"(pk[8 * q + 1]), "r"(pk[8 * q + 2]), "r"(pk[8 * q + 3]),
+                   "r"(pk[8 * q + 4]), "r"(pk[8 * q + 5]), "r"(pk[8 * q + 6]), "r"(pk[8 * q + 7])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      reinterpret_cast<uint4 *>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+}
+
+template <bool DECAY>
+__global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_constant__ Chunk128Params p) {
+  constexpr size_t kRec = static_cast<size_t>(kD) * kDV + kD;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  int *item = reinterpret_cast<int *>(sm + kOffMisc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.BH, N = p.N, P = p.P;
+
+  // ---- set-up: work item, constant operand blocks, barriers, TMEM ----
+  if (tid == 0) {
+    int t = static_cast<int>(blockIdx.x);
+    if (P > 1) t = atomicAdd(p.ws_ticket, 1);
+    item[0] = t / BH;  // part (part-major order)
+    item[1] = t % BH;  // batch * head
+  }
+  {
+    // ones atoms of both v slots and the [T | z] operand: zero, then
+    // column 0 of every ones row = 1
+    for (int i = tid; i < 2 * kVAtom / 16; i += kThreads) {
+      const int sl = i / (kVAtom / 16), j = i % (kVAtom / 16);
+      reinterpret_cast<uint4 *>(sm + kOffV + sl * kVSlot + 4 * kVAtom)[j] = make_uint4(0, 0, 0, 0);
+    }
+    for (int i = tid; i < 5 * kSopAtom / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(sm + kOffSop)[i] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  if (tid < 2 * kC) {
+    const int sl = tid / kC, r = tid % kC;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + kOffV + sl * kVSlot + 4 * kVAtom + sw64_off(r, 0)) =
+        __float2bfloat16_rn(1.f);
+  }
+  if (tid == 32 * kWarpTma) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[kKFull + s], 1);
+      mbar_init(&bar[kKEmpty + s], 1);
+      mbar_init(&bar[kVFull + s], 1);
+      mbar_init(&bar[kVEmpty + s], 1);
+      mbar_init(&bar[kKMapped + s], 16);
+    }
+    mbar_init(&bar[kQFull], 1);
+    mbar_init(&bar[kQEmpty], 8);
+    mbar_init(&bar[kQReady], 8);
+    mbar_init(&bar[kAFull], 1);
+    mbar_init(&bar[kPFull], 4);
+    mbar_init(&bar[kTReady], 1);
+    mbar_init(&bar[kTFree], 4);
+    mbar_init(&bar[kSFull], 4);
+    mbar_init(&bar[kInterDone], 1);
+    mbar_init(&bar[kOFull], 1);
+    mbar_init(&bar[kOFree], 4);
+    mbar_init(&bar[kDrain], 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int part = item[0], bh = item[1];
+
+  // the part: chunks [cb, cb + nch) of this (batch, head)
+  const int nch_all = (N + kC - 1) / kC;
+  const int pbase = nch_all / P, prem = nch_all % P;
+  const int cb = part * pbase + min(part, prem);
+  const int nch = pbase + (part < prem ? 1 : 0);
+  const int len = min(N, (cb + nch) * kC) - cb * kC;
+  const bool hasA = part < P - 1;
+  const bool needPrev = part > 0;
+  const int nA = hasA ? nch : 0;
+  const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
+  int WC = 64;  // chunks per decay window
+  if (DECAY && lg < 0.f) {
+    const float c = kLog2Floor / lg / static_cast<float>(kC);
+    WC = c < 1.f ? 1 : (c > 64.f ? 64 : static_cast<int>(c));
+  }
+  const int W = kC * WC;
+  auto scale2 = [&](float e) -> uint32_t {  // gamma^e as a bf16 pair
+    const float f = DECAY ? exp2f(e * lg) : 1.f;
+    return pack_bf16x2(f, f);
+  };
+
+  // Phase A feature map, kh_s = gamma^(e_p - s) phi(k_s) with e_p the
+  // chunk-aligned end of the part, by all 16 compute warps: warp u maps
+  // rows 32 (u % 4) + lane, 16-byte chunks [4 (u / 4), + 4) of the row
+  // (box u / 8).
+  auto phase_a_map = [&](int u) {
+    const int r = 32 * (u & 3) + lane, quarter = u >> 2;
+    for (int i = 0; i < nA; ++i) {
+      const int sl = i & 1;
+      if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
+      const int nv = min(kC, N - (cb + i) * kC);
+      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nch - i) - 1 - r)) : 0u;
+      map_row4(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kKMapped + sl]);
+    }
+  };
+
+  // Before phase C, run by the state/output warps, thread c = d = 32 w +
+  // lane on row d: S0 = incl_(p-1) (0 for the first part); incl_p =
+  // A_p + gamma^len S0 is published for the next part unless this is the
+  // last; T = gamma^W S0 goes to tensor memory and, in bf16, to [T | z].
+  auto chain_part = [&](int w, int c) {
+    const int d = 32 * w + lane;
+    const uint32_t tT = tmem_addr(tmem, 32 * w, kColT);
+    uint8_t *sop = sm + kOffSop;
+    const bool pub = hasA;
+    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+    const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
+    const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+    if (hasA) {
+      warp_wait(&bar[kTReady], 0, abort_flag, p.timeouts);
+      tc_fence_after();
+    }
+    if (needPrev) {
+      if (c == 0) {
+        const int *f = p.ws_flag + bh * P + part - 1;
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(f) == 0) {
+          if (*abort_flag) break;
+          if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicAdd(p.timeouts, 1u);
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      named_sync(1, 128);
+    }
+    const float *prev = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
+    float *dst = p.rec + (static_cast<size_t>(bh) * P + part) * kRec;
+#pragma unroll 1
+    for (int cc = 0; cc < kDV / 32; ++cc) {
+      float x[32], t[32];
+      if (hasA) tmem_ld32(tT + 32 * cc, t);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (needPrev) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * kDV + 32 * cc) + q);
+        x[4 * q] = v4.x;
+        x[4 * q + 1] = v4.y;
+        x[4 * q + 2] = v4.z;
+        x[4 * q + 3] = v4.w;
+      }
+      if (hasA) tmem_wait_ld();
+      if (pub) {
+        float4 *o4 = reinterpret_cast<float4 *>(dst + d * kDV + 32 * cc);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o4[q] = make_float4(fmaf(gLen, x[4 * q], corr * t[4 * q]),
+                              fmaf(gLen, x[4 * q + 1], corr * t[4 * q + 1]),
+                              fmaf(gLen, x[4 * q + 2], corr * t[4 * q + 2]),
+                              fmaf(gLen, x[4 * q + 3], corr * t[4 * q + 3]));
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] *= gW;
+      tmem_st32(tT + 32 * cc, x);
+      put_sop32(sop, kSopAtom, cc, d, x);
+    }
+    {
+      float sp[16], tz[16];
+      if (hasA) {
+        tmem_ld16(tT + kDV, tz);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) sp[e] = 0.f;
+      if (needPrev) sp[0] = __ldcg(prev + kD * kDV + d);
+      if (pub) dst[kD * kDV + d] = fmaf(gLen, sp[0], hasA ? corr * tz[0] : 0.f);
+      sp[0] *= gW;
+      tmem_st16(tT + kDV, sp);
+      put_sop16(sop, kSopAtom, kDV / 32, d, sp);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    fence_async_smem();
+    named_sync(1, 128);
+    if (pub && c == 0) {
+      // the state is visible device-wide before the flag
+      __threadfence();
+      st_release_gpu(p.ws_flag + bh * P + part, 1);
+    }
+  };
+
+  if (warp == kWarpTma) {
+    // ---------------- TMA: three independent rings, one lane each ----------------
+    // lane 0: k tiles (phase A then phase C), lane 1: v tiles, lane 2: q tiles
+    // (phase C).  Slot of ring chunk c: c % 2, phase (c / 2) & 1.
+    if (lane < 3) {
+      const CUtensorMap *map = lane == 0 ? &p.tmK : (lane == 1 ? &p.tmV : &p.tmQ);
+      prefetch_tmap(map);
+      const int n = lane == 2 ? nch : nA + nch;
+      const int slots = lane == 2 ? 1 : 2;
+      uint64_t *fullb = &bar[lane == 0 ? kKFull : (lane == 1 ? kVFull : kQFull)];
+      uint64_t *emptyb = &bar[lane == 0 ? kKEmpty : (lane == 1 ? kVEmpty : kQEmpty)];
+      int issued = 0;
+      for (int c = 0; c < n; ++c) {
+        const int sl = c % slots;
+        const uint32_t ph = static_cast<uint32_t>((c / slots) & 1);
+        if (!mbar_wait(&emptyb[sl], ph ^ 1, abort_flag, p.timeouts)) break;
+        const int row = (cb + (lane == 2 ? c : (c < nA ? c : c - nA))) * kC;
+        mbar_arrive_expect_tx(&fullb[sl], lane == 1 ? 4 * kVAtom : kKSlot);
+        if (lane == 1) {
+          uint8_t *dst = sm + kOffV + sl * kVSlot;
+#pragma unroll
+          for (int a = 0; a < 4; ++a) tma_load_3d(dst + a * kVAtom, map, 32 * a, row, bh, &fullb[sl]);
+        } else {
+          uint8_t *dst = sm + (lane == 0 ? kOffK + sl * kKSlot : kOffQ);
+          tma_load_3d(dst, map, 0, row, bh, &fullb[sl]);
+          tma_load_3d(dst + kKBox, map, 64, row, bh, &fullb[sl]);
+        }
+        issued = c + 1;
+        // L2 prefetch of the tile two ring chunks ahead (its load waits for a slot)
+        const int cp = c + 2;
+        if (cp < n) {
+          const int rowp = (cb + (lane == 2 ? cp : (cp < nA ? cp : cp - nA))) * kC;
+          if (lane == 1) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) tma_prefetch_3d(map, 32 * a, rowp, bh);
+          } else {
+            tma_prefetch_3d(map, 0, rowp, bh);
+            tma_prefetch_3d(map, 64, rowp, bh);
+          }
+        }
+      }
+      if (*abort_flag) {  // let every issued copy land before the CTA exits
+        for (int c = issued > slots ? issued - slots : 0; c < issued; ++c)
+          mbar_wait_drain(&fullb[c % slots], (c / slots) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer (warp-wide loop, lane 0 issues) ----------------
+    const bool leader = lane == 0;
+    constexpr uint32_t ID_A = idesc_bf16(128, 128, false, false);  // qh (TMEM) kh^T
+    constexpr uint32_t ID_DS = idesc_bf16(128, kNA, true, true);   // kh^T [V | 1]
+    constexpr uint32_t ID_O = idesc_bf16(128, kNA, false, true);   // qh [T|z], P [V|1]
+    const uint32_t base = smem_u32(sm);
+    // kh as B of A' (K-major: rows s, K = d), kh^T as A of dS (MN-major: M = d
+    // in two 64-wide atoms, K = tokens), [V | 1] and [T | z] as B (MN-major:
+    // N in 32-wide atoms, K = tokens or d)
+    auto dk = [&](int sl) { return smem_desc(base + kOffK + sl * kKSlot, 16, 1024, kSw128); };
+    auto dkt = [&](int sl) { return smem_desc(base + kOffK + sl * kKSlot, kKBox, 1024, kSw128); };
+    auto dv = [&](int sl) { return smem_desc(base + kOffV + sl * kVSlot, kVAtom, 512, kSw64); };
+    const uint64_t dsop = smem_desc(base + kOffSop, kSopAtom, 512, kSw64);
+    const uint32_t tQ = tmem + kColQ, tA = tmem + kColA, tT = tmem + kColT, tO = tmem + kColO;
+    bool ok = true;
+    // phase A: T = kh^T [V | 1] over the part
+    for (int i = 0; i < nA; ++i) {
+      const int sl = i & 1;
+      const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
+      if (!warp_wait(&bar[kKMapped + sl], ph, abort_flag, p.timeouts) ||
+          !warp_wait(&bar[kVFull + sl], ph, abort_flag, p.timeouts)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t a = dkt(sl), b = dv(sl);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk)
+          mma_bf16(tT, a + kk * 128, b + kk * 64, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar[kKEmpty + sl]);
+        mma_commit(&bar[kVEmpty + sl]);
+      }
+      __syncwarp();
+    }
+    if (ok && hasA) {
+      if (leader) mma_commit(&bar[kTReady]);
+      __syncwarp();
+    }
+    // phase C.  Iteration i: [dS_i], inter_i, intra_i, then A'_(i+1), so that
+    // each consumer round trip (P, the [T | z] copy, the O read-out, qh) has
+    // at least one group of 8 MMAs queued in front of the MMA that waits on it.
+    auto issue_a = [&](int i) -> bool {  // A'_i = qh_i kh_i^T  (M 128 t, N 128 s, K = D)
+      const int c = nA + i, sl = c & 1;
+      if (!warp_wait(&bar[kKMapped + sl], (c >> 1) & 1, abort_flag, p.timeouts) ||
+          !warp_wait(&bar[kQReady], i & 1, abort_flag, p.timeouts))
+        return false;
+      tc_fence_after();
+      if (leader) {
+        const uint64_t b = dk(sl);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16_ta(tA, tQ + 8 * kk, b + (kk >> 2) * (kKBox >> 4) + (kk & 3) * 2, ID_A,
+                      kk > 0 ? 1u : 0u);
+        mma_commit(&bar[kAFull]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && nch > 0 && !issue_a(0)) ok = false;
+    for (int i = 0; ok && i < nch; ++i) {
+      const int c = nA + i, sl = c & 1;
+      const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
+      if (i + 1 < nch) {
+        // T += kh^T [V | 1]: not needed after the last chunk
+        if (!warp_wait(&bar[kTFree], i & 1, abort_flag, p.timeouts) ||
+            !warp_wait(&bar[kVFull + sl], ph, abort_flag, p.timeouts))
+          break;
+        tc_fence_after();
+        if (leader) {
+          const uint64_t a = dkt(sl), b = dv(sl);
+#pragma unroll
+          for (int kk = 0; kk < kC / 16; ++kk) mma_bf16(tT, a + kk * 128, b + kk * 64, ID_DS, 1u);
+          mma_commit(&bar[kTReady]);
+        }
+      }
+      if (leader) mma_commit(&bar[kKEmpty + sl]);
+      __syncwarp();
+      // O = qh [T | z]  (M 128, N Dv + 16, K = D)
+      if (!warp_wait(&bar[kSFull], i & 1, abort_flag, p.timeouts)) break;
+      if (i > 0 && !warp_wait(&bar[kOFree], (i - 1) & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16_ta(tO, tQ + 8 * kk, dsop + kk * 64, ID_O, kk > 0 ? 1u : 0u);
+        mma_commit(&bar[kInterDone]);
+      }
+      __syncwarp();
+      // O += P [V | 1]  (M 128, N Dv + 16, K 128 tokens)
+      if (!warp_wait(&bar[kPFull], i & 1, abort_flag, p.timeouts) ||
+          !warp_wait(&bar[kVFull + sl], ph, abort_flag, p.timeouts))
+        break;
+      tc_fence_after();
+      if (leader) {
+        const uint64_t b = dv(sl);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) mma_bf16_ta(tO, tA + 8 * kk, b + kk * 64, ID_O, 1u);
+        mma_commit(&bar[kOFull]);
+        mma_commit(&bar[kVEmpty + sl]);
+      }
+      __syncwarp();
+      if (i + 1 < nch && !issue_a(i + 1)) break;
+    }
+    // every MMA issued has completed before TMEM is released
+    if (leader) {
+      mma_commit(&bar[kDrain]);
+      mbar_wait_drain(&bar[kDrain], 0);
+    }
+    __syncwarp();
+  } else if (warp >= kWarpPhi) {
+    // ---------------- feature map: kh in place, qh into tensor memory ----------------
+    const int j = warp - kWarpPhi;
+    const int qd = j & 3, h = j >> 2;  // TMEM lane quadrant, half of the dims
+    const int r = 32 * qd + lane;      // token row of the chunk
+    phase_a_map(warp);
+    const uint32_t tq = tmem_addr(tmem, 32 * qd, kColQ + 32 * h);
+    for (int i = 0; i < nch; ++i) {
+      const int c = nA + i, sl = c & 1;
+      const int nv = min(kC, N - (cb + i) * kC);
+      const int jw = i % WC;  // chunk within its decay window
+      // kh_s = gamma^(E - s) phi(k_s), rows past the sequence end zero
+      if (!warp_wait(&bar[kKFull + sl], (c >> 1) & 1, abort_flag, p.timeouts)) break;
+      map_row(sm + kOffK + sl * kKSlot + h * kKBox, r,
+              r < nv ? scale2(static_cast<float>(W - 1 - kC * jw - r)) : 0u);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(&bar[kKMapped + sl], 2);
+      // qh_t = gamma^(t - E) phi(q_t), as bf16 pairs (column m = dims 2m, 2m+1)
+      if (!warp_wait(&bar[kQFull], i & 1, abort_flag, p.timeouts)) break;
+      uint32_t qh[32];
+      {
+        const uint32_t sc = scale2(static_cast<float>(kC * jw - (W - 1) + r));
+        uint4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          x[q] = *reinterpret_cast<const uint4 *>(sm + kOffQ + h * kKBox + sw128_off(r, 16 * q));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          qh[4 * q + 0] = phi_scale_bf16x2(x[q].x, sc);
+          qh[4 * q + 1] = phi_scale_bf16x2(x[q].y, sc);
+          qh[4 * q + 2] = phi_scale_bf16x2(x[q].z, sc);
+          qh[4 * q + 3] = phi_scale_bf16x2(x[q].w, sc);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kQEmpty]);
+      // qh_(i-1) is consumed once O = qh [T | z] of chunk i-1 is done
+      if (i > 0 && !warp_wait(&bar[kInterDone], (i - 1) & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      tmem_st32u(tq, qh);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kQReady]);
+    }
+  } else if (warp >= kWarpS) {
+    // ---------------- state, then output rows ----------------
+    const int w = warp - kWarpS;  // TMEM lane quadrant
+    const int d = 32 * w + lane;  // row of T (state) and token row (output)
+    const uint32_t tT = tmem_addr(tmem, 32 * w, kColT);
+    const uint32_t to = tmem_addr(tmem, 32 * w, kColO);
+    uint8_t *sop = sm + kOffSop;
+    phase_a_map(warp);
+    chain_part(w, d);
+    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+    if (lane == 0) {  // the chain is done (chain_part ends with a barrier)
+      mbar_arrive(&bar[kTFree]);
+      mbar_arrive(&bar[kSFull]);
+    }
+    for (int i = 1; i <= nch; ++i) {
+      // (1) after T += kh^T [V | 1] of chunk i-1 and once O = qh [T | z] of
+      // chunk i-1 has read the old copy, publish bf16 [T | z] for chunk i
+      // (rescaled when chunk i opens a new decay window)
+      if (i < nch) {
+        if (!warp_wait(&bar[kTReady], static_cast<uint32_t>((i - 1 + (hasA ? 1 : 0)) & 1), abort_flag,
+                       p.timeouts) ||
+            !warp_wait(&bar[kInterDone], static_cast<uint32_t>((i - 1) & 1), abort_flag, p.timeouts))
+          break;
+        tc_fence_after();
+        const bool rebase = DECAY && (i % WC == 0);
+#pragma unroll 1
+        for (int cc = 0; cc < kDV / 32; cc += 2) {
+          float x0[32], x1[32];
+          tmem_ld32(tT + 32 * cc, x0);
+          tmem_ld32(tT + 32 * cc + 32, x1);
+          tmem_wait_ld();
+          if (rebase) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x0[e] *= gW;
+              x1[e] *= gW;
+            }
+            tmem_st32(tT + 32 * cc, x0);
+            tmem_st32(tT + 32 * cc + 32, x1);
+          }
+          put_sop32(sop, kSopAtom, cc, d, x0);
+          put_sop32(sop, kSopAtom, cc + 1, d, x1);
+        }
+        {
+          float x0[16];
+          tmem_ld16(tT + kDV, x0);
+          tmem_wait_ld();
+          if (rebase) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x0[e] *= gW;
+            tmem_st16(tT + kDV, x0);
+          }
+          put_sop16(sop, kSopAtom, kDV / 32, d, x0);
+        }
+        if (rebase) tmem_wait_st();
+        tc_fence_before();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar[kTFree]);
+          mbar_arrive(&bar[kSFull]);
+        }
+      }
+      // (2) output rows of chunk i-1: o_t = O[t, :Dv] / (O[t, Dv] + eps)
+      const int io = i - 1;
+      if (!warp_wait(&bar[kOFull], io & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      const int nv = min(kC, N - (cb + io) * kC);
+      __nv_bfloat16 *orow =
+          p.o + (static_cast<size_t>(bh) * N + static_cast<size_t>(cb + io) * kC + d) * kDV;
+      // first half stored before the second is loaded (at most 64 values live)
+      float inv;
+      {
+        float x[64];
+        const float den = tmem_ld1(to + kDV);
+        tmem_ld32(to, x);
+        tmem_ld32(to + 32, x + 32);
+        tmem_wait_ld();
+        inv = 1.f / (den + p.eps);
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e] * inv, x[2 * e + 1] * inv);
+        if (d < nv) store_row_half(orow, pk, p.o_v8);
+      }
+      {
+        float x[64];
+        tmem_ld32(to + 64, x);
+        tmem_ld32(to + 96, x + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&bar[kOFree]);
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e] * inv, x[2 * e + 1] * inv);
+        if (d < nv) store_row_half(orow + 64, pk, p.o_v8);
+      }
+    }
+  } else {
+    // ---------------- P = A' masked to s <= t, bf16 pairs in place ----------------
+    const int w = warp;  // TMEM lane quadrant
+    const int t = 32 * w + lane;
+    const uint32_t ta = tmem_addr(tmem, 32 * w, kColA);
+    phase_a_map(warp);
+    for (int i = 0; i < nch; ++i) {
+      if (!warp_wait(&bar[kAFull], i & 1, abort_flag, p.timeouts)) break;
+      tc_fence_after();
+      // A' columns [32 g, 32 g + 32) -> P pair columns [16 g, 16 g + 16): a
+      // block wholly above this warp's diagonal is zero without a load
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t pk[16];
+        if (g <= w) {
+          float a[32];
+          tmem_ld32(ta + 32 * g, a);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int s0 = 32 * g + 2 * e;
+            pk[e] = pack_bf16x2(s0 <= t ? a[2 * e] : 0.f, s0 + 1 <= t ? a[2 * e + 1] : 0.f);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = 0u;
+        }
+        tmem_st16u(ta + 16 * g, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kPFull]);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+int num_sms128() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 148;
+  return v;
+}
+
+size_t flag_bytes(int BH, int P) {
+  const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
+  return (flags + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+
+bool chunk128_supported(const Problem &p, const Gammas &g) {
+  if (p.dtype != kBF16 || p.D != kD || p.Dv != kDV || p.N <= 0) return false;
+  const long long rows = static_cast<long long>(p.B) * p.H;
+  if (rows <= 0 || rows * chunk128_parts(static_cast<int>(rows), p.N) >= (1LL << 31)) return false;
+  if (p.decay)
+    for (int h = 0; h < p.H; ++h)
+      if (!(g.g[h] >= kGammaMin)) return false;
+  return true;
+}
+
+int chunk128_parts(int BH, int N) {
+  // at most one wave of CTAs (one per SM); a part's CTA pays phase A and
+  // the chain links before it, so no more parts than minimise phase C +
+  // chain: P ~ sqrt(0.43 * (N / 64))
+  const int nch = (N + kC - 1) / kC;
+  if (BH <= 0 || nch <= 0) return 1;
+  int P = num_sms128() / BH;
+  const int pmax = static_cast<int>(sqrt(0.43 * ((N + 63) / 64)));
+  if (P > pmax) P = pmax;
+  if (P > nch) P = nch;
+  return P < 1 ? 1 : P;
+}
+
+size_t chunk128_workspace_bytes(int BH, int P) {
+  if (P <= 1) return 0;
+  return flag_bytes(BH, P) +
+         sizeof(float) * static_cast<size_t>(BH) * P * (static_cast<size_t>(kD) * kDV + kD);
+}
+
+cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, int P, cudaStream_t s) {
+  if (!chunk128_supported(p, g) || P < 1) return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  Chunk128Params prm = {};
+  if (!make_tmap_3d_bf16(&prm.tmQ, p.q, kD, p.N, BH, 64, kC, 128) ||
+      !make_tmap_3d_bf16(&prm.tmK, p.k, kD, p.N, BH, 64, kC, 128) ||
+      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 32, kC, 64))
+    return cudaErrorNotSupported;
+  prm.timeouts = wait_timeout_counter();
+  if (!prm.timeouts) return cudaErrorNotSupported;
+  prm.o = static_cast<__nv_bfloat16 *>(p.o);
+  prm.BH = BH;
+  prm.H = p.H;
+  prm.N = p.N;
+  prm.P = P;
+  prm.o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0 ? 1 : 0;
+  prm.eps = p.eps;
+  prm.lg = log2_gammas(g, p.H, p.decay);
+  if (P > 1) {
+    if (!ws) return cudaErrorInvalidValue;
+    // flags and ticket start at zero; the records need no initialisation
+    prm.ws_flag = static_cast<int *>(ws);
+    prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;
+    prm.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + flag_bytes(BH, P));
+    cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = p.decay ? chunk128_kernel<true> : chunk128_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (err != cudaSuccess) return err;
+  kern<<<BH * P, kThreads, kAlloc, s>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace linattn

@@ -151,25 +151,6 @@ struct ChunkParams {
   Gammas lg;  // log2(gamma) per head
 };
 
-// phi(x) = elu(x) + 1 on a pair of bf16 values, times a per-row scale:
-// exp(min(x, 0)) + max(x, 0), with exp(y) = 2^(y log2 e) on the packed bf16
-// exp2 unit.  log2 e is split into a bf16 head and tail so that the argument
-// carries one rounding only.
-__device__ __forceinline__ uint32_t phi_scale_bf16x2(uint32_t w, uint32_t scale2) {
-  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
-  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
-  const __nv_bfloat162 l2e_hi = __float2bfloat162_rn(1.4453125f);
-  const __nv_bfloat162 l2e_lo = __float2bfloat162_rn(1.4426950408889634f - 1.4453125f);
-  const __nv_bfloat162 m = __hmin2(x, zero);
-  const __nv_bfloat162 a = __hfma2(m, l2e_hi, __hmul2(m, l2e_lo));
-  uint32_t au = *reinterpret_cast<const uint32_t *>(&a), eu;
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(eu) : "r"(au));
-  const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162 *>(&eu);
-  __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
-  r = __hmul2(r, *reinterpret_cast<const __nv_bfloat162 *>(&scale2));
-  return *reinterpret_cast<const uint32_t *>(&r);
-}
-
 // phi and the row scales in place on NB boxes of 64 rows x 128 bytes.  Thread
 // tp (0..127) handles the 16-byte chunks tp + 128 m of every box, which lie in
 // rows (tp / 8) + 16 m, m = 0..3.
@@ -221,27 +202,6 @@ __device__ __forceinline__ void map_boxes_split(uint8_t *box0, uint8_t *lo0, flo
       reinterpret_cast<uint4 *>(lo0 + b * kBox)[tp] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   }
-}
-
-// Row d of [T | z] (fp32 values of 32 consecutive columns starting at column
-// 32 * atom) into the MN-major, 64-byte-swizzled bf16 operand.
-__device__ __forceinline__ void put_sop32(uint8_t *sop, int atom_bytes, int atom, int d,
-                                          const float *x) {
-  uint8_t *a = sop + atom * atom_bytes;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
-        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
-                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
-}
-__device__ __forceinline__ void put_sop16(uint8_t *sop, int atom_bytes, int atom, int d,
-                                          const float *x) {
-  uint8_t *a = sop + atom * atom_bytes;
-#pragma unroll
-  for (int q = 0; q < 2; ++q)
-    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
-        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
-                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
 }
 
 template <int D, int DV, int MODE, bool DECAY>

@@ -41,6 +41,14 @@ size_t chunk_causal_workspace_bytes(int BH, int P, int D, int Dv);
 Gammas log2_gammas(const Gammas &g, int H, bool decay);
 cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int P,
                                 cudaStream_t s);
+// The causal kernel with 128-token chunks for D = Dv = 128 (chunk128.cu):
+// bf16, every decay >= 0.61; workspace (flags and inclusive states) for P
+// parts, 0 for one part.
+bool chunk128_supported(const Problem &p, const Gammas &g);
+int chunk128_parts(int BH, int N);
+size_t chunk128_workspace_bytes(int BH, int P);
+cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, int P,
+                                   cudaStream_t s);
 // Final state S [BH][D][Dv], z [BH][D] of the causal recurrence over N tokens.
 cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
                                  int N, int D, int Dv, bool decay, const Gammas &g, void *ws,

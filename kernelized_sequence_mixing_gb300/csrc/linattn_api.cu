@@ -71,6 +71,7 @@ int la_causal_kernel(int B, int H, int N, int D, int Dv, const float *gamma,
   if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return -static_cast<int>(st);
   Problem p{nullptr, nullptr, nullptr, nullptr, B, H, N, D, Dv, decay, 0.f,
             dtype == LA_F32 ? kF32 : kBF16};
+  if (chunk128_supported(p, g)) return 2;
   return chunk_tc_supported(p, g) ? 1 : 0;
 }
 
@@ -122,6 +123,17 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
             dtype == LA_F32 ? kF32 : kBF16};
   const int BH = B * H;
   if (causal) {
+    if (chunk128_supported(p, g)) {
+      // 128-token chunks (D = Dv = 128); parts as below
+      const int P = chunk128_parts(BH, N);
+      const size_t wsb = chunk128_workspace_bytes(BH, P);
+      void *ws = nullptr;
+      if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
+      cudaError_t e = launch_causal_chunk128(p, g, ws, P, s);
+      cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+      if (e != cudaSuccess) return from_cuda(e);
+      return from_cuda(ef);
+    }
     if (chunk_tc_supported(p, g)) {
       // parts of the sequence run on separate SMs; the workspace carries the
       // state from one part to the next

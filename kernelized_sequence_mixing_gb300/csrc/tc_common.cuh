@@ -285,6 +285,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// phi(x) = elu(x) + 1 on a pair of bf16 values, times a per-row scale:
+// exp(min(x, 0)) + max(x, 0), with exp(y) = 2^(y log2 e) on the packed bf16
+// exp2 unit.  log2 e is split into a bf16 head and tail so that the argument
+// carries one rounding only.
+__device__ __forceinline__ uint32_t phi_scale_bf16x2(uint32_t w, uint32_t scale2) {
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 l2e_hi = __float2bfloat162_rn(1.4453125f);
+  const __nv_bfloat162 l2e_lo = __float2bfloat162_rn(1.4426950408889634f - 1.4453125f);
+  const __nv_bfloat162 m = __hmin2(x, zero);
+  const __nv_bfloat162 a = __hfma2(m, l2e_hi, __hmul2(m, l2e_lo));
+  uint32_t au = *reinterpret_cast<const uint32_t *>(&a), eu;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(eu) : "r"(au));
+  const __nv_bfloat162 e = *reinterpret_cast<const __nv_bfloat162 *>(&eu);
+  __nv_bfloat162 r = __hadd2(e, __hmax2(x, zero));
+  r = __hmul2(r, *reinterpret_cast<const __nv_bfloat162 *>(&scale2));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // ---- swizzled shared-memory addressing ---------------------------------------
 // Byte offset of (row, byte-in-row) in a tile of 128-byte rows with the
 // 128-byte swizzle (16-byte chunk index XOR row % 8); tile 1024-byte aligned.
@@ -296,6 +315,38 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int byte) {
 __device__ __forceinline__ uint32_t sw64_off(int row, int byte) {
   return static_cast<uint32_t>(row * 64 +
                                ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15)));
+}
+
+// Row d of [T | z] (fp32 values of 32 consecutive columns starting at column
+// 32 * atom) into the MN-major, 64-byte-swizzled bf16 operand.
+__device__ __forceinline__ void put_sop32(uint8_t *sop, int atom_bytes, int atom, int d,
+                                          const float *x) {
+  uint8_t *a = sop + atom * atom_bytes;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
+        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+}
+__device__ __forceinline__ void put_sop16(uint8_t *sop, int atom_bytes, int atom, int d,
+                                          const float *x) {
+  uint8_t *a = sop + atom * atom_bytes;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    *reinterpret_cast<uint4 *>(a + sw64_off(d, 16 * q)) =
+        make_uint4(pack_bf16x2(x[8 * q + 0], x[8 * q + 1]), pack_bf16x2(x[8 * q + 2], x[8 * q + 3]),
+                   pack_bf16x2(x[8 * q + 4], x[8 * q + 5]), pack_bf16x2(x[8 * q + 6], x[8 * q + 7]));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: row m of A in tensor-memory lane m, its
+// K values as bf16 pairs, 16 K values in 8 consecutive 32-bit columns.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 }  // namespace tc

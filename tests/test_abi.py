@@ -127,7 +127,9 @@ def test_decode_rejects_bad_arguments(lib):
 def test_causal_kernel_dispatch(lib):
     K = lib.la_causal_kernel
     g = lambda *x: (ctypes.c_float * len(x))(*x)  # noqa: E731
-    assert K(2, 16, 16384, 128, 128, None, BF16) == 1
+    assert K(2, 16, 16384, 128, 128, None, BF16) == 2           # 128-token chunks
+    assert K(2, 16, 16384, 128, 128, g(*[0.96875] * 16), BF16) == 2
+    assert K(1, 2, 100, 128, 128, g(0.6, 1.0), BF16) == 1       # too strong for 128
     assert K(4, 8, 4096, 64, 64, None, BF16) == 1
     assert K(1, 2, 100, 64, 128, g(0.35, 1.0), BF16) == 1
     assert K(1, 2, 100, 64, 128, g(0.34, 1.0), BF16) == 0   # strong decay

@@ -76,9 +76,12 @@ def test_causal_small(la, ora, dtype, gkind, shape):
     q, k, v = gen(B, H, N, D, Dv, dtype, seed=N + D + 7 * H)
     g = gammas_for(H, gkind)
     path = la.causal_kernel(B, H, N, D, Dv, gamma=g, dtype=dtype)
-    # "mix" always holds 0.0 for head 0, which sends the call to the CUDA cores
+    # "mix" always holds 0.0 for head 0, which sends the call to the CUDA
+    # cores; "mild" holds 0.35 and 0.5, too strong for 128-token chunks
     tc_expected = dtype == torch.bfloat16 and gkind != "mix"
-    assert path == ("tensor-core" if tc_expected else "cuda-core"), path
+    c128 = tc_expected and (D, Dv) == (128, 128) and gkind is None
+    assert path == ("tensor-core-128" if c128 else
+                    "tensor-core" if tc_expected else "cuda-core"), path
     o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
     torch.cuda.synchronize()
     ref = ora.causal(to_np(q), to_np(k), to_np(v),
@@ -110,6 +113,38 @@ def test_causal_parts_and_windows(la, ora, case):
     o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
     torch.cuda.synchronize()
     ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=g.numpy(), eps=1e-6)
+    err = max_row_error(to_np(o), ref)
+    assert err < 2e-2, err
+
+
+# The 128-token-chunk kernel (bf16, D = Dv = 128, every gamma >= 0.61): one
+# token, ragged single chunks, a chunk plus one token, windows of one chunk
+# (gamma = 0.61) and of several, several parts per head (few heads) with the
+# state crossing parts and windows, one part per head (many heads).
+CAUSAL128 = [
+    # (B, H, N, gammas)
+    (1, 1, 1, None),
+    (1, 2, 127, [0.61, 1.0]),
+    (2, 3, 129, [0.7, 0.9, 1.0]),
+    (1, 2, 1000, [0.61, 0.999]),
+    (1, 8, 5000, [0.8, 0.97, 1.0, 0.9]),
+    (1, 3, 20000, [0.61, 0.99, 1.0]),
+    (2, 76, 700, [0.75, 0.96875, 1.0, 0.999]),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL128, ids=lambda c: "x".join(map(str, c[:3])))
+def test_causal_chunk128(la, ora, case):
+    B, H, N, gl = case
+    D = Dv = 128
+    q, k, v = gen(B, H, N, D, Dv, torch.bfloat16, seed=3 * H + N)
+    g = None if gl is None else torch.tensor([gl[h % len(gl)] for h in range(H)],
+                                             dtype=torch.float32)
+    assert la.causal_kernel(B, H, N, D, Dv, gamma=g, dtype=torch.bfloat16) == "tensor-core-128"
+    o = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = ora.causal(to_np(q), to_np(k), to_np(v),
+                     gamma=None if g is None else g.numpy(), eps=1e-6)
     err = max_row_error(to_np(o), ref)
     assert err < 2e-2, err
 
@@ -328,17 +363,20 @@ def test_tensor_core_and_cuda_core_paths_agree(la, ora):
     spare head forces the CUDA-core kernel) against the oracle."""
     B, H, N, D, Dv = 1, 3, 777, 128, 128
     q, k, v = gen(B, H, N, D, Dv, torch.bfloat16, 77)
-    g_tc = torch.tensor([0.9, 0.99, 1.0])
+    g_128 = torch.tensor([0.9, 0.99, 1.0])
+    g_64 = torch.tensor([0.9, 0.99, 0.5])
     g_cc = torch.tensor([0.9, 0.99, 0.1])
-    assert la.causal_kernel(B, H, N, D, Dv, g_tc) == "tensor-core"
+    assert la.causal_kernel(B, H, N, D, Dv, g_128) == "tensor-core-128"
+    assert la.causal_kernel(B, H, N, D, Dv, g_64) == "tensor-core"
     assert la.causal_kernel(B, H, N, D, Dv, g_cc) == "cuda-core"
-    o_tc = to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=g_tc))
-    o_cc = to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=g_cc))
-    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=g_tc.numpy())
+    outs = [to_np(la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=g))
+            for g in (g_128, g_64, g_cc)]
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=g_128.numpy())
     for h in range(2):
-        assert max_row_error(o_tc[0, h], ref[0, h]) < 2e-2
-        assert max_row_error(o_cc[0, h], ref[0, h]) < 2e-2
-        assert max_row_error(o_tc[0, h], o_cc[0, h]) < 2e-2
+        for o in outs:
+            assert max_row_error(o[0, h], ref[0, h]) < 2e-2
+        for o in outs[:2]:
+            assert max_row_error(o[0, h], outs[2][0, h]) < 2e-2
 
 
 def test_zz_no_device_wait_timeouts(la):
