@@ -63,6 +63,8 @@ constexpr float kLog2Floor = -93.0139f;  // log2(1e-28): smallest factor in a wi
 //           swizzle, then the ones atom: column 0 = 1) = [V | 1]
 //   q tile: one slot, 2 boxes like k
 //   [T | z]: bf16, 5 atoms of 128 rows (d) x 64 bytes, 64-byte swizzle
+//   output staging: per state/output warp 32 rows x 64 bytes (32 columns of
+//           o), 64-byte swizzle, written back by TMA tile stores
 constexpr int kKBox = 128 * 128;
 constexpr int kVAtom = 128 * 64;
 constexpr int kKSlot = 2 * kKBox;
@@ -72,8 +74,10 @@ constexpr int kOffV = kOffK + 2 * kKSlot;
 constexpr int kOffQ = kOffV + 2 * kVSlot;
 constexpr int kSopAtom = kD * 64;
 constexpr int kOffSop = kOffQ + kKSlot;
+constexpr int kStgBytes = 32 * 64;
+constexpr int kOffStg = kOffSop + 5 * kSopAtom;
 constexpr int kNumBars = 24;
-constexpr int kOffBar = kOffSop + 5 * kSopAtom;
+constexpr int kOffBar = kOffStg + 4 * kStgBytes;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kBytes = kOffMisc + 32;
 constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
@@ -110,14 +114,12 @@ enum Bar : int {
 };
 
 struct Chunk128Params {
-  CUtensorMap tmQ, tmK, tmV;
-  __nv_bfloat16 *o;
+  CUtensorMap tmQ, tmK, tmV, tmO;
   float *rec;      // P > 1: inclusive states [B*H][P][D*Dv + D]
   int *ws_flag;    // P > 1: [B*H][P], 1 once incl_p is published
   int *ws_ticket;  // P > 1: part-major work counter
   unsigned int *timeouts;
   int BH, H, N, P;
-  int o_v8;  // o is 32-byte aligned: 256-bit stores
   float eps;
   Gammas lg;  // log2(gamma) per head
 };
@@ -164,23 +166,6 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
   tmem_st16(taddr, f);
-}
-
-// 64 bf16 (32 pairs) to global memory: 256-bit stores when the row is
-// 32-byte aligned, else 128-bit.
-__device__ __forceinline__ void store_row_half(__nv_bfloat16 *dst, const uint32_t *pk, int v8) {
-  if (v8) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * q),
-                   "r"(pk[8 * q]), "r"(pk[8 * q + 1]), "r"(pk[8 * q + 2]), "r"(pk[8 * q + 3]),
-                   "r"(pk[8 * q + 4]), "r"(pk[8 * q + 5]), "r"(pk[8 * q + 6]), "r"(pk[8 * q + 7])
-                   : "memory");
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      reinterpret_cast<uint4 *>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-  }
 }
 
 template <bool DECAY>
@@ -273,16 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   };
 
   // Phase A feature map, kh_s = gamma^(e_p - s) phi(k_s) with e_p the
-  // chunk-aligned end of the part, by all 16 compute warps: warp u maps
+  // chunk-aligned end of the part.  Phase A takes the chunks last first, so
+  // the k and v tiles phase C needs first are the most recent in L2.
+  // All 16 compute warps share the map: warp u maps
   // rows 32 (u % 4) + lane, 16-byte chunks [4 (u / 4), + 4) of the row
   // (box u / 8).
   auto phase_a_map = [&](int u) {
     const int r = 32 * (u & 3) + lane, quarter = u >> 2;
     for (int i = 0; i < nA; ++i) {
-      const int sl = i & 1;
+      const int sl = i & 1, ia = nA - 1 - i;  // last chunk first
       if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
-      const int nv = min(kC, N - (cb + i) * kC);
-      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nch - i) - 1 - r)) : 0u;
+      const int nv = min(kC, N - (cb + ia) * kC);
+      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nch - ia) - 1 - r)) : 0u;
       map_row4(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
       fence_async_smem();
       __syncwarp();
@@ -388,12 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int slots = lane == 2 ? 1 : 2;
       uint64_t *fullb = &bar[lane == 0 ? kKFull : (lane == 1 ? kVFull : kQFull)];
       uint64_t *emptyb = &bar[lane == 0 ? kKEmpty : (lane == 1 ? kVEmpty : kQEmpty)];
+      // first token row of ring chunk c: phase A last chunk first, then phase C
+      auto ring_row = [&](int c) {
+        return (cb + (lane == 2 ? c : (c < nA ? nA - 1 - c : c - nA))) * kC;
+      };
       int issued = 0;
       for (int c = 0; c < n; ++c) {
         const int sl = c % slots;
         const uint32_t ph = static_cast<uint32_t>((c / slots) & 1);
         if (!mbar_wait(&emptyb[sl], ph ^ 1, abort_flag, p.timeouts)) break;
-        const int row = (cb + (lane == 2 ? c : (c < nA ? c : c - nA))) * kC;
+        const int row = ring_row(c);
         mbar_arrive_expect_tx(&fullb[sl], lane == 1 ? 4 * kVAtom : kKSlot);
         if (lane == 1) {
           uint8_t *dst = sm + kOffV + sl * kVSlot;
@@ -408,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         // L2 prefetch of the tile two ring chunks ahead (its load waits for a slot)
         const int cp = c + 2;
         if (cp < n) {
-          const int rowp = (cb + (lane == 2 ? cp : (cp < nA ? cp : cp - nA))) * kC;
+          const int rowp = ring_row(cp);
           if (lane == 1) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) tma_prefetch_3d(map, 32 * a, rowp, bh);
@@ -588,6 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     const uint32_t tT = tmem_addr(tmem, 32 * w, kColT);
     const uint32_t to = tmem_addr(tmem, 32 * w, kColO);
     uint8_t *sop = sm + kOffSop;
+    uint8_t *stg = sm + kOffStg + w * kStgBytes;
+    if (lane == 0) prefetch_tmap(&p.tmO);
     phase_a_map(warp);
     chain_part(w, d);
     const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
@@ -644,41 +637,43 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           mbar_arrive(&bar[kSFull]);
         }
       }
-      // (2) output rows of chunk i-1: o_t = O[t, :Dv] / (O[t, Dv] + eps)
+      // (2) output rows of chunk i-1: o_t = O[t, :Dv] / (O[t, Dv] + eps),
+      // 32 columns at a time through this warp's staging tile and a TMA
+      // store (rows past the sequence end are clipped by the tensor map)
       const int io = i - 1;
       if (!warp_wait(&bar[kOFull], io & 1, abort_flag, p.timeouts)) break;
       tc_fence_after();
-      const int nv = min(kC, N - (cb + io) * kC);
-      __nv_bfloat16 *orow =
-          p.o + (static_cast<size_t>(bh) * N + static_cast<size_t>(cb + io) * kC + d) * kDV;
-      // first half stored before the second is loaded (at most 64 values live)
-      float inv;
-      {
-        float x[64];
-        const float den = tmem_ld1(to + kDV);
-        tmem_ld32(to, x);
-        tmem_ld32(to + 32, x + 32);
+      float inv = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < kDV / 32; ++j) {
+        float x[32], den = 0.f;
+        tmem_ld32(to + 32 * j, x);
+        if (j == 0) den = tmem_ld1(to + kDV);
         tmem_wait_ld();
-        inv = 1.f / (den + p.eps);
-        uint32_t pk[32];
+        if (j == 0) inv = 1.f / (den + p.eps);
+        if (j == kDV / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_relaxed(&bar[kOFree]);
+        }
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e] * inv, x[2 * e + 1] * inv);
-        if (d < nv) store_row_half(orow, pk, p.o_v8);
-      }
-      {
-        float x[64];
-        tmem_ld32(to + 64, x);
-        tmem_ld32(to + 96, x + 32);
-        tmem_wait_ld();
-        tc_fence_before();
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e] * inv, x[2 * e + 1] * inv);
+        if (lane == 0) bulk_wait_group_read0();  // the previous store has read the tile
         __syncwarp();
-        if (lane == 0) mbar_arrive_relaxed(&bar[kOFree]);
-        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e] * inv, x[2 * e + 1] * inv);
-        if (d < nv) store_row_half(orow + 64, pk, p.o_v8);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4 *>(stg + sw64_off(lane, 16 * q)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tmO, stg, 32 * j, (cb + io) * kC + 32 * w, bh);
+          bulk_commit_group();
+        }
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store complete before the CTA exits
   } else {
     // ---------------- P = A' masked to s <= t, bf16 pairs in place ----------------
     const int w = warp;  // TMEM lane quadrant
@@ -771,16 +766,15 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   Chunk128Params prm = {};
   if (!make_tmap_3d_bf16(&prm.tmQ, p.q, kD, p.N, BH, 64, kC, 128) ||
       !make_tmap_3d_bf16(&prm.tmK, p.k, kD, p.N, BH, 64, kC, 128) ||
-      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 32, kC, 64))
+      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 32, kC, 64) ||
+      !make_tmap_3d_bf16(&prm.tmO, p.o, kDV, p.N, BH, 32, 32, 64))
     return cudaErrorNotSupported;
   prm.timeouts = wait_timeout_counter();
   if (!prm.timeouts) return cudaErrorNotSupported;
-  prm.o = static_cast<__nv_bfloat16 *>(p.o);
   prm.BH = BH;
   prm.H = p.H;
   prm.N = p.N;
   prm.P = P;
-  prm.o_v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0 ? 1 : 0;
   prm.eps = p.eps;
   prm.lg = log2_gammas(g, p.H, p.decay);
   if (P > 1) {
