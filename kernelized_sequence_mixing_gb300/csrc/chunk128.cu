@@ -113,6 +113,18 @@ enum Bar : int {
   kDrain = 21,
 };
 
+// Part boundaries (in chunks): equal parts.  The CTA of part p > 0 runs
+// phase A over part p - 1 and then, once every earlier part's sum is
+// published, phase C over part p; part 0 runs phase C only.  Every part
+// p >= 2 waits for the sums of all earlier parts, so the slowest phase A
+// sets the start of its phase C: equal parts keep those equal.
+__host__ __device__ __forceinline__ int part_begin(int p, int P, int nch_all) {
+  if (p <= 0) return 0;
+  if (p >= P) return nch_all;
+  const int base = nch_all / P, rem = nch_all % P;
+  return p * base + (p < rem ? p : rem);
+}
+
 struct Chunk128Params {
   CUtensorMap tmQ, tmK, tmV, tmO;
   float *rec;      // P > 1: inclusive states [B*H][P][D*Dv + D]
@@ -236,15 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const int part = item[0], bh = item[1];
 
-  // the part: chunks [cb, cb + nch) of this (batch, head)
+  // the part: chunks [cb, cb + nch) of this (batch, head); phase A runs
+  // over the previous part, chunks [cbA, cbA + nA)
   const int nch_all = (N + kC - 1) / kC;
-  const int pbase = nch_all / P, prem = nch_all % P;
-  const int cb = part * pbase + min(part, prem);
-  const int nch = pbase + (part < prem ? 1 : 0);
-  const int len = min(N, (cb + nch) * kC) - cb * kC;
-  const bool hasA = part < P - 1;
-  const bool needPrev = part > 0;
-  const int nA = hasA ? nch : 0;
+  const int cb = part_begin(part, P, nch_all);
+  const int nch = part_begin(part + 1, P, nch_all) - cb;
+  const bool hasA = part > 0;
+  const int cbA = hasA ? part_begin(part - 1, P, nch_all) : 0;
+  const int nA = hasA ? cb - cbA : 0;
   const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
   int WC = 64;  // chunks per decay window
   if (DECAY && lg < 0.f) {
@@ -252,24 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     WC = c < 1.f ? 1 : (c > 64.f ? 64 : static_cast<int>(c));
   }
   const int W = kC * WC;
+  auto phase_a_chunk = [&](int i) { return part == 1 ? i : nA - 1 - i; };
   auto scale2 = [&](float e) -> uint32_t {  // gamma^e as a bf16 pair
     const float f = DECAY ? exp2f(e * lg) : 1.f;
     return pack_bf16x2(f, f);
   };
 
-  // Phase A feature map, kh_s = gamma^(e_p - s) phi(k_s) with e_p the
-  // chunk-aligned end of the part.  Phase A takes the chunks last first, so
-  // the k and v tiles phase C needs first are the most recent in L2.
-  // All 16 compute warps share the map: warp u maps
-  // rows 32 (u % 4) + lane, 16-byte chunks [4 (u / 4), + 4) of the row
-  // (box u / 8).
+  // Phase A feature map over the previous part, kh_s = gamma^(E - 1 - s)
+  // phi(k_s) with E the end of that part (a chunk boundary).  Phase A takes
+  // the chunks of parts 1, 2, ... last first, so that the tiles the owner of
+  // that part reads first in its phase C are the most recent in L2; part 0
+  // (read in phase C from time zero) goes first chunk first, ahead of its
+  // owner.  All 16 compute warps share the map: warp u maps rows
+  // 32 (u % 4) + lane, 16-byte chunks [4 (u / 4), + 4) of the row (box u / 8).
   auto phase_a_map = [&](int u) {
     const int r = 32 * (u & 3) + lane, quarter = u >> 2;
     for (int i = 0; i < nA; ++i) {
-      const int sl = i & 1, ia = nA - 1 - i;  // last chunk first
+      const int sl = i & 1, ia = phase_a_chunk(i);
       if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
-      const int nv = min(kC, N - (cb + ia) * kC);
-      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nch - ia) - 1 - r)) : 0u;
+      const int nv = min(kC, N - (cbA + ia) * kC);
+      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
       map_row4(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
       fence_async_smem();
       __syncwarp();
@@ -277,91 +290,95 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     }
   };
 
-  // Before phase C, run by the state/output warps, thread c = d = 32 w +
-  // lane on row d: S0 = incl_(p-1) (0 for the first part); incl_p =
-  // A_p + gamma^len S0 is published for the next part unless this is the
-  // last; T = gamma^W S0 goes to tensor memory and, in bf16, to [T | z].
-  auto chain_part = [&](int w, int c) {
-    const int d = 32 * w + lane;
-    const uint32_t tT = tmem_addr(tmem, 32 * w, kColT);
-    uint8_t *sop = sm + kOffSop;
-    const bool pub = hasA;
-    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
-    const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
-    const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+  // Before phase C, by the 16 compute warps (warp u: rows 32 (u % 4) +
+  // lane, columns [32 (u / 4), + 32) of S; warps 0-3 also z): the state
+  // before the part, S0 = sum_(j < part) gamma^(c0 - E_j) A_j (c0 = the
+  // part's first token, E_j = the end of part j, A_j = part j's own sum
+  // scaled to E_j).  A_(part-1) is this CTA's phase A, in tensor memory; it
+  // is published for the later parts that need it.  A_j, j < part - 1, was
+  // published by the CTA of part j + 1 (a flag per record, release/acquire
+  // at GPU scope; parts are started in part-major order by an atomic ticket,
+  // so every wait ends).  T = gamma^W S0 goes to tensor memory and, in
+  // bf16, to [T | z].
+  auto look_back = [&](int u) {
+    const int qd = u & 3, g4 = u >> 2;
+    const int d = 32 * qd + lane;
+    const bool zcol = g4 == 0;
+    const uint32_t tS = tmem_addr(tmem, 32 * qd, kColT + 32 * g4);
+    const uint32_t tZ = tmem_addr(tmem, 32 * qd, kColT + kDV);
+    float acc[32], accz = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     if (hasA) {
       warp_wait(&bar[kTReady], 0, abort_flag, p.timeouts);
       tc_fence_after();
-    }
-    if (needPrev) {
-      if (c == 0) {
-        const int *f = p.ws_flag + bh * P + part - 1;
-        const long long t0 = clock64();
-        while (ld_acquire_gpu(f) == 0) {
-          if (*abort_flag) break;
-          if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            atomicAdd(p.timeouts, 1u);
-            break;
-          }
-          __nanosleep(32);
-        }
-      }
-      named_sync(1, 128);
-    }
-    const float *prev = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
-    float *dst = p.rec + (static_cast<size_t>(bh) * P + part) * kRec;
-#pragma unroll 1
-    for (int cc = 0; cc < kDV / 32; ++cc) {
-      float x[32], t[32];
-      if (hasA) tmem_ld32(tT + 32 * cc, t);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (needPrev) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * kDV + 32 * cc) + q);
-        x[4 * q] = v4.x;
-        x[4 * q + 1] = v4.y;
-        x[4 * q + 2] = v4.z;
-        x[4 * q + 3] = v4.w;
-      }
-      if (hasA) tmem_wait_ld();
-      if (pub) {
-        float4 *o4 = reinterpret_cast<float4 *>(dst + d * kDV + 32 * cc);
+      tmem_ld32(tS, acc);
+      if (zcol) accz = tmem_ld1(tZ);
+      tmem_wait_ld();
+      if (part < P - 1) {  // A_(part-1) is read by the parts after this one
+        float *rec = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          o4[q] = make_float4(fmaf(gLen, x[4 * q], corr * t[4 * q]),
-                              fmaf(gLen, x[4 * q + 1], corr * t[4 * q + 1]),
-                              fmaf(gLen, x[4 * q + 2], corr * t[4 * q + 2]),
-                              fmaf(gLen, x[4 * q + 3], corr * t[4 * q + 3]));
+          __stcg(reinterpret_cast<float4 *>(rec) + (8 * g4 + q) * kD + d,
+                 make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+        if (zcol) __stcg(rec + kD * kDV + d, accz);
+        __threadfence();
       }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] *= gW;
-      tmem_st32(tT + 32 * cc, x);
-      put_sop32(sop, kSopAtom, cc, d, x);
     }
-    {
-      float sp[16], tz[16];
-      if (hasA) {
-        tmem_ld16(tT + kDV, tz);
-        tmem_wait_ld();
+    named_sync(1, 512);
+    if (hasA && part < P - 1 && tid == 0) st_release_gpu(p.ws_flag + bh * P + part - 1, 1);
+    if (part >= 2) {
+      if (tid == 0) {
+        const long long t0 = clock64();
+        for (int j = 0; j < part - 1 && !*abort_flag; ++j) {
+          const int *f = p.ws_flag + bh * P + j;
+          while (ld_acquire_gpu(f) == 0) {
+            if (*abort_flag) break;
+            if (clock64() - t0 > kWaitCycles) {
+              *abort_flag = 1;
+              atomicAdd(p.timeouts, 1u);
+              break;
+            }
+            __nanosleep(32);
+          }
+        }
       }
+      named_sync(1, 512);
+      for (int j = 0; j < part - 1 && !*abort_flag; ++j) {
+        const float wj =
+            DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1, P, nch_all)) * kC) * lg) : 1.f;
+        const float *rec = p.rec + (static_cast<size_t>(bh) * P + j) * kRec;
+        float4 v[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) sp[e] = 0.f;
-      if (needPrev) sp[0] = __ldcg(prev + kD * kDV + d);
-      if (pub) dst[kD * kDV + d] = fmaf(gLen, sp[0], hasA ? corr * tz[0] : 0.f);
-      sp[0] *= gW;
-      tmem_st16(tT + kDV, sp);
-      put_sop16(sop, kSopAtom, kDV / 32, d, sp);
+        for (int q = 0; q < 8; ++q) v[q] = __ldcg(reinterpret_cast<const float4 *>(rec) + (8 * g4 + q) * kD + d);
+        const float vz = zcol ? __ldcg(rec + kD * kDV + d) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          acc[4 * q] = fmaf(wj, v[q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(wj, v[q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(wj, v[q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(wj, v[q].w, acc[4 * q + 3]);
+        }
+        accz = fmaf(wj, vz, accz);
+      }
+    }
+    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] *= gW;
+    tmem_st32(tS, acc);
+    put_sop32(sm + kOffSop, kSopAtom, g4, d, acc);
+    if (zcol) {
+      float zz[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) zz[e] = 0.f;
+      zz[0] = accz * gW;
+      tmem_st16(tZ, zz);
+      put_sop16(sm + kOffSop, kSopAtom, kDV / 32, d, zz);
     }
     tmem_wait_st();
     tc_fence_before();
     fence_async_smem();
-    named_sync(1, 128);
-    if (pub && c == 0) {
-      // the state is visible device-wide before the flag
-      __threadfence();
-      st_release_gpu(p.ws_flag + bh * P + part, 1);
-    }
+    named_sync(1, 512);
   };
 
   if (warp == kWarpTma) {
@@ -375,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int slots = lane == 2 ? 1 : 2;
       uint64_t *fullb = &bar[lane == 0 ? kKFull : (lane == 1 ? kVFull : kQFull)];
       uint64_t *emptyb = &bar[lane == 0 ? kKEmpty : (lane == 1 ? kVEmpty : kQEmpty)];
-      // first token row of ring chunk c: phase A last chunk first, then phase C
+      // first token row of ring chunk c: phase A (previous part), then phase C
       auto ring_row = [&](int c) {
-        return (cb + (lane == 2 ? c : (c < nA ? nA - 1 - c : c - nA))) * kC;
+        return (lane == 2 ? cb + c : (c < nA ? cbA + phase_a_chunk(c) : cb + c - nA)) * kC;
       };
       int issued = 0;
       for (int c = 0; c < n; ++c) {
@@ -533,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     const int r = 32 * qd + lane;      // token row of the chunk
     phase_a_map(warp);
     const uint32_t tq = tmem_addr(tmem, 32 * qd, kColQ + 32 * h);
+    bool looked = false;  // the look-back runs once, after chunk 0 is mapped
     for (int i = 0; i < nch; ++i) {
       const int c = nA + i, sl = c & 1;
       const int nv = min(kC, N - (cb + i) * kC);
@@ -571,7 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kQReady]);
+      if (i == 0) {
+        look_back(warp);
+        looked = true;
+      }
     }
+    if (!looked) look_back(warp);
   } else if (warp >= kWarpS) {
     // ---------------- state, then output rows ----------------
     const int w = warp - kWarpS;  // TMEM lane quadrant
@@ -582,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     uint8_t *stg = sm + kOffStg + w * kStgBytes;
     if (lane == 0) prefetch_tmap(&p.tmO);
     phase_a_map(warp);
-    chain_part(w, d);
+    look_back(warp);
     const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
     if (lane == 0) {  // the chain is done (chain_part ends with a barrier)
       mbar_arrive(&bar[kTFree]);
@@ -680,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     const int t = 32 * w + lane;
     const uint32_t ta = tmem_addr(tmem, 32 * w, kColA);
     phase_a_map(warp);
+    look_back(warp);
     for (int i = 0; i < nch; ++i) {
       if (!warp_wait(&bar[kAFull], i & 1, abort_flag, p.timeouts)) break;
       tc_fence_after();

@@ -373,8 +373,9 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
 }  // namespace tc
 
 // Host: encode a rank-3 bf16 tensor map over a dense [z][y][x] array
-// (x innermost), box (box_x, box_y, 1), swizzle of 64 or 128 bytes, zero fill
-// out of bounds.  Returns false if the driver rejects it.
+// (x innermost), box (box_x, box_y, 1), swizzle of 32, 64 or 128 bytes (0:
+// none), zero fill out of bounds.  Returns false for another swizzle value
+// or if the driver rejects the map.
 bool make_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t dim_x, uint64_t dim_y,
                        uint64_t dim_z, uint32_t box_x, uint32_t box_y, int swizzle_bytes);
 

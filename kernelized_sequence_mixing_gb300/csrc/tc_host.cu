@@ -36,10 +36,14 @@ bool make_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t dim_x, uint6
   const cuuint64_t strides[2] = {dim_x * 2, dim_x * dim_y * 2};  // bytes, dims 1..2
   const cuuint32_t box[3] = {box_x, box_y, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw =
-      swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                           : (swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                  : CU_TENSOR_MAP_SWIZZLE_NONE);
+  CUtensorMapSwizzle sw;
+  switch (swizzle_bytes) {
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+    default: return false;
+  }
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
