@@ -61,6 +61,11 @@ WORKLOADS = {
     "causal_decay_bf16_n16384": Workload("causal_decay_bf16_n16384", True, 2,
                                          16, 16384, 128, 128, torch.bfloat16,
                                          0.5, 2, decayed=True),
+    # the same at half the sequence length (same grid of CTAs, 268 MB of
+    # inputs, above the L2 size): the case for multi-pass counter captures
+    "causal_decay_bf16_n8192": Workload("causal_decay_bf16_n8192", True, 2,
+                                        16, 8192, 128, 128, torch.bfloat16,
+                                        0.5, 2, decayed=True),
     # non-causal, bf16, B8 H16 N65536 D=Dv=64, seed 3
     "noncausal_bf16_n65536": Workload("noncausal_bf16_n65536", False, 8, 16,
                                       65536, 64, 64, torch.bfloat16, 0.5, 3),
