@@ -18,13 +18,14 @@
 //            carries about 16 significant bits),
 //              A_p = sum_(s in part) gamma^(e_p - s) phi(k_s) [v_s | 1]^T,
 //            e_p = the part's last token.
-//   causal mode (one kernel): every part but the last runs phase A, then
-//            takes the inclusive state of part p-1 from the CTA that owns it
-//            (a flag in device memory) and publishes its own,
-//              incl_p = A_p + gamma^len_p incl_(p-1);
+//   causal mode (one kernel): the CTA of part p > 0 runs phase A over part
+//            p - 1, publishes A_(p-1) for the later parts, reads A_j, j < p - 1
+//            (published by the CTA of part j + 1; a flag per record), and
+//            starts from the state before its part,
+//              S0 = sum_(j < p) gamma^(c0 - E_j) A_j   (E_j = end of part j);
 //            parts are handed out in part-major order by an atomic ticket, so
-//            the owner of part p-1 has already started and every wait ends.
-//            Then phase C runs the part's chunks in order from incl_(p-1).
+//            the CTAs it waits for have already started and every wait ends.
+//            Part 0 starts from zero.  Then phase C runs the part's chunks.
 //            For a chunk at c0 inside a decay window ending at E (windows of
 //            W tokens from the part's start, W chosen so gamma^W stays far
 //            above the bf16 range limit):
@@ -139,11 +140,12 @@ struct Lay {
 struct ChunkParams {
   CUtensorMap tmQ, tmK, tmV;
   __nv_bfloat16 *o;
-  // per-part records [B*H][rec_parts][D*Dv + D] (S rows, then z): state mode
-  // writes A_p; causal mode the inclusive states incl_p; apply mode reads
-  // the sum in slot 0 of its (batch, head)
+  // per-part records [B*H][rec_parts][D*Dv + D]: state mode writes A_p (S
+  // rows, then z); causal mode A_(p-1) column-group-major (float4 of
+  // columns 4g..4g+3 of row d at g * D + d, then z); apply mode reads the
+  // sum in slot 0 of its (batch, head)
   float *rec;
-  int *ws_flag;    // causal, P > 1: [B*H][P], 1 once incl_p is published
+  int *ws_flag;    // causal, P > 1: [B*H][P], 1 once A_p is published
   int *ws_ticket;  // causal, P > 1: part-major work counter
   unsigned int *timeouts;
   int BH, H, N, P, rec_parts;
@@ -286,14 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const int part = item[0], bh = item[1];
 
-  // the part: chunks [cb, cb + nch) of this (batch, head)
+  // the part: chunks [cb, cb + nch) of this (batch, head).  Phase A runs
+  // over chunks [cbA, cbA + nA): the part itself in state mode, the previous
+  // part in causal mode.
   const int nch_all = (N + kC - 1) / kC;
   const int pbase = nch_all / P, prem = nch_all % P;
-  const int cb = part * pbase + min(part, prem);
+  auto part_begin = [&](int q) { return q * pbase + min(q, prem); };
+  const int cb = part_begin(part);
   const int nch = pbase + (part < prem ? 1 : 0);
   const int len = min(N, (cb + nch) * kC) - cb * kC;
-  const bool hasA = MODE == kState || (MODE == kCausal && part < P - 1);
-  const bool needPrev = MODE == kCausal && part > 0;
+  const bool hasA = MODE == kState || (MODE == kCausal && part > 0);
+  const int cbA = MODE == kCausal && part > 0 ? part_begin(part - 1) : cb;
+  const int nA = !hasA ? 0 : (MODE == kCausal ? cb - cbA : nch);
   (void)prun;
   const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
   int WC = 64;  // chunks per decay window
@@ -310,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   auto phase_a_map = [&](int tp) {
     int s = 0;
     uint32_t ph = 0;
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < nA; ++i) {
       if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
-      const int nv = min(kC, N - (cb + i) * kC);
+      const int nv = min(kC, N - (cbA + i) * kC);
       uint8_t *st = sm + s * L::kStageBytes;
-      const int e0 = kC * nch - 1 - kC * i;
+      const int e0 = kC * nA - 1 - kC * i;
       if (MODE == kState) {
         const int row = tp >> 3;
         float f = DECAY ? exp2f(static_cast<float>(e0 - row) * lg) : 1.f;
@@ -341,94 +347,122 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     }
   };
 
-  // Causal mode, before phase C, run by the state warps (columns
-  // [0, Dv/2)) and the output warps (columns [Dv/2, Dv) and z) together:
-  // S0 = incl_(p-1) (0 for the first part); incl_p = A_p + gamma^len_p S0 is
-  // published for the next part unless this is the last; T = gamma^W S0 goes
-  // to tensor memory and, in bf16, to the [T | z] operand.  Thread c of the
-  // 256 handles row d = 32 w + lane.
-  auto chain_part = [&](int w, int cc0, int cc1, bool with_z, int c) {
-    const int d = 32 * w + lane;
-    const bool act = d < D;
-    const uint32_t tT = tmem_addr(tmem, 32 * w, L::kColT);
+  // Causal mode, before phase C, by the state and output warps (w8 = 0..7:
+  // rows 32 (w8 % 4) + lane, columns [Dv/2 (w8 / 4), + Dv/2); w8 >= 4 also
+  // z).  The state before the part is S0 = sum_(j < part) gamma^(c0 - E_j)
+  // A_j (c0 = the part's first token, E_j = the end of part j, A_j = part
+  // j's own sum scaled to E_j).  This CTA's phase A summed A_(part-1) in
+  // tensor memory; it is published for the later parts that need it
+  // (column-group-major records: float4 of columns 4g..4g+3 of row d at
+  // g * D + d, then z; a flag per record, release/acquire at GPU scope).
+  // A_j for j < part - 1 was published by the CTA of part j + 1; parts are
+  // started in part-major order by an atomic ticket, so every wait ends.
+  // T = gamma^W S0 goes to tensor memory and, in bf16, to [T | z].
+  auto look_back = [&](int w8, int c) {
+    const int qd = w8 & 3, hf = w8 >> 2;
+    const int d = 32 * qd + lane;
+    const bool act = d < D, zcol = hf == 1;
+    const uint32_t tT = tmem_addr(tmem, 32 * qd, L::kColT);
     uint8_t *sop = sm + L::kOffSop;
-    const bool pub = part < P - 1;
-    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
-    const float gLen = DECAY ? exp2f(static_cast<float>(len) * lg) : 1.f;
-    const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
+    constexpr int NG = DV / 64;  // 32-column groups per thread
+    const int g0 = hf * NG;
     if (hasA) {
       warp_wait(T_ready, 0, abort_flag, p.timeouts);
       tc_fence_after();
+      if (part < P - 1) {  // A_(part-1) is read by the parts after this one
+        float *rec = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
+#pragma unroll 1
+        for (int g = g0; g < g0 + NG; ++g) {
+          float x[32];
+          tmem_ld32(tT + 32 * g, x);
+          tmem_wait_ld();
+          if (act)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(reinterpret_cast<float4 *>(rec) + (8 * g + q) * D + d,
+                     make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+        }
+        if (zcol) {
+          const float zd = tmem_ld1(tT + DV);
+          tmem_wait_ld();
+          if (act) __stcg(rec + D * DV + d, zd);
+        }
+        __threadfence();
+      }
     }
-    if (needPrev) {
+    named_sync(1, 256);
+    if (hasA && part < P - 1 && c == 0) st_release_gpu(p.ws_flag + bh * P + part - 1, 1);
+    if (part >= 2) {
       if (c == 0) {
-        const int *f = p.ws_flag + bh * P + part - 1;
         const long long t0 = clock64();
-        while (ld_acquire_gpu(f) == 0) {
-          if (*abort_flag) break;
-          if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            atomicAdd(p.timeouts, 1u);
-            break;
+        for (int j = 0; j < part - 1 && !*abort_flag; ++j) {
+          const int *f = p.ws_flag + bh * P + j;
+          while (ld_acquire_gpu(f) == 0) {
+            if (*abort_flag) break;
+            if (clock64() - t0 > kWaitCycles) {
+              *abort_flag = 1;
+              atomicAdd(p.timeouts, 1u);
+              break;
+            }
+            __nanosleep(32);
           }
-          __nanosleep(32);
         }
       }
       named_sync(1, 256);
     }
-    const float *prev = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
-    float *dst = p.rec + (static_cast<size_t>(bh) * P + part) * kRec;
+    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
 #pragma unroll 1
-    for (int cc = cc0; cc < cc1; ++cc) {
-      float x[32], t[32];
-      if (hasA) tmem_ld32(tT + 32 * cc, t);
+    for (int g = g0; g < g0 + NG; ++g) {
+      float acc[32];
+      if (hasA) {
+        tmem_ld32(tT + 32 * g, acc);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (needPrev && act) v4 = __ldcg(reinterpret_cast<const float4 *>(prev + d * DV + 32 * cc) + q);
-        x[4 * q] = v4.x;
-        x[4 * q + 1] = v4.y;
-        x[4 * q + 2] = v4.z;
-        x[4 * q + 3] = v4.w;
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
       }
-      if (hasA) tmem_wait_ld();
-      if (pub && act) {
-        float4 *o4 = reinterpret_cast<float4 *>(dst + d * DV + 32 * cc);
+      for (int j = 0; j < part - 1; ++j) {
+        const float wj = DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1)) * kC) * lg) : 1.f;
+        const float *rec = p.rec + (static_cast<size_t>(bh) * P + j) * kRec;
+        float4 v[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          o4[q] = make_float4(fmaf(gLen, x[4 * q], hasA ? corr * t[4 * q] : 0.f),
-                              fmaf(gLen, x[4 * q + 1], hasA ? corr * t[4 * q + 1] : 0.f),
-                              fmaf(gLen, x[4 * q + 2], hasA ? corr * t[4 * q + 2] : 0.f),
-                              fmaf(gLen, x[4 * q + 3], hasA ? corr * t[4 * q + 3] : 0.f));
+          v[q] = act ? __ldcg(reinterpret_cast<const float4 *>(rec) + (8 * g + q) * D + d)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          acc[4 * q] = fmaf(wj, v[q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(wj, v[q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(wj, v[q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(wj, v[q].w, acc[4 * q + 3]);
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] *= gW;
-      tmem_st32(tT + 32 * cc, x);
-      if (act) put_sop32(sop, L::kSopAtom, cc, d, x);
+      for (int e = 0; e < 32; ++e) acc[e] *= gW;
+      tmem_st32(tT + 32 * g, acc);
+      if (act) put_sop32(sop, L::kSopAtom, g, d, acc);
     }
-    if (with_z) {
-      float sp[16], tz[16];
+    if (zcol) {
+      float zz[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) zz[e] = 0.f;
       if (hasA) {
-        tmem_ld16(tT + DV, tz);
+        zz[0] = tmem_ld1(tT + DV);
         tmem_wait_ld();
       }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) sp[e] = 0.f;
-      if (needPrev && act) sp[0] = __ldcg(prev + D * DV + d);
-      if (pub && act) dst[D * DV + d] = fmaf(gLen, sp[0], hasA ? corr * tz[0] : 0.f);
-      sp[0] *= gW;
-      tmem_st16(tT + DV, sp);
-      if (act) put_sop16(sop, L::kSopAtom, DV / 32, d, sp);
+      for (int j = 0; j < part - 1; ++j) {
+        const float wj = DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1)) * kC) * lg) : 1.f;
+        const float *rec = p.rec + (static_cast<size_t>(bh) * P + j) * kRec;
+        if (act) zz[0] = fmaf(wj, __ldcg(rec + D * DV + d), zz[0]);
+      }
+      zz[0] *= gW;
+      tmem_st16(tT + DV, zz);
+      if (act) put_sop16(sop, L::kSopAtom, DV / 32, d, zz);
     }
     tmem_wait_st();
     tc_fence_before();
     fence_async_smem();
     named_sync(1, 256);
-    if (pub && c == 0) {
-      // the state is visible device-wide before the flag
-      __threadfence();
-      st_release_gpu(p.ws_flag + bh * P + part, 1);
-    }
   };
 
   if (warp == kWarpTma) {
@@ -438,14 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       prefetch_tmap(&p.tmV);
       if (kPhaseC) prefetch_tmap(&p.tmQ);
     }
-    const int nA = hasA ? nch : 0, nC = kPhaseC ? nch : 0;
+    const int nC = kPhaseC ? nch : 0;
     int s = 0, issued = 0;
     uint32_t ph = 0;
     for (int it = 0; it < nA + nC; ++it) {
       if (!warp_wait(&empty[s], ph ^ 1, abort_flag, p.timeouts)) break;
       if (lane == 0) {
         const bool phaseA = it < nA;
-        const int row = (cb + (phaseA ? it : it - nA)) * kC;
+        const int row = (phaseA ? cbA + it : cb + it - nA) * kC;
         const bool wq = !phaseA, wkv = phaseA || MODE != kApply;
         uint8_t *st = sm + s * L::kStageBytes;
         mbar_arrive_expect_tx(&full[s], (wq ? L::KB * kBox : 0) + (wkv ? (L::KB + L::VB) * kBox : 0));
@@ -503,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     uint32_t ph = 0;
     bool ok = true;
     // phase A: T = kh^T [V | 1] over the part
-    for (int i = 0; hasA && i < nch; ++i) {
+    for (int i = 0; i < nA; ++i) {
       if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) {
         ok = false;
         break;
@@ -631,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     const int tp = tid - kWarpPhi * 32;
     const int r0 = tp >> 3;
     if (hasA) phase_a_map(MODE == kState ? tid : tp);
-    int s = (hasA ? nch : 0) % S;
-    uint32_t ph = static_cast<uint32_t>(((hasA ? nch : 0) / S) & 1);
+    int s = nA % S;
+    uint32_t ph = static_cast<uint32_t>((nA / S) & 1);
     for (int i = 0; kPhaseC && i < nch; ++i) {
       if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
       const int nv = min(kC, N - (cb + i) * kC);
@@ -673,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     // ---------------- output rows ----------------
     if (MODE == kState) phase_a_map(tid);
     const int w = warp - kWarpO;  // TMEM lane quadrant
-    if (MODE == kCausal) chain_part(w, DV / 64, DV / 32, true, 128 + tid - kWarpO * 32);
+    if (MODE == kCausal) look_back(4 + w, 128 + tid - kWarpO * 32);
     const int t = 16 * w + lane;  // M = 64 layout: rows 16w..16w+15 in lanes 0..15
     for (int i = 0; kPhaseC && i < nch; ++i) {
       const int b = i & 1;
@@ -781,10 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       tmem_wait_ld();
       if (act) aS[D * DV + d] = corr * tz[0];
     } else {
-      chain_part(w, 0, DV / 64, false, tid - kWarpS * 32);
+      look_back(w, tid - kWarpS * 32);
       const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
       if (kPhaseC) {
-        if (lane == 0) {  // both warp groups of the chain are done (chain_part)
+        if (lane == 0) {  // both warp groups are done (look_back ends with a barrier)
           mbar_arrive(T_free);
           mbar_arrive(S_full);
         }
