@@ -59,21 +59,27 @@ constexpr float kLog2Floor = -93.0139f;  // log2(1e-28): smallest factor in a wi
 
 // Shared memory, from a 1024-byte aligned base.
 //   k ring: 2 slots x 2 boxes of 128 rows x 128 bytes (64 dims), 128-byte swizzle
-//   v ring: 2 slots x (4 atoms of 128 rows x 64 bytes (32 columns), 64-byte
-//           swizzle, then the ones atom: column 0 = 1) = [V | 1]
-//   q tile: one slot, 2 boxes like k
+//   v ring: 2 slots x 2 atoms of 128 rows x 128 bytes (64 columns), 128-byte
+//           swizzle, and one ones atom (column 0 = 1) shared by both slots:
+//           [V | 1] is MN-major with atom stride LBO, so slot 0 (atoms at
+//           +64K, +80K, LBO 16 KB) and slot 1 (atoms at +0, +48K, LBO 48 KB)
+//           both reach the ones atom at +96K; the q tile fills the gap
+//   q tile: one slot, 2 boxes like k, at +16K in the v region
 //   [T | z]: bf16, 5 atoms of 128 rows (d) x 64 bytes, 64-byte swizzle
 //   output staging: per state/output warp 32 rows x 64 bytes (32 columns of
 //           o), 64-byte swizzle, written back by TMA tile stores
 constexpr int kKBox = 128 * 128;
-constexpr int kVAtom = 128 * 64;
+constexpr int kVAtom = 128 * 128;  // 64 columns of v, 128-byte swizzle
 constexpr int kKSlot = 2 * kKBox;
-constexpr int kVSlot = 5 * kVAtom;
+
 constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + 2 * kKSlot;
-constexpr int kOffQ = kOffV + 2 * kVSlot;
+constexpr int kOffVR = kOffK + 2 * kKSlot;  // v slot 1 atom 0 | q | v slot 1 atom 1 | v slot 0 | ones
+constexpr int kOffQ = kOffVR + kVAtom;
+constexpr int kOffOnes = kOffVR + 6 * kVAtom;
+__host__ __device__ constexpr int v_base(int sl) { return sl == 0 ? kOffVR + 4 * kVAtom : kOffVR; }
+__host__ __device__ constexpr int v_lbo(int sl) { return sl == 0 ? kVAtom : 3 * kVAtom; }
 constexpr int kSopAtom = kD * 64;
-constexpr int kOffSop = kOffQ + kKSlot;
+constexpr int kOffSop = kOffVR + 7 * kVAtom;
 constexpr int kStgBytes = 32 * 64;
 constexpr int kOffStg = kOffSop + 5 * kSopAtom;
 constexpr int kNumBars = 24;
@@ -82,7 +88,7 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kBytes = kOffMisc + 32;
 constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
 static_assert(kAlloc <= 227 * 1024, "shared memory");
-static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffSop % 1024 == 0, "align");
+static_assert(kOffVR % 1024 == 0 && kOffQ % 1024 == 0 && kOffSop % 1024 == 0, "align");
 
 // Tensor memory (512 columns): qh as bf16 pairs, A' (fp32; P as bf16 pairs
 // in its first 64 columns), T = [S | z] (fp32), O (fp32).
@@ -202,19 +208,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     item[1] = t % BH;  // batch * head
   }
   {
-    // ones atoms of both v slots and the [T | z] operand: zero, then
-    // column 0 of every ones row = 1
-    for (int i = tid; i < 2 * kVAtom / 16; i += kThreads) {
-      const int sl = i / (kVAtom / 16), j = i % (kVAtom / 16);
-      reinterpret_cast<uint4 *>(sm + kOffV + sl * kVSlot + 4 * kVAtom)[j] = make_uint4(0, 0, 0, 0);
-    }
+    // the ones atom (shared by both v slots) and the [T | z] operand: zero,
+    // then column 0 of every ones row = 1
+    for (int i = tid; i < kVAtom / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
     for (int i = tid; i < 5 * kSopAtom / 16; i += kThreads)
       reinterpret_cast<uint4 *>(sm + kOffSop)[i] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  if (tid < 2 * kC) {
-    const int sl = tid / kC, r = tid % kC;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + kOffV + sl * kVSlot + 4 * kVAtom + sw64_off(r, 0)) =
+  if (tid < kC) {
+    const int r = tid;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + kOffOnes + sw128_off(r, 0)) =
         __float2bfloat16_rn(1.f);
   }
   if (tid == 32 * kWarpTma) {
@@ -402,11 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         const uint32_t ph = static_cast<uint32_t>((c / slots) & 1);
         if (!mbar_wait(&emptyb[sl], ph ^ 1, abort_flag, p.timeouts)) break;
         const int row = ring_row(c);
-        mbar_arrive_expect_tx(&fullb[sl], lane == 1 ? 4 * kVAtom : kKSlot);
+        mbar_arrive_expect_tx(&fullb[sl], lane == 1 ? 2 * kVAtom : kKSlot);
         if (lane == 1) {
-          uint8_t *dst = sm + kOffV + sl * kVSlot;
-#pragma unroll
-          for (int a = 0; a < 4; ++a) tma_load_3d(dst + a * kVAtom, map, 32 * a, row, bh, &fullb[sl]);
+          tma_load_3d(sm + v_base(sl), map, 0, row, bh, &fullb[sl]);
+          tma_load_3d(sm + v_base(sl) + v_lbo(sl), map, 64, row, bh, &fullb[sl]);
         } else {
           uint8_t *dst = sm + (lane == 0 ? kOffK + sl * kKSlot : kOffQ);
           tma_load_3d(dst, map, 0, row, bh, &fullb[sl]);
@@ -418,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         if (cp < n) {
           const int rowp = ring_row(cp);
           if (lane == 1) {
-#pragma unroll
-            for (int a = 0; a < 4; ++a) tma_prefetch_3d(map, 32 * a, rowp, bh);
+            tma_prefetch_3d(map, 0, rowp, bh);
+            tma_prefetch_3d(map, 64, rowp, bh);
           } else {
             tma_prefetch_3d(map, 0, rowp, bh);
             tma_prefetch_3d(map, 64, rowp, bh);
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     // N in 32-wide atoms, K = tokens or d)
     auto dk = [&](int sl) { return smem_desc(base + kOffK + sl * kKSlot, 16, 1024, kSw128); };
     auto dkt = [&](int sl) { return smem_desc(base + kOffK + sl * kKSlot, kKBox, 1024, kSw128); };
-    auto dv = [&](int sl) { return smem_desc(base + kOffV + sl * kVSlot, kVAtom, 512, kSw64); };
+    auto dv = [&](int sl) { return smem_desc(base + v_base(sl), v_lbo(sl), 1024, kSw128); };
     const uint64_t dsop = smem_desc(base + kOffSop, kSopAtom, 512, kSw64);
     const uint32_t tQ = tmem + kColQ, tA = tmem + kColA, tT = tmem + kColT, tO = tmem + kColO;
     bool ok = true;
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         const uint64_t a = dkt(sl), b = dv(sl);
 #pragma unroll
         for (int kk = 0; kk < kC / 16; ++kk)
-          mma_bf16(tT, a + kk * 128, b + kk * 64, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tT, a + kk * 128, b + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar[kKEmpty + sl]);
         mma_commit(&bar[kVEmpty + sl]);
       }
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         if (leader) {
           const uint64_t a = dkt(sl), b = dv(sl);
 #pragma unroll
-          for (int kk = 0; kk < kC / 16; ++kk) mma_bf16(tT, a + kk * 128, b + kk * 64, ID_DS, 1u);
+          for (int kk = 0; kk < kC / 16; ++kk) mma_bf16(tT, a + kk * 128, b + kk * 128, ID_DS, 1u);
           mma_commit(&bar[kTReady]);
         }
       }
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       if (leader) {
         const uint64_t b = dv(sl);
 #pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk) mma_bf16_ta(tO, tA + 8 * kk, b + kk * 64, ID_O, 1u);
+        for (int kk = 0; kk < kC / 16; ++kk) mma_bf16_ta(tO, tA + 8 * kk, b + kk * 128, ID_O, 1u);
         mma_commit(&bar[kOFull]);
         mma_commit(&bar[kVEmpty + sl]);
       }
@@ -790,7 +793,7 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   Chunk128Params prm = {};
   if (!make_tmap_3d_bf16(&prm.tmQ, p.q, kD, p.N, BH, 64, kC, 128) ||
       !make_tmap_3d_bf16(&prm.tmK, p.k, kD, p.N, BH, 64, kC, 128) ||
-      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 32, kC, 64) ||
+      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 64, kC, 128) ||
       !make_tmap_3d_bf16(&prm.tmO, p.o, kDV, p.N, BH, 32, 32, 64))
     return cudaErrorNotSupported;
   prm.timeouts = wait_timeout_counter();
