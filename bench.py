@@ -317,6 +317,9 @@ def run_ours(args, w):
     from kernelized_sequence_mixing_gb300.workloads import make_qkv
 
     ws, rank, local = dist_env()
+    final_state = bool(getattr(args, "final_state", False))
+    if final_state and (w.steps or not w.causal):
+        raise SystemExit("--final-state applies to the causal forward workloads")
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -368,13 +371,29 @@ def run_ours(args, w):
             for _ in range(ncopy - 1)]
         rot = [0]
 
-        def step():
-            qc, kc, vc, oc = copies[rot[0] % ncopy]
-            rot[0] += 1
-            la.forward(qc, kc, vc, causal=w.causal, gamma=g, eps=w.eps, out=oc)
+        if final_state:
+            Sd = torch.empty((w.B, w.H, w.D, w.Dv), dtype=torch.float32, device=dev)
+            zd = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device=dev)
 
-        def e2e_step(qh, kh, vh, oh):
-            la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
+            def step():
+                qc, kc, vc, oc = copies[rot[0] % ncopy]
+                rot[0] += 1
+                la.forward_state(qc, kc, vc, gamma=g, eps=w.eps, out=oc, S=Sd, z=zd)
+
+            def e2e_step(qh, kh, vh, oh):
+                qd.copy_(qh, non_blocking=True)
+                kd.copy_(kh, non_blocking=True)
+                vd.copy_(vh, non_blocking=True)
+                la.forward_state(qd, kd, vd, gamma=g, eps=w.eps, out=od, S=Sd, z=zd)
+                oh.copy_(od, non_blocking=True)
+        else:
+            def step():
+                qc, kc, vc, oc = copies[rot[0] % ncopy]
+                rot[0] += 1
+                la.forward(qc, kc, vc, causal=w.causal, gamma=g, eps=w.eps, out=oc)
+
+            def e2e_step(qh, kh, vh, oh):
+                la.forward(qh, kh, vh, causal=w.causal, gamma=g, eps=w.eps, out=oh)
         tokens_rank = w.B * w.N
     stream = torch.cuda.current_stream(dev)
     if w.steps:
@@ -440,11 +459,13 @@ def run_ours(args, w):
 
     hbm_peak, tc_peak, peak_src = measured_peaks()
     byts, flops = decode_work(w) if w.steps else algorithmic_work(w)
+    if final_state:  # the state written once at the end, fp32
+        byts += w.B * w.H * (w.D * w.Dv + w.D) * 4
     launch_ms = statistics.mean(per_launch)  # one kernel launch per step
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
     tr = NCU_TRAFFIC.get(w.name)
-    traffic = tr["bytes"] if tr and tr.get("source") == src_hash else None
+    traffic = tr["bytes"] if tr and tr.get("source") == src_hash and not final_state else None
 
     # CPU baseline: the fp64 oracle on the host cores, one pass over a bounded
     # sample (all 32 heads of the default workload, ~20 s of CPU work)
@@ -471,7 +492,9 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype.itemsize == 2 else "f32",
         "data": "synthetic",
-        "config": dict(workload_config(w),
+        "config": dict(workload_config(w), **({"final_state": "S [B][H][D][Dv] and z [B][H][D] "
+                                               "fp32 written after the last token"}
+                                              if final_state else {}),
                        l2=(f"working set larger than L2 ({byts / 1e6:.0f} MB "
                            "read and written per step), no flush")
                        if w.steps or ncopy == 1 else
@@ -505,6 +528,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--final-state", action="store_true",
+                    help="causal workloads: time la_forward_state (the forward "
+                         "plus the state after the last token) instead")
     ap.add_argument("--quick", action="store_true",
                     help="skip the clock-sampling window and the end-to-end "
                          "leg (few launches, for profiler runs)")

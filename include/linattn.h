@@ -106,6 +106,25 @@ LA_API la_status_t la_prefill_state(const void *k, const void *v, float *S, floa
                              void *stream);
 
 /*
+ * Causal forward that also returns the state after the last token: o as
+ * la_forward(..., causal = 1, ...), and S, z as la_prefill_state over the
+ * same k, v (the state the decode loop continues from).  On the tensor-core
+ * path for D = Dv = 128 the state comes out of the forward's own pass (the
+ * CTA of the last part writes it); otherwise the library runs the forward,
+ * then the prefill reduction, on `stream`.
+ * q, k: [B][H][N][D]; v, o: [B][H][N][Dv] (dtype); S: [B][H][D][Dv] fp32 and
+ * z: [B][H][D] fp32 are overwritten (zero for N = 0).  No buffer may overlap
+ * another.  Errors as la_forward and la_prefill_state.
+ * Defined on the pages "Linear Attention Mechanisms" (dileepadev.github.io),
+ * "Recurrent Reformulation" (the state S_i, z_i at i = N - 1) and "Gating
+ * and Selective State Updates" (the decay on both).
+ */
+LA_API la_status_t la_forward_state(const void *q, const void *k, const void *v, void *o,
+                                    float *S, float *z, int B, int H, int N, int D, int Dv,
+                                    const float *gamma, float eps, la_dtype_t dtype,
+                                    void *stream);
+
+/*
  * One recurrent decode step, in place: first
  *   S <- gamma S + phi(k) v^T,  z <- gamma z + phi(k),
  * then  o = phi(q)^T S / (phi(q) . z + eps)  with the updated state.

@@ -62,6 +62,9 @@ def load_library() -> ctypes.CDLL:
             lib.la_forward.restype = I
             lib.la_prefill_state.argtypes = [P, P, P, P, I, I, I, I, I, FP, I, P]
             lib.la_prefill_state.restype = I
+            lib.la_forward_state.argtypes = [P, P, P, P, P, P, I, I, I, I, I, FP, F,
+                                             I, P]
+            lib.la_forward_state.restype = I
             lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, FP, F,
                                            I, P]
             lib.la_decode_step.restype = I
@@ -204,6 +207,35 @@ def prefill_state(k, v, gamma=None, S=None, z=None):
             _ptr(k), _ptr(v), _ptr(S), _ptr(z), B, H, N, D, Dv,
             _gamma_arg(gamma, H), _dtype_code(k), _stream(dev)))
     return S, z
+
+
+def forward_state(q, k, v, gamma=None, eps=1e-6, out=None, S=None, z=None):
+    """Causal forward that also returns the state after the last token:
+    (o [B, H, N, Dv], S [B, H, D, Dv] fp32, z [B, H, D] fp32), the state the
+    decode loop continues from.  q, k: [B, H, N, D]; v: [B, H, N, Dv] CUDA
+    tensors of one dtype; out, S, z: optional destinations."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    with torch.cuda.device(dev):
+        o = out if out is not None else torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
+        if S is None:
+            S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
+        if z is None:
+            z = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+        for n, t in (("out", o), ("S", S), ("z", z)):
+            _contig(n, t)
+        _check("la_forward_state", lib.la_forward_state(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H, N, D, Dv,
+            _gamma_arg(gamma, H), float(eps), _dtype_code(q), _stream(dev)))
+    return o, S, z
 
 
 def decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None):

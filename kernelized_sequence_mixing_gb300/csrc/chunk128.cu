@@ -137,6 +137,9 @@ struct Chunk128Params {
   int *ws_flag;    // P > 1: [B*H][P], 1 once incl_p is published
   int *ws_ticket;  // P > 1: part-major work counter
   unsigned int *timeouts;
+  // optional: the state after the last token, S [B*H][D][Dv] and z [B*H][D]
+  // fp32, written by the CTA of the last part (nullptr: not written)
+  float *S_out, *z_out;
   int BH, H, N, P;
   float eps;
   Gammas lg;  // log2(gamma) per head
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   const int cbA = hasA ? part_begin(part - 1, P, nch_all) : 0;
   const int nA = hasA ? cb - cbA : 0;
   const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
+  const bool final_state = p.S_out != nullptr && part == P - 1;
   int WC = 64;  // chunks per decay window
   if (DECAY && lg < 0.f) {
     const float c = kLog2Floor / lg / static_cast<float>(kC);
@@ -499,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     for (int i = 0; ok && i < nch; ++i) {
       const int c = nA + i, sl = c & 1;
       const uint32_t ph = static_cast<uint32_t>((c >> 1) & 1);
-      if (i + 1 < nch) {
-        // T += kh^T [V | 1]: not needed after the last chunk
+      if (i + 1 < nch || final_state) {
+        // T += kh^T [V | 1]: after the last chunk only for the final state
         if (!warp_wait(&bar[kTFree], i & 1, abort_flag, p.timeouts) ||
             !warp_wait(&bar[kVFull + sl], ph, abort_flag, p.timeouts))
           break;
@@ -699,6 +703,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         }
       }
     }
+    if (final_state && !*abort_flag) {
+      // the state after the last token: T after the last chunk's update is
+      // scaled to the end of its decay window, E; the state wants the last
+      // token N - 1 as its reference, a factor gamma^((N - 1) - E)
+      warp_wait(&bar[kTReady], static_cast<uint32_t>((nch - 1 + (hasA ? 1 : 0)) & 1), abort_flag,
+                p.timeouts);
+      tc_fence_after();
+      const int jl = (nch - 1) % WC;
+      const long long e_abs = static_cast<long long>(cb + nch - 1 - jl) * kC + W - 1;
+      const float fs = DECAY ? exp2f(static_cast<float>(static_cast<long long>(N - 1) - e_abs) * lg) : 1.f;
+      float *srow = p.S_out + (static_cast<size_t>(bh) * kD + d) * kDV;
+#pragma unroll 1
+      for (int cc = 0; cc < kDV / 32; ++cc) {
+        float x[32];
+        tmem_ld32(tT + 32 * cc, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4 *>(srow + 32 * cc)[q] =
+              make_float4(fs * x[4 * q], fs * x[4 * q + 1], fs * x[4 * q + 2], fs * x[4 * q + 3]);
+      }
+      const float zd = tmem_ld1(tT + kDV);
+      tmem_wait_ld();
+      p.z_out[static_cast<size_t>(bh) * kD + d] = fs * zd;
+    }
     if (lane == 0) bulk_wait_group0();  // every store complete before the CTA exits
   } else {
     // ---------------- P = A' masked to s <= t, bf16 pairs in place ----------------
@@ -787,7 +816,8 @@ size_t chunk128_workspace_bytes(int BH, int P) {
          sizeof(float) * static_cast<size_t>(BH) * P * (static_cast<size_t>(kD) * kDV + kD);
 }
 
-cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, int P, cudaStream_t s) {
+cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, int P, cudaStream_t s,
+                                   float *S_out, float *z_out) {
   if (!chunk128_supported(p, g) || P < 1) return cudaErrorNotSupported;
   const int BH = p.B * p.H;
   Chunk128Params prm = {};
@@ -803,6 +833,8 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   prm.N = p.N;
   prm.P = P;
   prm.eps = p.eps;
+  prm.S_out = S_out;
+  prm.z_out = z_out;
   prm.lg = log2_gammas(g, p.H, p.decay);
   if (P > 1) {
     if (!ws) return cudaErrorInvalidValue;

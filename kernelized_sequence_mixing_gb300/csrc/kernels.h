@@ -47,8 +47,11 @@ cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int
 bool chunk128_supported(const Problem &p, const Gammas &g);
 int chunk128_parts(int BH, int N);
 size_t chunk128_workspace_bytes(int BH, int P);
+// S_out, z_out (optional, both or neither): the state after the last token,
+// [B*H][D][Dv] and [B*H][D] fp32.
 cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, int P,
-                                   cudaStream_t s);
+                                   cudaStream_t s, float *S_out = nullptr,
+                                   float *z_out = nullptr);
 // Final state S [BH][D][Dv], z [BH][D] of the causal recurrence over N tokens.
 cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
                                  int N, int D, int Dv, bool decay, const Gammas &g, void *ws,

@@ -225,6 +225,53 @@ la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
   return from_cuda(ef);
 }
 
+la_status_t la_forward_state(const void *q, const void *k, const void *v, void *o,
+                             float *S, float *z, int B, int H, int N, int D, int Dv,
+                             const float *gamma, float eps, la_dtype_t dtype,
+                             void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  const int BH = B * H;
+  if (BH == 0) return LA_OK;
+  if (!S || !z || !aligned16(S) || !aligned16(z)) return LA_ERR_INVALID_ARG;
+  const size_t nS = sizeof(float) * (size_t)BH * D * Dv, nz = sizeof(float) * (size_t)BH * D;
+  if (overlaps(S, nS, z, nz)) return LA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (cudaMemsetAsync(S, 0, nS, s) != cudaSuccess || cudaMemsetAsync(z, 0, nz, s) != cudaSuccess)
+      return LA_ERR_CUDA;
+    return LA_OK;
+  }
+  if (!q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * Dv * es;
+  const void *ins[4] = {q, k, v, o};
+  const size_t insz[4] = {nqk, nqk, nv, nv};
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(S, nS, ins[i], insz[i]) || overlaps(z, nz, ins[i], insz[i])) return LA_ERR_INVALID_ARG;
+  if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv))
+    return LA_ERR_INVALID_ARG;
+  Problem p{q, k, v, o, B, H, N, D, Dv, decay, eps, dtype == LA_F32 ? kF32 : kBF16};
+  if (chunk128_supported(p, g)) {
+    // one pass: the CTA of the last part writes the state
+    const int P = chunk128_parts(BH, N);
+    const size_t wsb = chunk128_workspace_bytes(BH, P);
+    void *ws = nullptr;
+    if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
+    cudaError_t e = launch_causal_chunk128(p, g, ws, P, s, S, z);
+    cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(ef);
+  }
+  if ((st = la_forward(q, k, v, o, B, H, N, D, Dv, 1, gamma, eps, dtype, stream)) != LA_OK) return st;
+  return la_prefill_state(k, v, S, z, B, H, N, D, Dv, gamma, dtype, stream);
+}
+
 la_status_t la_decode_step(const void *q, const void *k, const void *v,
                            float *S, float *z, void *o, int B, int H, int D,
                            int Dv, const float *gamma, float eps,

@@ -34,7 +34,7 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     syms = declared_symbols()
-    for s in ("la_forward", "la_prefill_state", "la_decode_step",
+    for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -104,6 +104,28 @@ def test_prefill_rejects_bad_arguments(lib):
     assert P(A, A + STEP, A + 2 * STEP, A + 3 * STEP, 1, 2, 8, 64, 64, bad, BF16, None) == INVALID
     assert P(A, A + STEP, A + 2 * STEP, A + 3 * STEP, 1, 2, 8, 48, 64, None, BF16, None) == UNSUPPORTED
     assert P(None, None, None, None, 0, 2, 8, 64, 64, None, BF16, None) == OK
+
+
+def test_forward_state_rejects_bad_arguments(lib):
+    Fs = lib.la_forward_state
+    q, k, v, o, S, z = (A + i * STEP for i in range(6))
+
+    def call(qq=q, kk=k, vv=v, oo=o, SS=S, zz=z, B=1, H=2, N=8, D=128, Dv=128, eps=1e-6,
+             g=None, dt=BF16):
+        return Fs(qq, kk, vv, oo, SS, zz, B, H, N, D, Dv, g, eps, dt, None)
+
+    assert call(SS=None) == INVALID
+    assert call(zz=None) == INVALID
+    assert call(SS=S + 8) == INVALID            # misaligned state
+    assert call(zz=S + 64) == INVALID           # z inside S
+    assert call(SS=q) == INVALID                # S aliases q
+    assert call(zz=o + 16) == INVALID           # z inside o
+    assert call(oo=v) == INVALID                # o aliases v
+    assert call(qq=None) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(g=(ctypes.c_float * 2)(0.5, 1.5)) == INVALID
+    assert call(D=96) == UNSUPPORTED
+    assert call(B=0, qq=None, kk=None, vv=None, oo=None, SS=None, zz=None) == OK
 
 
 def test_decode_rejects_bad_arguments(lib):

@@ -358,6 +358,44 @@ def test_decode_bf16_h32_full(la, ora):
     assert state_error(to_np(z[bs, hs])[..., None], zr[..., None]) < 1e-4
 
 
+# The causal forward that also returns the final state: the fused path of
+# the 128-token kernel (the last part's CTA writes S, z; one part, a few
+# parts, many parts, one token) and the composed path (forward, then the
+# prefill reduction) of the 64-token and CUDA-core kernels.
+FORWARD_STATE = [
+    # (B, H, N, D, Dv, dtype, gammas)
+    (1, 2, 1000, 128, 128, torch.bfloat16, [0.61, 0.999]),
+    (1, 3, 20000, 128, 128, torch.bfloat16, [0.9, 0.99, 1.0]),
+    (2, 76, 700, 128, 128, torch.bfloat16, [0.75, 0.97, 1.0, 0.999]),
+    (1, 1, 1, 128, 128, torch.bfloat16, None),
+    (1, 2, 333, 64, 64, torch.bfloat16, [0.9, 1.0]),
+    (1, 2, 300, 64, 128, torch.float32, [0.5, 1.0]),
+]
+
+
+@pytest.mark.parametrize("case", FORWARD_STATE,
+                         ids=lambda c: "x".join(map(str, c[:5])) + ("-f32" if c[5] == torch.float32 else ""))
+def test_forward_state(la, ora, case):
+    B, H, N, D, Dv, dtype, gl = case
+    q, k, v = gen(B, H, N, D, Dv, dtype, seed=5 * H + N)
+    g = None if gl is None else torch.tensor([gl[h % len(gl)] for h in range(H)],
+                                             dtype=torch.float32)
+    o, S, z = la.forward_state(q.cuda(), k.cuda(), v.cuda(), gamma=g, eps=1e-6)
+    torch.cuda.synchronize()
+    gn = None if g is None else g.numpy()
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=gn, eps=1e-6)
+    S_ref, z_ref = ora.prefill(to_np(k), to_np(v), gamma=gn)
+    tol = TOL[dtype]
+    assert max_row_error(to_np(o), ref) < tol
+    eS = state_error(to_np(S), S_ref)
+    ez = state_error(to_np(z)[..., None], z_ref[..., None])
+    # the fused state sums bf16 operands like the output: the bf16 bound
+    assert eS < tol and ez < tol, (eS, ez)
+    # and it equals the forward's own output path: la.forward gives the same o
+    o2 = la.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, gamma=g, eps=1e-6)
+    assert torch.equal(o, o2)
+
+
 def test_tensor_core_and_cuda_core_paths_agree(la, ora):
     """The same bf16 problem through both causal kernels (a strong decay on a
     spare head forces the CUDA-core kernel) against the oracle."""
