@@ -22,6 +22,11 @@ What each function computes, with the passage it follows:
                      Attention Mechanisms" (sadullah.online).
 * ``prefill``     -- the (S, z) left by ``causal`` after the last token.
 * ``decode_step`` -- one iteration of the causal loop on a given (S, z).
+* ``gated``       -- the causal loop with a data-dependent gate per step and
+                     key feature in place of gamma: S_i = G_i (.) S_{i-1} +
+                     phi(k_i) v_i^T with G_i = a_i 1^T, z gated alike.  Same
+                     page, "Gating and Selective State Updates" (Gated Linear
+                     Attention); "Evolution: add decay/gating".
 
 Pins (tests/test_oracle.py) check every function against things other than
 itself: a quadratic masked brute force, an exact rational evaluation, a
@@ -79,6 +84,9 @@ def _load():
             lib.oracle_decode_step.argtypes = [P, P, P, P, f64, i64, i32, i32,
                                                P, P, P, i32]
             lib.oracle_decode_step.restype = i32
+            lib.oracle_gated.argtypes = [P, P, P, P, f64, i64, i64, i32, i32,
+                                         P, P, P, i32]
+            lib.oracle_gated.restype = i32
             _lib = lib
     return _lib
 
@@ -218,3 +226,27 @@ def decode_step(q, k, v, S, z, gamma=None, eps=1e-6, nthreads=None):
     if rc:
         raise RuntimeError("oracle_decode_step rejected its arguments")
     return o, S, z
+
+
+def gated(q, k, v, a, eps=1e-6, return_state=False, nthreads=None):
+    """Gated causal linear attention in fp64: q, k, a [..., N, D];
+    v [..., N, Dv]; a holds the gate a_i[d] of each step and key feature
+    (fp32 values, widened).  Returns o [..., N, Dv], plus (S, z) after the
+    last token if ``return_state``."""
+    lib = _load()
+    q = _f32(q, np.ndim(q)); k = _f32(k, q.ndim); v = _f32(v, q.ndim)
+    a = _f32(a, q.ndim)
+    N, D = q.shape[-2], q.shape[-1]
+    Dv = v.shape[-1]
+    if k.shape != q.shape or a.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+        raise ValueError("shape mismatch")
+    U, lead = _units(q)
+    o = np.empty(q.shape[:-1] + (Dv,), dtype=np.float64)
+    S = np.zeros(lead + (D, Dv), dtype=np.float64)
+    z = np.zeros(lead + (D,), dtype=np.float64)
+    rc = lib.oracle_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), float(eps), U, N,
+                          D, Dv, _ptr(o), _ptr(S), _ptr(z),
+                          nthreads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_gated rejected its arguments")
+    return (o, S, z) if return_state else o

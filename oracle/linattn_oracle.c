@@ -39,9 +39,20 @@
  *   decode step: one iteration of the causal loop on a caller-held (S, z):
  *     update first, then read out.
  *
+ *   gated: the causal loop with a data-dependent gate in place of gamma,
+ *     S_i = G_i (.) S_{i-1} + phi(k_i) v_i^T, G_i = a_i 1^T (a gate a_i[d] in
+ *     [0, 1] per step and key feature, the same for every value column), and
+ *     z_i[d] = a_i[d] z_{i-1}[d] + phi(k_i)[d]; the same read-out.
+ *     -- "Linear Attention Mechanisms" (dileepadev.github.io), "Gating and
+ *        Selective State Updates", Gated Linear Attention (G_t applied
+ *        elementwise to the state; G_t = 1 is plain linear attention,
+ *        G_t = 0 overwrites the state); "Attention-Free / Sub-Quadratic
+ *        Architectures", "Evolution: add decay/gating".
+ *
  * Inputs are fp32 arrays (bf16 inputs are widened exactly by the caller);
  * all arithmetic and all outputs are fp64.  Layouts: q, k [U][N][D],
- * v [U][N][Dv], o [U][N][Dv], S [U][D][Dv], z [U][D], gamma [U], where U is
+ * v [U][N][Dv], o [U][N][Dv], S [U][D][Dv], z [U][D], gamma [U], gates
+ * a [U][N][D], where U is
  * the number of independent (batch, head) units.  Units are spread over
  * POSIX threads; each unit is computed by one thread in the order above, so
  * results do not depend on the thread count.
@@ -71,6 +82,38 @@ static void causal_unit(const float *q, const float *k, const float *v,
     }
     if (o) {
       /* o_i = phi(q_i)^T S_i / (phi(q_i) . z_i + eps) */
+      const float *qi = q + i * D;
+      for (int d = 0; d < D; ++d) fq[d] = oracle_phi((double)qi[d]);
+      double den = 0.0;
+      for (int d = 0; d < D; ++d) den += fq[d] * z[d];
+      den += eps;
+      double *oi = o + i * Dv;
+      for (int e = 0; e < Dv; ++e) {
+        double num = 0.0;
+        for (int d = 0; d < D; ++d) num += fq[d] * S[(int64_t)d * Dv + e];
+        oi[e] = num / den;
+      }
+    }
+  }
+}
+
+/* One unit of the gated recurrence: a [N][D] gates, S, z running state. */
+static void gated_unit(const float *q, const float *k, const float *v,
+                       const float *a, double eps, int64_t N, int D, int Dv,
+                       double *S, double *z, double *o, double *fq,
+                       double *fk) {
+  for (int64_t i = 0; i < N; ++i) {
+    const float *ki = k + i * D, *vi = v + i * Dv, *ai = a + i * D;
+    for (int d = 0; d < D; ++d) fk[d] = oracle_phi((double)ki[d]);
+    /* S_i[d][:] = a_i[d] S_{i-1}[d][:] + phi(k_i)[d] v_i^T ;
+       z_i[d] = a_i[d] z_{i-1}[d] + phi(k_i)[d] */
+    for (int d = 0; d < D; ++d) {
+      const double g = (double)ai[d];
+      double *Sd = S + (int64_t)d * Dv;
+      for (int e = 0; e < Dv; ++e) Sd[e] = g * Sd[e] + fk[d] * (double)vi[e];
+      z[d] = g * z[d] + fk[d];
+    }
+    if (o) {
       const float *qi = q + i * D;
       for (int d = 0; d < D; ++d) fq[d] = oracle_phi((double)qi[d]);
       double den = 0.0;
@@ -121,12 +164,13 @@ static void noncausal_unit(const float *q, const float *k, const float *v,
 
 /* ------------------------------------------------------------------------ */
 /* Thread pool over units.                                                  */
-enum { MODE_CAUSAL = 0, MODE_NONCAUSAL = 1, MODE_DECODE = 2 };
+enum { MODE_CAUSAL = 0, MODE_NONCAUSAL = 1, MODE_DECODE = 2, MODE_GATED = 3 };
 
 typedef struct {
   int mode, tid, nthreads, D, Dv;
   int64_t U, N;
   const float *q, *k, *v;
+  const float *a; /* gated: [U][N][D] */
   const double *gamma;
   double eps;
   double *o, *S, *z; /* S, z: per-unit state out (or in/out for decode) */
@@ -155,6 +199,12 @@ static void *worker(void *arg) {
                   J->v + u * N * Dv, g,
                   J->eps, N, D, Dv, S, z, J->o ? J->o + u * N * Dv : NULL, fq,
                   fk);
+    } else if (J->mode == MODE_GATED) {
+      memset(S, 0, sizeof(double) * (size_t)D * Dv);
+      memset(z, 0, sizeof(double) * (size_t)D);
+      gated_unit(J->q ? J->q + u * N * D : NULL, J->k + u * N * D, J->v + u * N * Dv,
+                 J->a + u * N * D, J->eps, N, D, Dv, S, z,
+                 J->o ? J->o + u * N * Dv : NULL, fq, fk);
     } else if (J->mode == MODE_NONCAUSAL) {
       noncausal_unit(J->q ? J->q + u * N * D : NULL, J->k + u * N * D,
                      J->v + u * N * Dv, J->eps, N, D, Dv, S, z,
@@ -246,5 +296,20 @@ int oracle_decode_step(const float *q, const float *k, const float *v,
   J.U = U; J.N = 1; J.D = D; J.Dv = Dv;
   J.q = q; J.k = k; J.v = v; J.gamma = gamma; J.eps = eps;
   J.o = o; J.S = S; J.z = z;
+  return run_jobs(J, nthreads);
+}
+
+/* Gated form.  a [U][N][D] gates; o may be NULL (state only); S_state,
+ * z_state may be NULL, else they receive the state after token N-1. */
+int oracle_gated(const float *q, const float *k, const float *v, const float *a,
+                 double eps, int64_t U, int64_t N, int D, int Dv, double *o,
+                 double *S_state, double *z_state, int nthreads) {
+  if (U < 0 || N < 0 || D <= 0 || Dv <= 0 || !k || !v || !a || (o && !q)) return -1;
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.mode = MODE_GATED;
+  J.U = U; J.N = N; J.D = D; J.Dv = Dv;
+  J.q = q; J.k = k; J.v = v; J.a = a; J.eps = eps;
+  J.o = o; J.S = S_state; J.z = z_state;
   return run_jobs(J, nthreads);
 }

@@ -324,3 +324,81 @@ def test_empty_sequence(oracle_mod):
     assert oracle_mod.causal(q, q, v).shape == (0, 3)
     S, z = oracle_mod.prefill(q, v)
     assert not S.any() and not z.any()
+
+
+# --------------------------------------------------------------------------
+# gated form (per-step, per-key-feature gate G_i = a_i 1^T)
+
+def brute_gated(q, k, v, a, eps):
+    """Quadratic form of the gated recurrence, written from its definition:
+    o_t = sum_(s <= t) w_ts v_s / (sum_(s <= t) w_ts + eps) with
+    w_ts = sum_d phi(q_t)[d] phi(k_s)[d] prod_(u = s+1..t) a_u[d] (the
+    product of the gates applied to the state after step s).  "Linear
+    Attention Mechanisms" (dileepadev.github.io), "Gating and Selective State
+    Updates", S_t = G_t (.) S_(t-1) + phi(k_t) v_t^T, unrolled."""
+    q, k, v, a = (np.asarray(x, dtype=np.float64) for x in (q, k, v, a))
+    N, D = q.shape
+    fq, fk = phi_np(q), phi_np(k)
+    o = np.zeros((N, v.shape[1]))
+    for t in range(N):
+        w = np.zeros(t + 1)
+        for s in range(t + 1):
+            prod = np.ones(D)
+            for u in range(s + 1, t + 1):
+                prod = prod * a[u]
+            w[s] = float(np.sum(fq[t] * fk[s] * prod))
+        o[t] = (w @ v[: t + 1]) / (w.sum() + eps)
+    return o
+
+
+def gate_inputs(seed, N, D, lo=0.0, hi=1.0):
+    r = np.random.default_rng(seed)
+    return r.uniform(lo, hi, size=(N, D)).astype(np.float32)
+
+
+@pytest.mark.parametrize("N,D,Dv", [(1, 3, 2), (9, 4, 5), (24, 6, 3)])
+def test_gated_matches_quadratic_brute_force(oracle_mod, N, D, Dv):
+    q, k, v = rng_inputs(300 + N, N, D, Dv)
+    for lo in (0.0, 0.5, 0.9):
+        a = gate_inputs(400 + N, N, D, lo, 1.0)
+        for eps in (0.0, 1e-6):
+            o = oracle_mod.gated(q, k, v, a, eps=eps)
+            assert rel_err(o, brute_gated(q, k, v, a, eps)) < 1e-12
+
+
+def test_gated_constant_gate_is_the_decayed_form(oracle_mod):
+    """a_i[d] = gamma for every step and feature is the RetNet decay; a = 1
+    is plain linear attention (the pages' G_t = 1 case)."""
+    q, k, v = rng_inputs(21, 40, 6, 5)
+    for g in (1.0, 0.9, 0.5):
+        a = np.full((40, 6), g, np.float32)
+        assert rel_err(oracle_mod.gated(q, k, v, a), brute_causal(q, k, v, g, 1e-6)) < 1e-12
+
+
+def test_gated_zero_gate_overwrites_the_state(oracle_mod):
+    """G_t = 0 overwrites the state (the pages' forget case): the output at
+    t depends on token t alone, o_t = v_t A / (A + eps), A = phi(q_t).phi(k_t),
+    and the state after t is phi(k_t) v_t^T."""
+    q, k, v = rng_inputs(22, 12, 5, 4)
+    a = gate_inputs(23, 12, 5, 0.2, 1.0)
+    a[7] = 0.0
+    o, S, z = oracle_mod.gated(q[:8], k[:8], v[:8], a[:8], eps=1e-6, return_state=True)
+    A = float(phi_np(q[7]) @ phi_np(k[7]))
+    assert rel_err(o[7], v[7].astype(np.float64) * A / (A + 1e-6)) < 1e-13
+    assert rel_err(S, np.outer(phi_np(k[7]), v[7].astype(np.float64))) < 1e-15
+    assert rel_err(z, phi_np(k[7])) < 1e-15
+
+
+def test_gated_feature_gates_act_per_row_of_the_state(oracle_mod):
+    """A gate that is 0 on one key feature and 1 elsewhere clears exactly
+    that row of S and entry of z, and leaves the rest as in the ungated sum."""
+    q, k, v = rng_inputs(24, 10, 4, 3)
+    a = np.ones((10, 4), np.float32)
+    a[9, 2] = 0.0
+    _, S, z = oracle_mod.gated(q, k, v, a, return_state=True)
+    _, S1, z1 = oracle_mod.causal(q, k, v, return_state=True)
+    fk9 = phi_np(k[9])
+    assert rel_err(S[2], fk9[2] * v[9].astype(np.float64)) < 1e-15
+    assert abs(z[2] - fk9[2]) <= 1e-15 * abs(fk9[2])
+    for d in (0, 1, 3):
+        assert rel_err(S[d], S1[d]) < 1e-14 and abs(z[d] - z1[d]) <= 1e-14 * abs(z1[d])
