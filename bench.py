@@ -37,17 +37,23 @@ METRIC = ("causal linear-attn fwd tokens/s and % roofline "
 METRICS = {
     "noncausal": "non-causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
+    "gated": "gated linear-attn fwd tokens/s and % fp32 ALU roofline, 1×GB300",
 }
 
 
 def workload_metric(w):
     if w.steps:
         return METRICS["decode"]
+    if w.gated:
+        return METRICS["gated"]
     return METRIC if w.causal else METRICS["noncausal"]
 DEFAULT_WORKLOAD = "causal_decay_bf16_n16384"
 FALLBACK_HBM_GBS = 6800.0  # profiling recipe fallback, used only if absent
 L2_BYTES = 129 * 1024 * 1024   # GB300 L2
 FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 CUDA-core peak of a GB300, from its unit counts and clock: 152 SMs x
+# 128 fp32 lanes x 2 flops (one FMA) x 2070 MHz maximum SM clock
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, keyed by workload, with the hash of the kernel source the
@@ -115,6 +121,11 @@ def algorithmic_work(w):
     units = w.B * w.H * w.N
     byts = units * (2 * w.D + 2 * w.Dv) * es
     flops = units * (4 * w.D * w.Dv + 3 * w.D + w.Dv)
+    if w.gated:
+        # plus the fp32 gates read once; the gate multiplies one more flop
+        # per state and normaliser entry
+        byts += units * w.D * 4
+        flops += units * (w.D * w.Dv + w.D)
     return byts, flops
 
 
@@ -130,12 +141,14 @@ def measured_peaks():
 
 # sources the causal tensor-core kernel is compiled from
 KERNEL_SOURCES = ("chunk128.cu", "chunk_tc.cu", "tc_common.cuh", "common.cuh")
+# sources of the gated CUDA-core kernel
+GATED_SOURCES = ("gla_simt.cu", "common.cuh")
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kernelized_sequence_mixing_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -208,10 +221,12 @@ class ClockSampler:
 def oracle_sample(w, heads_per_pass):
     """A bounded sample of the workload for the fp64 oracle: the first
     `heads_per_pass` (b, h) units, every token."""
-    from kernelized_sequence_mixing_gb300.workloads import workload_inputs
+    from kernelized_sequence_mixing_gb300.workloads import workload_gates, workload_inputs
     import numpy as np
     q, k, v = workload_inputs(w)
     f = lambda t: t.float().reshape(-1, w.N, t.shape[-1])[:heads_per_pass].numpy()  # noqa: E731
+    if w.gated:  # the gates in place of per-head decays
+        return f(q), f(k), f(v), f(workload_gates(w))
     g = w.gamma()
     gu = None
     if g is not None:
@@ -226,7 +241,9 @@ def time_oracle(w, heads_per_pass, passes):
     times = []
     for _ in range(passes):
         t0 = time.perf_counter()
-        if w.causal:
+        if w.gated:
+            oracle.gated(qs, ks, vs, gu, eps=w.eps, nthreads=threads)
+        elif w.causal:
             oracle.causal(qs, ks, vs, gamma=gu, eps=w.eps, nthreads=threads)
         else:
             oracle.noncausal(qs, ks, vs, eps=w.eps, nthreads=threads)
@@ -300,6 +317,9 @@ def workload_config(w):
            "seq_len": w.N, "parallelism": "replicas (independent batches)"}
     if w.decayed:
         cfg["gamma"] = "per head 1 - 2^(-5 - h/4)"
+    if w.gated:
+        cfg["gates"] = (f"fp32 a [B][H][N][D] uniform in [{w.gate_lo}, 1), one per key "
+                        "feature and token")
     if w.steps:
         cfg.update(seq_len=1, prefill_len=w.N, state="fp32 S [D][Dv] and z [D] "
                    "per (sequence, head), from the prefill",
@@ -318,7 +338,7 @@ def run_ours(args, w):
 
     ws, rank, local = dist_env()
     final_state = bool(getattr(args, "final_state", False))
-    if final_state and (w.steps or not w.causal):
+    if final_state and (w.steps or not w.causal or w.gated):
         raise SystemExit("--final-state applies to the causal forward workloads")
     if ws > 1:
         import torch.distributed as dist
@@ -355,6 +375,35 @@ def run_ours(args, w):
             step()
             oh.copy_(od, non_blocking=True)
         tokens_rank = w.B
+    elif w.gated:
+        # gated forward: the state pass and the scan over sequence parts,
+        # then the output pass (one launch when the sequence is one part)
+        from kernelized_sequence_mixing_gb300.workloads import make_gates
+        q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
+        a = make_gates(w.B, w.H, w.N, w.D, seed + 1, w.gate_lo)
+        qd, kd, vd, ad = q.to(dev), k.to(dev), v.to(dev), a.to(dev)
+        od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
+        ncopy = 1
+        step_bytes = sum(t.numel() * t.element_size() for t in (qd, kd, vd, ad, od))
+        assert step_bytes > L2_BYTES, "gated workloads are sized above L2"
+        # number of sequence parts: the library's rule (2 CTAs per SM over
+        # B*H*(Dv/32) CTAs per part, at most one part per 64-token chunk)
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        ctas = w.B * w.H * (w.Dv // 32)
+        parts = max(1, min(-(-w.N // 64), -(-2 * nsm // ctas)))
+        launches_per_step = 3 if parts > 1 else 1
+
+        def step():
+            la.forward_gated(qd, kd, vd, ad, eps=w.eps, out=od)
+
+        def e2e_step(qh, kh, vh, oh, ah=None):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            ad.copy_(ah, non_blocking=True)
+            step()
+            oh.copy_(od, non_blocking=True)
+        tokens_rank = w.B * w.N
     else:
         q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -441,17 +490,18 @@ def run_ours(args, w):
     if not args.quick:
         qh, kh, vh = (t.pin_memory() for t in (q, k, v))
         oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-        e2e_step(qh, kh, vh, oh)
+        extra = {"ah": a.pin_memory()} if w.gated else {}
+        e2e_step(qh, kh, vh, oh, **extra)
         torch.cuda.synchronize(dev)
         e2e_steps = max(1, min(args.steps, 10))
         barrier(ws)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            e2e_step(qh, kh, vh, oh)
+            e2e_step(qh, kh, vh, oh, **extra)
         torch.cuda.synchronize(dev)
         e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, ws)
     es = q.element_size()
-    h2d = (q.numel() + k.numel() + v.numel()) * es
+    h2d = (q.numel() + k.numel() + v.numel()) * es + (a.numel() * 4 if w.gated else 0)
     d2h = od.numel() * es
 
     if rank != 0:
@@ -461,9 +511,9 @@ def run_ours(args, w):
     byts, flops = decode_work(w) if w.steps else algorithmic_work(w)
     if final_state:  # the state written once at the end, fp32
         byts += w.B * w.H * (w.D * w.Dv + w.D) * 4
-    launch_ms = statistics.mean(per_launch)  # one kernel launch per step
+    launch_ms = statistics.mean(per_launch)  # the whole step's launches
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash(GATED_SOURCES if w.gated else KERNEL_SOURCES)
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes"] if tr and tr.get("source") == src_hash and not final_state else None
 
@@ -500,14 +550,8 @@ def run_ours(args, w):
                        if w.steps or ncopy == 1 else
                           (f"working set {byts / 1e6:.0f} MB < L2: steps rotate "
                            f"over {ncopy} input/output copies")),
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs,
-                     "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-                                    if peak_src == "measured" else "fallback",
-                     "algorithmic_bytes": byts,
-                     "tflops": flops / (launch_ms / 1e3) / 1e12,
-                     "tensor_peak_tflops": tc_peak},
+        "roofline": roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src,
+                                   tc_peak, traffic, launches_per_step),
         "cpu_baseline": cpu,
         "e2e": None if e2e_s is None else {
             "value": tokens_rank * ws / e2e_s, "unit": "tokens/s",
@@ -518,6 +562,27 @@ def run_ours(args, w):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traffic,
+                   launches):
+    """HBM roofline for the forward and decode kernels; for the gated
+    CUDA-core kernel, the fp32 ALU roofline (its bound), with the HBM figure
+    beside it.  Timed over the whole step (all of its launches)."""
+    achieved_gbs = byts / (launch_ms / 1e3) / 1e9
+    tflops = flops / (launch_ms / 1e3) / 1e12
+    hbm_src = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+               else "fallback")
+    if w.gated:
+        return {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
+                "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": traffic,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                "algorithmic_flops": flops, "algorithmic_bytes": byts,
+                "hbm_achieved_gbs": achieved_gbs, "hbm_frac": achieved_gbs / hbm_peak,
+                "hbm_peak_source": hbm_src, "launches_per_step": launches}
+    return {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved_gbs / hbm_peak, "traffic": traffic, "peak_source": hbm_src,
+            "algorithmic_bytes": byts, "tflops": tflops, "tensor_peak_tflops": tc_peak}
 
 
 def main(argv=None):

@@ -18,7 +18,10 @@
  *   - non-causal: S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j) over every
  *                 key, shared by every query ("The Kernel Trick for
  *                 Attention"; "Linear Attention (the core trick)");
- *   - decode:     one step of the causal recurrence on a caller-held state.
+ *   - decode:     one step of the causal recurrence on a caller-held state;
+ *   - gated:      the causal recurrence with a data-dependent gate per key
+ *                 feature and token ("Gating and Selective State Updates",
+ *                 gated linear attention), forward and decode step.
  * eps is added to the denominator after the dot product, as in the NumPy
  * listing on "Linear Attention Mechanisms" (sadullah.online), "The linear
  * attention trick".
@@ -135,6 +138,45 @@ LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
                            float *S, float *z, void *o, int B, int H, int D,
                            int Dv, const float *gamma, float eps,
                            la_dtype_t dtype, void *stream);
+
+/*
+ * Gated causal forward (gated linear attention): per token t
+ *   S_t = diag(a_t) S_{t-1} + phi(k_t) v_t^T,  z_t = a_t (.) z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t / (phi(q_t) . z_t + eps),   S_{-1} = 0, z_{-1} = 0,
+ * i.e. the data-dependent gate G_t of "Linear Attention Mechanisms"
+ * (dileepadev.github.io), "Gating and Selective State Updates", taken as one
+ * value per key feature and token, G_t = a_t 1^T (row d of S is scaled by
+ * a_t[d]), and applied to the normaliser z as well.  a_t = 1 everywhere is
+ * la_forward(causal = 1, gamma = NULL); a_t = gamma[h] everywhere is the
+ * fixed decay; a_t[d] = 0 clears row d of the state before token t's update.
+ * q, k: [B][H][N][D]; v, o: [B][H][N][Dv] (dtype); a: [B][H][N][D] fp32 in
+ * DEVICE memory, every value in [0, 1] (the library cannot check device
+ * values: outside [0, 1] the result is unspecified, a NaN gate gives NaN
+ * outputs).  S: [B][H][D][Dv] fp32 and z: [B][H][D] fp32 are both NULL or
+ * both set; when set they receive the state after the last token (zero for
+ * N = 0).  fp32 arithmetic on CUDA cores for every dtype; a sequence-split
+ * workspace of about B*H*(P-1)*(D*Dv + 2D)*4 bytes (P <= ceil(N/64) parts)
+ * is taken with cudaMallocAsync on `stream` and released on it.  No written
+ * buffer may overlap another buffer.  Errors as la_forward.
+ */
+LA_API la_status_t la_forward_gated(const void *q, const void *k, const void *v,
+                                    const float *a, void *o, float *S, float *z, int B,
+                                    int H, int N, int D, int Dv, float eps,
+                                    la_dtype_t dtype, void *stream);
+
+/*
+ * One gated decode step, in place: first
+ *   S <- diag(a) S + phi(k) v^T,  z <- a (.) z + phi(k),
+ * then  o = phi(q)^T S / (phi(q) . z + eps)  with the updated state (the
+ * recurrence of la_forward_gated for one token).  q, k: [B][H][D]; v, o:
+ * [B][H][Dv] (dtype); a: [B][H][D] fp32 gates in [0, 1] (device); S:
+ * [B][H][D][Dv] fp32 and z: [B][H][D] fp32 are read and rewritten.  No
+ * buffer may overlap another.  Errors as la_decode_step.
+ */
+LA_API la_status_t la_decode_gated(const void *q, const void *k, const void *v,
+                                   const float *a, float *S, float *z, void *o, int B,
+                                   int H, int D, int Dv, float eps, la_dtype_t dtype,
+                                   void *stream);
 
 /*
  * Which kernel la_forward would run for a causal call with these arguments:

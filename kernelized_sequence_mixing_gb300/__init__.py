@@ -11,6 +11,9 @@ Functions (same names as the C entry points, minus the ``la_`` prefix):
   forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None)
   prefill_state(k, v, gamma=None, S=None, z=None)
   decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None)
+  forward_state(q, k, v, gamma=None, eps=1e-6, out=None, S=None, z=None)
+  forward_gated(q, k, v, a, eps=1e-6, out=None, return_state=False, S=None, z=None)
+  decode_gated(q, k, v, a, S, z, eps=1e-6, out=None)
 """
 from __future__ import annotations
 
@@ -22,7 +25,8 @@ import torch
 
 from . import workloads  # noqa: F401  (seeded input generators)
 
-__all__ = ["forward", "prefill_state", "decode_step", "status_string",
+__all__ = ["forward", "prefill_state", "decode_step", "forward_state",
+           "forward_gated", "decode_gated", "status_string",
            "device_wait_timeouts", "causal_kernel",
            "load_library", "library_path", "LinAttnError", "workloads"]
 
@@ -68,6 +72,11 @@ def load_library() -> ctypes.CDLL:
             lib.la_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, FP, F,
                                            I, P]
             lib.la_decode_step.restype = I
+            lib.la_forward_gated.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F,
+                                             I, P]
+            lib.la_forward_gated.restype = I
+            lib.la_decode_gated.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, P]
+            lib.la_decode_gated.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
             lib.la_device_wait_timeouts.argtypes = [I]
@@ -255,4 +264,63 @@ def decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None):
             _ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out), B, H, D,
             Dv, _gamma_arg(gamma, H), float(eps), _dtype_code(q),
             _stream(dev)))
+    return out
+
+
+def forward_gated(q, k, v, a, eps=1e-6, out=None, return_state=False, S=None, z=None):
+    """Gated causal forward: S_t = diag(a_t) S_(t-1) + phi(k_t) v_t^T,
+    z_t = a_t * z_(t-1) + phi(k_t), o_t = phi(q_t)^T S_t / (phi(q_t).z_t + eps).
+    q, k: [B, H, N, D]; v: [B, H, N, Dv] CUDA tensors of one dtype; a:
+    [B, H, N, D] float32 gates in [0, 1] on the same device.  Returns o, or
+    (o, S [B, H, D, Dv] fp32, z [B, H, D] fp32) with the state after the last
+    token when return_state is true (or S, z are given)."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("a", a)):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if a.shape != q.shape or a.dtype != torch.float32:
+        raise ValueError("a must be float32 with the shape of q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    want_state = return_state or S is not None or z is not None
+    with torch.cuda.device(dev):
+        o = out if out is not None else torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
+        _contig("out", o)
+        if want_state:
+            if S is None:
+                S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
+            if z is None:
+                z = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+            _contig("S", S)
+            _contig("z", z)
+        _check("la_forward_gated", lib.la_forward_gated(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o),
+            _ptr(S) if want_state else None, _ptr(z) if want_state else None,
+            B, H, N, D, Dv, float(eps), _dtype_code(q), _stream(dev)))
+    return (o, S, z) if want_state else o
+
+
+def decode_gated(q, k, v, a, S, z, eps=1e-6, out=None):
+    """One gated recurrent step in place on (S, z): S <- diag(a) S +
+    phi(k) v^T, z <- a * z + phi(k), then read out with q.  q, k, a: [B, H, D]
+    (a float32); v: [B, H, Dv]; S: [B, H, D, Dv] fp32; z: [B, H, D] fp32 (all
+    CUDA).  Returns o: [B, H, Dv]."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("a", a), ("S", S), ("z", z)):
+        _contig(n, t)
+    if a.dtype != torch.float32 or a.shape != q.shape:
+        raise ValueError("a must be float32 with the shape of q")
+    B, H, D = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty((B, H, Dv), dtype=q.dtype, device=dev)
+        _check("la_decode_gated", lib.la_decode_gated(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S), _ptr(z), _ptr(out), B, H, D,
+            Dv, float(eps), _dtype_code(q), _stream(dev)))
     return out

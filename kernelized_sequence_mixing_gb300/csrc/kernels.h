@@ -96,4 +96,20 @@ cudaError_t launch_decode_step(const void *q, const void *k, const void *v,
                                int D, int Dv, bool decay, const Gammas &g,
                                float eps, Dtype dt, cudaStream_t s);
 
+// One gated decode step in place on S, z: row d of S and z[d] scaled by
+// a[(b, h)][d] (fp32 gates in [0, 1]) before the update.
+cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, const float *a,
+                                float *S, float *z, void *o, int B, int H, int D, int Dv,
+                                float eps, Dtype dt, cudaStream_t s);
+
+// Gated causal forward on CUDA cores (gla_simt.cu): gates a [B*H][N][D] fp32
+// in [0, 1], one per key feature and token.  gla_parts() gives the number of
+// sequence parts, gla_workspace_bytes() the per-part records (0 for one
+// part).  S_out, z_out (optional, both or neither): the state after the last
+// token, [B*H][D][Dv] and [B*H][D] fp32.
+int gla_parts(int BH, int N, int Dv);
+size_t gla_workspace_bytes(int BH, int P, int D, int Dv);
+cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, float *S_out,
+                            float *z_out, cudaStream_t s);
+
 }  // namespace linattn

@@ -302,4 +302,74 @@ la_status_t la_decode_step(const void *q, const void *k, const void *v,
                                       static_cast<cudaStream_t>(stream)));
 }
 
+la_status_t la_forward_gated(const void *q, const void *k, const void *v, const float *a,
+                             void *o, float *S, float *z, int B, int H, int N, int D, int Dv,
+                             float eps, la_dtype_t dtype, void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  if ((S == nullptr) != (z == nullptr)) return LA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  if (BH == 0) return LA_OK;
+  const size_t nS = sizeof(float) * (size_t)BH * D * Dv, nz = sizeof(float) * (size_t)BH * D;
+  if (S) {
+    if (!aligned16(S) || !aligned16(z) || overlaps(S, nS, z, nz)) return LA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    if (S && (cudaMemsetAsync(S, 0, nS, s) != cudaSuccess || cudaMemsetAsync(z, 0, nz, s) != cudaSuccess))
+      return LA_ERR_CUDA;
+    return LA_OK;
+  }
+  if (!q || !k || !v || !a || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(o))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * Dv * es;
+  const size_t na = sizeof(float) * (size_t)BH * N * D;
+  const void *ins[4] = {q, k, v, a};
+  const size_t insz[4] = {nqk, nqk, nv, na};
+  for (int i = 0; i < 4; ++i) {
+    if (overlaps(o, nv, ins[i], insz[i])) return LA_ERR_INVALID_ARG;
+    if (S && (overlaps(S, nS, ins[i], insz[i]) || overlaps(z, nz, ins[i], insz[i])))
+      return LA_ERR_INVALID_ARG;
+  }
+  if (S && (overlaps(S, nS, o, nv) || overlaps(z, nz, o, nv))) return LA_ERR_INVALID_ARG;
+  const Problem p{q, k, v, o, B, H, N, D, Dv, false, eps, dtype == LA_F32 ? kF32 : kBF16};
+  const int P = gla_parts(BH, N, Dv);
+  const size_t wsb = gla_workspace_bytes(BH, P, D, Dv);
+  void *ws = nullptr;
+  if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
+  cudaError_t e = launch_gla_simt(p, a, ws, P, S, z, s);
+  cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(ef);
+}
+
+la_status_t la_decode_gated(const void *q, const void *k, const void *v, const float *a,
+                            float *S, float *z, void *o, int B, int H, int D, int Dv, float eps,
+                            la_dtype_t dtype, void *stream) {
+  la_status_t st = check_sizes(B, H, 1, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  if (BH == 0) return LA_OK;
+  if (!q || !k || !v || !a || !S || !z || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(a) || !aligned16(S) ||
+      !aligned16(z) || !aligned16(o))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const void *ptr[7] = {q, k, v, a, S, z, o};
+  const size_t len[7] = {(size_t)BH * D * es, (size_t)BH * D * es, (size_t)BH * Dv * es,
+                         sizeof(float) * (size_t)BH * D, sizeof(float) * (size_t)BH * D * Dv,
+                         sizeof(float) * (size_t)BH * D, (size_t)BH * Dv * es};
+  // the written buffers (S, z, o) may overlap nothing
+  for (int w = 4; w < 7; ++w)
+    for (int i = 0; i < 7; ++i)
+      if (i != w && overlaps(ptr[w], len[w], ptr[i], len[i])) return LA_ERR_INVALID_ARG;
+  return from_cuda(launch_decode_gated(q, k, v, a, S, z, o, B, H, D, Dv, eps,
+                                       dtype == LA_F32 ? kF32 : kBF16,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

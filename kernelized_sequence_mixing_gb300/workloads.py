@@ -1,8 +1,9 @@
 """Seeded synthetic workloads: shapes, seeds and input generators.
 
 This module holds no arithmetic of the method itself.  It only draws the
-inputs (q, k, v and the per-head decay values) that both the CUDA path and
-the CPU oracle consume, so the two sides always see the same numbers.
+inputs (q, k, v, the per-head decay values and the per-feature gates) that
+both the CUDA path and the CPU oracle consume, so the two sides always see the
+same numbers.
 
 Recipe: a CPU ``torch.Generator`` seeded per workload draws fp32 N(0, 1)
 samples in the order q, k, v; they are multiplied by the workload's scale and
@@ -34,6 +35,9 @@ class Workload:
     # decode workloads: number of single-token steps after the prefill of N
     steps: int = 0
     step_seed0: int = 0
+    # gated workloads: fp32 gates a [B, H, N, D] uniform in [gate_lo, 1)
+    gated: bool = False
+    gate_lo: float = 0.9
 
     @property
     def tokens(self) -> int:
@@ -71,6 +75,10 @@ WORKLOADS = {
                                       65536, 64, 64, torch.bfloat16, 0.5, 3),
     # decode: 256 sequences x H32, D=Dv=128; prefill of 512 tokens (seed 4),
     # then 1024 single-token steps with fresh inputs from seed 1000 + t
+    # gated (one gate per key feature and token), bf16, B2 H16 N16384
+    # D=Dv=128, gates U[0.9, 1) from seed 5 + 1
+    "gla_bf16_n16384": Workload("gla_bf16_n16384", True, 2, 16, 16384, 128,
+                                128, torch.bfloat16, 0.5, 5, gated=True),
     "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
                                 128, torch.bfloat16, 0.5, 4, steps=1024,
                                 step_seed0=1000),
@@ -103,3 +111,25 @@ def decode_step_inputs(w: Workload, t: int, device="cpu"):
     q, k, v = make_qkv(w.B, w.H, 1, w.D, w.Dv, w.dtype, w.step_seed0 + t,
                        w.scale, device)
     return q[:, :, 0], k[:, :, 0], v[:, :, 0]
+
+
+def make_gates(B, H, N, D, seed=0, lo=0.9, hi=1.0, zero_frac=0.0, one_frac=0.0,
+               device="cpu"):
+    """Gates a: [B, H, N, D] fp32, uniform in [lo, hi) from a CPU generator
+    seeded with ``seed``; then a ``zero_frac`` share of the entries (drawn
+    from the same generator) is set to exactly 0 and a ``one_frac`` share to
+    exactly 1."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    a = torch.rand((B, H, N, D), generator=g, dtype=torch.float32) * (hi - lo) + lo
+    a.clamp_(0.0, 1.0)
+    if zero_frac > 0:
+        a[torch.rand(a.shape, generator=g) < zero_frac] = 0.0
+    if one_frac > 0:
+        a[torch.rand(a.shape, generator=g) < one_frac] = 1.0
+    return a.to(device)
+
+
+def workload_gates(w: Workload, device="cpu"):
+    """The gates of a gated workload (seed + 1, uniform in [gate_lo, 1))."""
+    return make_gates(w.B, w.H, w.N, w.D, w.seed + 1, w.gate_lo, 1.0, device=device)

@@ -35,6 +35,7 @@ def declared_symbols():
 def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
+              "la_forward_gated", "la_decode_gated",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -144,6 +145,48 @@ def test_decode_rejects_bad_arguments(lib):
     assert call(D=100) == UNSUPPORTED
     assert call(g=(ctypes.c_float * 2)(1.0, -0.5)) == INVALID
     assert call(B=0, p=[None] * 6) == OK
+
+
+def test_forward_gated_rejects_bad_arguments(lib):
+    Fg = lib.la_forward_gated
+    Fg.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                                ctypes.c_void_p]
+    q, k, v, a, o, S, z = (A + i * STEP for i in range(7))
+
+    def call(qq=q, kk=k, vv=v, aa=a, oo=o, SS=S, zz=z, B=1, H=2, N=8, D=128, Dv=128,
+             eps=1e-6, dt=BF16):
+        return Fg(qq, kk, vv, aa, oo, SS, zz, B, H, N, D, Dv, eps, dt, None)
+
+    assert call(SS=None) == INVALID             # S without z
+    assert call(zz=None) == INVALID             # z without S
+    assert call(aa=None) == INVALID             # no gates
+    assert call(aa=a + 4) == INVALID            # misaligned gates
+    assert call(oo=a + 64) == INVALID           # o inside the gates
+    assert call(SS=a) == INVALID                # S aliases the gates
+    assert call(zz=o + 16) == INVALID           # z inside o
+    assert call(oo=q) == INVALID                # o aliases q
+    assert call(eps=float("nan")) == INVALID
+    assert call(D=96) == UNSUPPORTED
+    assert call(dt=7) == INVALID
+    assert call(B=0, qq=None, kk=None, vv=None, aa=None, oo=None, SS=None, zz=None) == OK
+
+
+def test_decode_gated_rejects_bad_arguments(lib):
+    Dg = lib.la_decode_gated
+    Dg.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int,
+                                                                ctypes.c_void_p]
+    ptrs = [A + i * STEP for i in range(7)]     # q, k, v, a, S, z, o
+
+    def call(p=ptrs, B=2, H=2, D=128, Dv=128, eps=1e-6, dt=BF16):
+        return Dg(*p, B, H, D, Dv, eps, dt, None)
+
+    assert call(p=ptrs[:3] + [None] + ptrs[4:]) == INVALID       # no gates
+    assert call(p=ptrs[:4] + [ptrs[3]] + ptrs[5:]) == INVALID    # S aliases a
+    assert call(p=ptrs[:6] + [ptrs[4] + 32]) == INVALID          # o inside S
+    assert call(p=ptrs[:3] + [ptrs[3] + 8] + ptrs[4:]) == INVALID  # misaligned a
+    assert call(eps=-1.0) == INVALID
+    assert call(Dv=32) == UNSUPPORTED
+    assert call(B=0, p=[None] * 7) == OK
 
 
 def test_causal_kernel_dispatch(lib):
