@@ -133,3 +133,30 @@ def make_gates(B, H, N, D, seed=0, lo=0.9, hi=1.0, zero_frac=0.0, one_frac=0.0,
 def workload_gates(w: Workload, device="cpu"):
     """The gates of a gated workload (seed + 1, uniform in [gate_lo, 1))."""
     return make_gates(w.B, w.H, w.N, w.D, w.seed + 1, w.gate_lo, 1.0, device=device)
+
+
+def favor_matrix(r, D, seed=0, orthogonal=True, dtype=torch.float32, device="cpu"):
+    """Random directions W [r, D] for the Performer feature map, drawn on the
+    CPU in fp64 and rounded once to ``dtype``.
+
+    orthogonal=False: every entry N(0, 1).  orthogonal=True (positive
+    orthogonal random features): each block of D rows is the transpose of the
+    Q factor of a D x D Gaussian matrix (signs fixed by R's diagonal, so the
+    block is Haar-distributed), and every row is rescaled by the norm of a
+    fresh D-dimensional Gaussian vector, so each row is still marginally
+    N(0, I) while the rows of a block are exactly orthogonal."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    if not orthogonal:
+        W = torch.randn((r, D), generator=g, dtype=torch.float64)
+    else:
+        blocks = []
+        for _ in range(-(-r // D)):
+            G = torch.randn((D, D), generator=g, dtype=torch.float64)
+            Q, R = torch.linalg.qr(G)
+            Q = Q * torch.sign(torch.diagonal(R))
+            blocks.append(Q.T)
+        W = torch.cat(blocks)[:r]
+        norms = torch.randn((r, D), generator=g, dtype=torch.float64).norm(dim=1)
+        W = W * norms[:, None]
+    return W.to(dtype).to(device)
