@@ -27,8 +27,21 @@
 // suffix products are at most 1, so no threshold is needed), and its gate
 // product g_p.  A scan turns the records into the state after each part,
 // S_after(p) = diag(g_p) S_after(p-1) + A_p, and the output pass runs each
-// part from the state after the previous one.  One CTA owns one (batch, head,
-// part) and a 32-column slice of Dv.
+// part from the state after the previous one.
+//
+// One CTA (8 warps) owns one (batch, head, part) and a 32-column slice of Dv;
+// about 109 KB of shared memory at D = 128, so two CTAs share an SM and one
+// loads while the other computes.  Per chunk:
+//   load   lane l of warp w holds tokens l and 32 + l of feature groups
+//          {w, w + 8} (8 features each): 16-byte loads, the prefix (or
+//          suffix) products of the gates by warp shuffles, the scaled
+//          features stored transposed ([feature][token]) without bank
+//          conflicts;
+//   A      16 x 16 threads, 4 x 4 register tiles of qc kc^T, masked, stored
+//          transposed ([s][t]);
+//   output 4 tokens x 2 columns per thread (two shared loads per 8 FMAs);
+//   state  4 feature rows x 4 columns per thread (two 16-byte shared loads
+//          per 16 FMAs).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,19 +51,17 @@ namespace {
 constexpr int kC = 64;        // tokens per chunk
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLd = kC + 4;   // row stride of the transposed tiles
+constexpr int kLdA = kC + 4;  // row stride of the transposed A tile
 constexpr int kDvs = 32;      // Dv columns per CTA
 constexpr float kMinProd = 0x1p-100f;
 
 template <int D>
 struct GlaLayout {
-  static constexpr int tile = D * kLd;
-  static constexpr int total = 3 * tile + kC * kDvs + D * kDvs + 3 * D + kC +
+  static constexpr int tile = D * kC;  // [D][kC] transposed features
+  static constexpr int total = 2 * tile + kC * kLdA + kC * kDvs + D * kDvs + 3 * D + kC +
                                2 * kWarps * kDvs + 2 * kWarps;
   static constexpr size_t bytes = sizeof(float) * total;
 };
-// the masked A tile reuses the gate tile once the prefix products are taken
-static_assert(kC * (kC + 1) <= 64 * kLd, "A tile must fit in the gate tile");
 
 enum { kPassState = 0, kPassOut = 1 };
 
@@ -63,52 +74,73 @@ __host__ __device__ constexpr size_t record_floats() {
   return static_cast<size_t>(D) * DV + 2 * D;  // A_p | z part | g_p
 }
 
-// Row d of the state slice: S = c (S + sum_s kc_s v_s) when `fold`, else
-// S = c S + sum_s kc_s v_s; z likewise.  Warp w owns rows d = w, w + 8, ...
-template <int D>
-__device__ __forceinline__ void state_update(float *Ss, float *zs, const float *fkT,
-                                             const float *vs, const float *cl, int nv,
-                                             bool fold, int warp, int lane) {
-  for (int d = warp; d < D; d += kWarps) {
-    float acc = 0.f, zp = 0.f;
-    for (int s = 0; s < nv; ++s) acc = fmaf(fkT[d * kLd + s], vs[s * kDvs + lane], acc);
-    for (int s = lane; s < nv; s += 32) zp += fkT[d * kLd + s];
+// 8 consecutive values widened to fp32 (16-byte aligned source).
+__device__ __forceinline__ void load8(const float *p, float *x) {
+  const float4 a = *reinterpret_cast<const float4 *>(p);
+  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *x) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) zp += __shfl_xor_sync(0xffffffffu, zp, off);
-    const float c = cl[d];
-    if (fold) {
-      Ss[d * kDvs + lane] = c * (Ss[d * kDvs + lane] + acc);
-      if (lane == 0) zs[d] = c * (zs[d] + zp);
-    } else {
-      Ss[d * kDvs + lane] = fmaf(c, Ss[d * kDvs + lane], acc);
-      if (lane == 0) zs[d] = fmaf(c, zs[d], zp);
-    }
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
+}
+
+__device__ __forceinline__ void store2(float *p, float a, float b) {
+  *reinterpret_cast<float2 *>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void store2(__nv_bfloat16 *p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// Inclusive products along the warp: lane l gets x_0 * ... * x_l.
+__device__ __forceinline__ float scan_prod(float x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x *= y;
+  }
+  return x;
+}
+// Inclusive suffix products: lane l gets x_l * ... * x_31.
+__device__ __forceinline__ float scan_prod_rev(float x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x *= y;
+  }
+  return x;
 }
 
 // grid: x = (batch, head) * Pg + part, y = Dv / 32; Pg = P - 1 for the state
 // pass (the last part needs no record), P for the output pass.
 template <int D, int DV, int PASS, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     gla_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ a,
                     T *__restrict__ o, float *__restrict__ rec,
                     float *__restrict__ S_out, float *__restrict__ z_out, int N,
                     int P, int Pg, float eps) {
+  constexpr int NG = D / 64;  // feature groups of 8 per warp
+  constexpr int RD = D / 32;  // state rows per thread
   extern __shared__ float4 smem4[];
   using L = GlaLayout<D>;
-  float *fqT = reinterpret_cast<float *>(smem4);  // [D][kLd] phi(q)^T, then qc^T
-  float *fkT = fqT + L::tile;                     // [D][kLd] phi(k)^T, then kc^T
-  float *aT = fkT + L::tile;                      // [D][kLd] gates^T
-  float *As = aT;                                 // [kC][kC+1] masked A tile
-  float *vs = aT + L::tile;                       // [kC][kDvs]
-  float *Ss = vs + kC * kDvs;                     // [D][kDvs] state slice
-  float *zs = Ss + D * kDvs;                      // [D]
-  float *cl = zs + D;                             // [D] c_last of the chunk
-  float *gp = cl + D;                             // [D] gate product of the part
-  float *den = gp + D;                            // [kC]
-  float *red = den + kC;                          // [2][kWarps][kDvs]
-  float *redz = red + 2 * kWarps * kDvs;          // [2][kWarps]
+  float *fq = reinterpret_cast<float *>(smem4);  // [D][kC] qc (or phi(q))
+  float *fk = fq + L::tile;                      // [D][kC] kc (or phi(k))
+  float *AT = fk + L::tile;                      // [kC][kLdA] masked A, transposed
+  float *vs = AT + kC * kLdA;                    // [kC][kDvs]
+  float *Ss = vs + kC * kDvs;                    // [D][kDvs] state slice
+  float *zs = Ss + D * kDvs;                     // [D]
+  float *cl = zs + D;                            // [D] c_last of the chunk
+  float *gp = cl + D;                            // [D] gate product of the part
+  float *den = gp + D;                           // [kC]
+  float *red = den + kC;                         // [2][kWarps][kDvs]
+  float *redz = red + 2 * kWarps * kDvs;         // [2][kWarps]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bh = blockIdx.x / Pg, part = blockIdx.x % Pg;
@@ -131,176 +163,295 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = tid; i < D; i += kThreads) gp[i] = 1.f;
   __syncthreads();
 
-  const int ty = tid >> 4, tx = tid & 15;  // 16 x 16 grid over the A tile
   for (int c = cb; c < ce; ++c) {
     const int c0 = c * kC, nv = min(kC, N - c0);
-    // 1. phi(q), phi(k) and the gates, transposed; the v slice.  Rows past the
-    //    end of the sequence: zero features, gate 1.
-    for (int i = tid; i < kC * D; i += kThreads) {
-      const int t = i / D, d = i % D;
-      float xq = 0.f, xk = 0.f, xa = 1.f;
-      if (t < nv) {
-        const int64_t off = qk0 + static_cast<int64_t>(c0 + t) * D + d;
-        if (PASS == kPassOut) xq = phi_f32(io<T>::load(q + off));
-        xk = phi_f32(io<T>::load(k + off));
-        xa = a[off];
+    // ---- load: tokens t = lane + 32 h, features 8 g .. 8 g + 7 for the
+    // groups g = w + 8 gi.  phi(q), phi(k) go to shared memory as they are
+    // (transposed; rows past the end are 0), the gates stay in registers.
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = lane + 32 * h, g = warp + kWarps * gi;
+        float xk[8], xq[8];
+        if (t < nv) {
+          const int64_t off = qk0 + static_cast<int64_t>(c0 + t) * D + 8 * g;
+          load8(k + off, xk);
+          if (PASS == kPassOut) load8(q + off, xq);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            xk[j] = phi_f32(xk[j]);
+            if (PASS == kPassOut) xq[j] = phi_f32(xq[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xk[j] = xq[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          fk[(8 * g + j) * kC + t] = xk[j];
+          if (PASS == kPassOut) fq[(8 * g + j) * kC + t] = xq[j];
+        }
       }
-      if (PASS == kPassOut) fqT[d * kLd + t] = xq;
-      fkT[d * kLd + t] = xk;
-      aT[d * kLd + t] = xa;
+    float xa[NG][2][8];
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = lane + 32 * h, g = warp + kWarps * gi;
+        if (t < nv) {
+          load8(a + qk0 + static_cast<int64_t>(c0 + t) * D + 8 * g, xa[gi][h]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xa[gi][h][j] = 1.f;
+        }
+      }
+    {
+      const int row = tid >> 2, col = 8 * (tid & 3);
+      float xv[8];
+      if (row < nv) {
+        load8(v + v0 + static_cast<int64_t>(c0 + row) * DV + e0 + col, xv);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xv[j] = 0.f;
+      }
+      *reinterpret_cast<float4 *>(vs + row * kDvs + col) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      *reinterpret_cast<float4 *>(vs + row * kDvs + col + 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
     }
-    for (int i = tid; i < kC * kDvs; i += kThreads) {
-      const int t = i / kDvs, e = i % kDvs;
-      vs[i] = t < nv ? io<T>::load(v + v0 + static_cast<int64_t>(c0 + t) * DV + e0 + e) : 0.f;
-    }
-    __syncthreads();
 
     if (PASS == kPassState) {
-      // suffix products: kc_s = phi(k_s) prod_(u>s) a_u, c_last = prod a
-      if (tid < D) {
-        float suf = 1.f;
-        for (int t = kC - 1; t >= 0; --t) {
-          fkT[tid * kLd + t] *= suf;
-          suf *= aT[tid * kLd + t];
-        }
-        cl[tid] = suf;
-        gp[tid] *= suf;
-      }
-      __syncthreads();
-      state_update<D>(Ss, zs, fkT, vs, cl, nv, false, warp, lane);
-      __syncthreads();
-      continue;
-    }
-
-    bool hard = false;  // some feature forgets below 2^-100 within the chunk
-    if (tid < D) {
-      float cp = 1.f;
-      for (int t = 0; t < nv; ++t) cp *= aT[tid * kLd + t];
-      hard = !(cp >= kMinProd);
-    }
-    if (!__syncthreads_or(hard)) {
-      // 2. prefix products: qc_t = c_t phi(q_t), kc_s = phi(k_s) / c_s
-      if (tid < D) {
-        float cp = 1.f;
-        for (int t = 0; t < kC; ++t) {
-          cp *= aT[tid * kLd + t];
-          fqT[tid * kLd + t] *= cp;
-          fkT[tid * kLd + t] /= cp;
-        }
-        cl[tid] = cp;
-      }
-      __syncthreads();
-      // 3. masked A tile and the denominators
-      {
-        float acc[4][4] = {};
-#pragma unroll 4
-        for (int d = 0; d < D; ++d) {
-          const float4 x = *reinterpret_cast<const float4 *>(fqT + d * kLd + ty * 4);
-          const float4 y = *reinterpret_cast<const float4 *>(fkT + d * kLd + tx * 4);
-          const float xv[4] = {x.x, x.y, x.z, x.w};
-          const float yv[4] = {y.x, y.y, y.z, y.w};
+      // exclusive suffix products: kc_s = phi(k_s) prod_(u>s) a_u (each
+      // thread rescales the entries it stored itself)
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+      for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], yv[j], acc[i][j]);
-        }
-        float rs[4], qz[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = ty * 4 + i;
-          rs[i] = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int s = tx * 4 + j;
-            const float x = s <= t ? acc[i][j] : 0.f;
-            As[t * (kC + 1) + s] = x;
-            rs[i] += x;
+        for (int j = 0; j < 8; ++j) {
+          const float s1 = scan_prod_rev(xa[gi][1][j], lane);
+          const float p1 = __shfl_sync(0xffffffffu, s1, 0);
+          const float s0 = scan_prod_rev(xa[gi][0][j], lane) * p1;
+          float e1 = __shfl_down_sync(0xffffffffu, s1, 1);
+          float e0x = __shfl_down_sync(0xffffffffu, s0, 1);
+          if (lane == 31) {
+            e1 = 1.f;
+            e0x = p1;
           }
-          float p = 0.f;  // qc_t . z_in, split over the 16 tx lanes
-          for (int d = tx; d < D; d += 16) p = fmaf(fqT[d * kLd + t], zs[d], p);
-          qz[i] = p;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int off = 8; off > 0; off >>= 1) {
-            rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], off);
-            qz[i] += __shfl_xor_sync(0xffffffffu, qz[i], off);
+          const int d = 8 * (warp + kWarps * gi) + j;
+          fk[d * kC + lane] *= e0x;
+          fk[d * kC + 32 + lane] *= e1;
+          if (lane == 0) {
+            cl[d] = s0;
+            gp[d] *= s0;
           }
         }
-        if (tx == 0) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) den[ty * 4 + i] = rs[i] + qz[i] + eps;
-        }
-      }
-      __syncthreads();
-      // 4. o_t = (A_t. V + qc_t^T S_in) / den_t; warp w owns rows 8w..8w+7
-      {
-        constexpr int Rw = kC / kWarps;
-        const int t0 = warp * Rw;
-        float num[Rw];
-#pragma unroll
-        for (int r = 0; r < Rw; ++r) num[r] = 0.f;
-        for (int s = 0; s < kC; ++s) {
-          const float vv = vs[s * kDvs + lane];
-#pragma unroll
-          for (int r = 0; r < Rw; ++r) num[r] = fmaf(As[(t0 + r) * (kC + 1) + s], vv, num[r]);
-        }
-#pragma unroll 4
-        for (int d = 0; d < D; ++d) {
-          const float sv = Ss[d * kDvs + lane];
-          const float4 f0 = *reinterpret_cast<const float4 *>(fqT + d * kLd + t0);
-          const float4 f1 = *reinterpret_cast<const float4 *>(fqT + d * kLd + t0 + 4);
-          const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-          for (int r = 0; r < Rw; ++r) num[r] = fmaf(fv[r], sv, num[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < Rw; ++r) {
-          const int t = t0 + r;
-          if (t < nv)
-            io<T>::store(o + v0 + static_cast<int64_t>(c0 + t) * DV + e0 + lane, num[r] / den[t]);
-        }
-      }
-      __syncthreads();
-      // 5. S = diag(c_last) (S + sum_s kc_s v_s^T), z likewise
-      state_update<D>(Ss, zs, fkT, vs, cl, nv, true, warp, lane);
       __syncthreads();
     } else {
-      // The token recurrence: thread (warp w, lane e) owns S[d][e] for
-      // d = w, w + 8, ...; lane 0 also owns z[d].  Partial read-outs meet in a
-      // double-buffered reduction, so one barrier per token suffices.
-      for (int t = 0; t < nv; ++t) {
-        const float ve = vs[t * kDvs + lane];
-        float num = 0.f, qz = 0.f;
-        for (int d = warp; d < D; d += kWarps) {
-          const float al = aT[d * kLd + t], fk = fkT[d * kLd + t], fq = fqT[d * kLd + t];
-          const float sn = fmaf(al, Ss[d * kDvs + lane], fk * ve);
-          Ss[d * kDvs + lane] = sn;
-          num = fmaf(fq, sn, num);
-          if (lane == 0) {
-            const float zn = fmaf(al, zs[d], fk);
-            zs[d] = zn;
-            qz = fmaf(fq, zn, qz);
+      // inclusive prefix products c_t; a chunk is hard if some feature's
+      // product over the chunk falls below 2^-100 (or is NaN)
+      bool hard = false;
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float c0v = scan_prod(xa[gi][0][j], lane);
+          const float c1v = scan_prod(xa[gi][1][j], lane) * __shfl_sync(0xffffffffu, c0v, 31);
+          const float tot = __shfl_sync(0xffffffffu, c1v, 31);
+          hard |= !(tot >= kMinProd);
+          xa[gi][0][j] = c0v;
+          xa[gi][1][j] = c1v;
+        }
+      if (!__syncthreads_or(hard)) {
+        // qc = c_t phi(q_t), kc = phi(k_t) / c_t on the thread's own entries
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int d = 8 * (warp + kWarps * gi) + j;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              fq[d * kC + 32 * h + lane] *= xa[gi][h][j];
+              fk[d * kC + 32 * h + lane] /= xa[gi][h][j];
+            }
+            if (lane == 31) cl[d] = xa[gi][1][j];
+          }
+        __syncthreads();
+        // ---- A = qc kc^T masked (s <= t), stored as AT[s][t]; denominators
+        {
+          const int ty = tid >> 4, tx = tid & 15;
+          float acc[4][4] = {};
+          if (tx <= ty) {
+#pragma unroll 4
+            for (int d = 0; d < D; ++d) {
+              const float4 x = *reinterpret_cast<const float4 *>(fq + d * kC + 4 * ty);
+              const float4 y = *reinterpret_cast<const float4 *>(fk + d * kC + 4 * tx);
+              const float xv[4] = {x.x, x.y, x.z, x.w};
+              const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], yv[j], acc[i][j]);
+            }
+          }
+          float rs[4], qz[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = 4 * ty + i;
+            rs[i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (4 * tx + j > t) acc[i][j] = 0.f;
+              rs[i] += acc[i][j];
+            }
+            float p = 0.f;  // qc_t . z_in, split over the 16 tx lanes
+            for (int d = tx; d < D; d += 16) p = fmaf(fq[d * kC + t], zs[d], p);
+            qz[i] = p;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4 *>(AT + (4 * tx + j) * kLdA + 4 * ty) =
+                make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) {
+              rs[i] += __shfl_xor_sync(0xffffffffu, rs[i], off);
+              qz[i] += __shfl_xor_sync(0xffffffffu, qz[i], off);
+            }
+          }
+          if (tx == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) den[4 * ty + i] = rs[i] + qz[i] + eps;
           }
         }
-        float *rb = red + (t & 1) * kWarps * kDvs;
-        float *rz = redz + (t & 1) * kWarps;
-        rb[warp * kDvs + lane] = num;
-        if (lane == 0) rz[warp] = qz;
         __syncthreads();
-        if (warp == 0) {
-          float n = 0.f, dz = 0.f;
+        // ---- o_t = (A_t. V + qc_t^T S_in) / den_t: 4 tokens x 2 columns
+        {
+          const int ep = tid & 15, tg = tid >> 4;
+          float num[4][2] = {};
+          const int smax = 4 * tg + 4;
+          for (int s = 0; s < smax; ++s) {
+            const float4 w = *reinterpret_cast<const float4 *>(AT + s * kLdA + 4 * tg);
+            const float2 x = *reinterpret_cast<const float2 *>(vs + s * kDvs + 2 * ep);
+            const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            n += rb[w * kDvs + lane];
-            dz += rz[w];
+            for (int i = 0; i < 4; ++i) {
+              num[i][0] = fmaf(wv[i], x.x, num[i][0]);
+              num[i][1] = fmaf(wv[i], x.y, num[i][1]);
+            }
           }
-          io<T>::store(o + v0 + static_cast<int64_t>(c0 + t) * DV + e0 + lane, n / (dz + eps));
+#pragma unroll 4
+          for (int d = 0; d < D; ++d) {
+            const float4 f = *reinterpret_cast<const float4 *>(fq + d * kC + 4 * tg);
+            const float2 sv = *reinterpret_cast<const float2 *>(Ss + d * kDvs + 2 * ep);
+            const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              num[i][0] = fmaf(fv[i], sv.x, num[i][0]);
+              num[i][1] = fmaf(fv[i], sv.y, num[i][1]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = 4 * tg + i;
+            if (t < nv) {
+              const float dn = den[t];
+              store2(o + v0 + static_cast<int64_t>(c0 + t) * DV + e0 + 2 * ep, num[i][0] / dn,
+                     num[i][1] / dn);
+            }
+          }
+        }
+        __syncthreads();
+      } else {
+        // ---- the token recurrence on raw features: thread (warp w, lane e)
+        // owns S[d][e] for d = w, w + 8, ...; lane 0 also owns z[d].  Partial
+        // read-outs meet in a double-buffered reduction (one barrier a token).
+        // The raw features are already in shared memory (the barrier above).
+        const float *ac = a + qk0 + static_cast<int64_t>(c0) * D;
+        for (int t = 0; t < nv; ++t) {
+          const float ve = vs[t * kDvs + lane];
+          float num = 0.f, qzp = 0.f;
+          for (int d = warp; d < D; d += kWarps) {
+            const float al = ac[t * D + d], fkv = fk[d * kC + t], fqv = fq[d * kC + t];
+            const float sn = fmaf(al, Ss[d * kDvs + lane], fkv * ve);
+            Ss[d * kDvs + lane] = sn;
+            num = fmaf(fqv, sn, num);
+            if (lane == 0) {
+              const float zn = fmaf(al, zs[d], fkv);
+              zs[d] = zn;
+              qzp = fmaf(fqv, zn, qzp);
+            }
+          }
+          float *rb = red + (t & 1) * kWarps * kDvs;
+          float *rz = redz + (t & 1) * kWarps;
+          rb[warp * kDvs + lane] = num;
+          if (lane == 0) rz[warp] = qzp;
+          __syncthreads();
+          if (warp == 0) {
+            float n = 0.f, dz = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+              n += rb[w * kDvs + lane];
+              dz += rz[w];
+            }
+            const float ov = n / (dz + eps);
+            o[v0 + static_cast<int64_t>(c0 + t) * DV + e0 + lane] =
+                static_cast<T>(ov);
+          }
+        }
+        __syncthreads();
+        continue;
+      }
+    }
+    // ---- state: S = c_last (S + sum kc v) (output pass) or c_last S +
+    // sum kc v (state pass); z likewise.  4 (D = 128) or 2 feature rows x 4
+    // columns per thread.
+    {
+      const int eq = tid & 7, dq = tid >> 3;
+      float acc[RD][4] = {}, zp[RD] = {};
+#pragma unroll 2
+      for (int s = 0; s < kC; s += 4) {
+        float4 kv[RD], vv[4];
+#pragma unroll
+        for (int r = 0; r < RD; ++r)
+          kv[r] = *reinterpret_cast<const float4 *>(fk + (RD * dq + r) * kC + s);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          vv[j] = *reinterpret_cast<const float4 *>(vs + (s + j) * kDvs + 4 * eq);
+#pragma unroll
+        for (int r = 0; r < RD; ++r) {
+          const float kr[4] = {kv[r].x, kv[r].y, kv[r].z, kv[r].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[r][0] = fmaf(kr[j], vv[j].x, acc[r][0]);
+            acc[r][1] = fmaf(kr[j], vv[j].y, acc[r][1]);
+            acc[r][2] = fmaf(kr[j], vv[j].z, acc[r][2]);
+            acc[r][3] = fmaf(kr[j], vv[j].w, acc[r][3]);
+            zp[r] += kr[j];
+          }
         }
       }
-      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < RD; ++r) {
+        const int d = RD * dq + r;
+        const float cv = cl[d];
+        float4 *sp = reinterpret_cast<float4 *>(Ss + d * kDvs + 4 * eq);
+        float4 sv = *sp;
+        if (PASS == kPassOut) {
+          sv.x = cv * (sv.x + acc[r][0]);
+          sv.y = cv * (sv.y + acc[r][1]);
+          sv.z = cv * (sv.z + acc[r][2]);
+          sv.w = cv * (sv.w + acc[r][3]);
+          if (eq == 0) zs[d] = cv * (zs[d] + zp[r]);
+        } else {
+          sv.x = fmaf(cv, sv.x, acc[r][0]);
+          sv.y = fmaf(cv, sv.y, acc[r][1]);
+          sv.z = fmaf(cv, sv.z, acc[r][2]);
+          sv.w = fmaf(cv, sv.w, acc[r][3]);
+          if (eq == 0) zs[d] = fmaf(cv, zs[d], zp[r]);
+        }
+        *sp = sv;
+      }
     }
+    __syncthreads();
   }
 
   if (PASS == kPassState) {
@@ -384,14 +535,28 @@ cudaError_t gla_shape(const Problem &p, const float *a, float *ws, int P, float 
 
 }  // namespace
 
+// Parts per (batch, head): the count that minimises the estimated time, in
+// units of one part's output pass over the whole sequence, of
+//   waves(P) / P  (output pass)  +  0.25 waves(P - 1) / P  (state pass),
+// with waves(n) = ceil(B*H*(Dv/32)*n / (2 CTAs per SM x SMs)), at most one
+// part per 64-token chunk.
 int gla_parts(int BH, int N, int Dv) {
   if (BH <= 0 || N <= 0) return 1;
   const long long nch = (N + kC - 1) / kC;
   const long long ctas = static_cast<long long>(BH) * (Dv / kDvs);
-  long long P = (2LL * num_sms_gla() + ctas - 1) / ctas;
-  if (P > nch) P = nch;
-  if (P < 1) P = 1;
-  return static_cast<int>(P);
+  const long long slots = 2LL * num_sms_gla();
+  auto waves = [&](long long n) { return (ctas * n + slots - 1) / slots; };
+  const long long pmax = nch < 64 ? nch : 64;
+  long long best = 1;
+  double best_t = static_cast<double>(waves(1));
+  for (long long P = 2; P <= pmax; ++P) {
+    const double t = (static_cast<double>(waves(P)) + 0.25 * static_cast<double>(waves(P - 1))) / P;
+    if (t < best_t * 0.98) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return static_cast<int>(best);
 }
 
 size_t gla_workspace_bytes(int BH, int P, int D, int Dv) {

@@ -52,7 +52,8 @@ GATED_SMALL = [
     (2, 3, 333, 64, 128),
     (1, 2, 1000, 128, 64),
     (1, 1, 4099, 128, 128),
-    (4, 40, 130, 64, 64),      # many (b, h): one sequence part
+    (4, 40, 130, 64, 64),      # many (b, h): three parts of one chunk each
+    (4, 40, 50, 64, 64),       # one chunk: one part, no state pass
 ]
 
 
