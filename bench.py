@@ -38,6 +38,7 @@ METRICS = {
     "noncausal": "non-causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
     "gated": "gated linear-attn fwd tokens/s and % fp32 ALU roofline, 1×GB300",
+    "favor": "Performer (FAVOR+) causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
 }
 
 
@@ -46,6 +47,8 @@ def workload_metric(w):
         return METRICS["decode"]
     if w.gated:
         return METRICS["gated"]
+    if w.favor_r:
+        return METRICS["favor"]
     return METRIC if w.causal else METRICS["noncausal"]
 DEFAULT_WORKLOAD = "causal_decay_bf16_n16384"
 FALLBACK_HBM_GBS = 6800.0  # profiling recipe fallback, used only if absent
@@ -126,6 +129,12 @@ def algorithmic_work(w):
         # per state and normaliser entry
         byts += units * w.D * 4
         flops += units * (w.D * w.Dv + w.D)
+    if w.favor_r:
+        # r features in place of D: the projections of q and k (2 D r flops
+        # each, plus the norm and the exponential) and the attention over r
+        r = w.favor_r
+        byts += r * w.D * es
+        flops = units * (2 * (2 * w.D * r + 2 * w.D + r) + 4 * r * w.Dv + 3 * r + w.Dv)
     return byts, flops
 
 
@@ -143,6 +152,8 @@ def measured_peaks():
 KERNEL_SOURCES = ("chunk128.cu", "chunk_tc.cu", "tc_common.cuh", "common.cuh")
 # sources of the gated CUDA-core kernel
 GATED_SOURCES = ("gla_simt.cu", "common.cuh")
+# sources of the Performer path (feature kernel, then the causal kernel)
+FAVOR_SOURCES = ("favor.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES):
@@ -227,6 +238,9 @@ def oracle_sample(w, heads_per_pass):
     f = lambda t: t.float().reshape(-1, w.N, t.shape[-1])[:heads_per_pass].numpy()  # noqa: E731
     if w.gated:  # the gates in place of per-head decays
         return f(q), f(k), f(v), f(workload_gates(w))
+    if w.favor_r:  # the random directions in place of per-head decays
+        from kernelized_sequence_mixing_gb300.workloads import workload_favor_matrix
+        return f(q), f(k), f(v), workload_favor_matrix(w).float().numpy()
     g = w.gamma()
     gu = None
     if g is not None:
@@ -243,6 +257,9 @@ def time_oracle(w, heads_per_pass, passes):
         t0 = time.perf_counter()
         if w.gated:
             oracle.gated(qs, ks, vs, gu, eps=w.eps, nthreads=threads)
+        elif w.favor_r:
+            from oracle import favor as fv
+            fv.favor(qs, ks, vs, gu, causal=True, eps=w.eps)
         elif w.causal:
             oracle.causal(qs, ks, vs, gamma=gu, eps=w.eps, nthreads=threads)
         else:
@@ -320,6 +337,9 @@ def workload_config(w):
     if w.gated:
         cfg["gates"] = (f"fp32 a [B][H][N][D] uniform in [{w.gate_lo}, 1), one per key "
                         "feature and token")
+    if w.favor_r:
+        cfg["features"] = (f"Performer, r = {w.favor_r} block-orthogonal directions; q, k "
+                           f"~ N(0, 1) * {w.scale:.4f} (D^-1/4)")
     if w.steps:
         cfg.update(seq_len=1, prefill_len=w.N, state="fp32 S [D][Dv] and z [D] "
                    "per (sequence, head), from the prefill",
@@ -338,7 +358,7 @@ def run_ours(args, w):
 
     ws, rank, local = dist_env()
     final_state = bool(getattr(args, "final_state", False))
-    if final_state and (w.steps or not w.causal or w.gated):
+    if final_state and (w.steps or not w.causal or w.gated or w.favor_r):
         raise SystemExit("--final-state applies to the causal forward workloads")
     if ws > 1:
         import torch.distributed as dist
@@ -400,6 +420,27 @@ def run_ours(args, w):
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
             ad.copy_(ah, non_blocking=True)
+            step()
+            oh.copy_(od, non_blocking=True)
+        tokens_rank = w.B * w.N
+    elif w.favor_r:
+        # Performer: the feature kernel (q and k in one launch), then the
+        # causal kernel over the features; the directions stay resident
+        from kernelized_sequence_mixing_gb300.workloads import favor_matrix
+        q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
+        Wd = favor_matrix(w.favor_r, w.D, w.seed + 2, True, w.dtype).to(dev)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
+        ncopy = 1
+        launches_per_step = 2
+
+        def step():
+            la.forward_favor(qd, kd, vd, Wd, causal=True, eps=w.eps, out=od)
+
+        def e2e_step(qh, kh, vh, oh):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
             step()
             oh.copy_(od, non_blocking=True)
         tokens_rank = w.B * w.N
@@ -512,7 +553,8 @@ def run_ours(args, w):
         byts += w.B * w.H * (w.D * w.Dv + w.D) * 4
     launch_ms = statistics.mean(per_launch)  # the whole step's launches
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
-    src_hash = kernel_source_hash(GATED_SOURCES if w.gated else KERNEL_SOURCES)
+    src_hash = kernel_source_hash(GATED_SOURCES if w.gated else
+                                  FAVOR_SOURCES if w.favor_r else KERNEL_SOURCES)
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes"] if tr and tr.get("source") == src_hash and not final_state else None
 

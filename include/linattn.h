@@ -21,7 +21,10 @@
  *   - decode:     one step of the causal recurrence on a caller-held state;
  *   - gated:      the causal recurrence with a data-dependent gate per key
  *                 feature and token ("Gating and Selective State Updates",
- *                 gated linear attention), forward and decode step.
+ *                 gated linear attention), forward and decode step;
+ *   - Performer:  random exponential features in place of elu + 1
+ *                 ("Choosing the Feature Map"), the map alone and the
+ *                 attention over it.
  * eps is added to the denominator after the dot product, as in the NumPy
  * listing on "Linear Attention Mechanisms" (sadullah.online), "The linear
  * attention trick".
@@ -177,6 +180,41 @@ LA_API la_status_t la_decode_gated(const void *q, const void *k, const void *v,
                                    const float *a, float *S, float *z, void *o, int B,
                                    int H, int D, int Dv, float eps, la_dtype_t dtype,
                                    void *stream);
+
+/*
+ * Performer random-feature map: for every row x of x [rows][D],
+ *   phi(x) = r^(-1/2) [exp(w_1 . x - |x|^2/2), ..., exp(w_r . x - |x|^2/2)]
+ * with the directions w_j the rows of W [r][D] (drawn by the caller: iid
+ * N(0, 1), or block-orthogonal rows for positive orthogonal random features).
+ * "Linear Attention Mechanisms" (dileepadev.github.io), "Choosing the Feature
+ * Map": Random Fourier Features (Performer) and FAVOR+.  The -|x|^2/2 term is
+ * the reading under which that passage's E[phi(q) . phi(k)] = exp(q . k)
+ * holds for w ~ N(0, I).
+ * x, W and phi [rows][r] (written) are DEVICE arrays of `dtype`; D and r in
+ * {64, 128}.  LA_BF16 runs a tcgen05 GEMM with the exponential in its
+ * epilogue (exact bf16 products, fp32 sums, phi rounded to bf16); LA_F32 runs
+ * in fp32 on CUDA cores.  exp overflows fp32 where w_j . x - |x|^2/2 > 88.
+ * phi may not overlap x or W.
+ */
+LA_API la_status_t la_favor_features(const void *x, const void *W, void *phi, int rows, int D,
+                                     int r, la_dtype_t dtype, void *stream);
+
+/*
+ * Performer attention: la_favor_features on q and on k, then linear
+ * attention over those r-dimensional features, o_i = phi(q_i)^T S_i /
+ * (phi(q_i)^T z_i + eps), causal (S_i, z_i over j <= i, decayed by
+ * gamma[h]^(i-j)) or non-causal (every j; gamma must be NULL or all 1).  The
+ * attention runs on the same kernels as la_forward with the features in place
+ * of phi(q), phi(k) (tensor cores for LA_BF16).  q, k: [B][H][N][D]; v, o:
+ * [B][H][N][Dv]; W: [r][D]; all of `dtype`; D, Dv and r in {64, 128}.  The
+ * features take a stream-ordered workspace of 2*B*H*N*r elements of `dtype`
+ * (cudaMallocAsync on `stream`), plus the attention kernel's own.  o may not
+ * overlap q, k, v or W.  Errors as la_forward.
+ */
+LA_API la_status_t la_forward_favor(const void *q, const void *k, const void *v, const void *W,
+                                    void *o, int B, int H, int N, int D, int Dv, int r,
+                                    int causal, const float *gamma, float eps,
+                                    la_dtype_t dtype, void *stream);
 
 /*
  * Which kernel la_forward would run for a causal call with these arguments:

@@ -14,6 +14,8 @@ Functions (same names as the C entry points, minus the ``la_`` prefix):
   forward_state(q, k, v, gamma=None, eps=1e-6, out=None, S=None, z=None)
   forward_gated(q, k, v, a, eps=1e-6, out=None, return_state=False, S=None, z=None)
   decode_gated(q, k, v, a, S, z, eps=1e-6, out=None)
+  favor_features(x, W, out=None)
+  forward_favor(q, k, v, W, causal=True, gamma=None, eps=1e-6, out=None)
 """
 from __future__ import annotations
 
@@ -26,7 +28,8 @@ import torch
 from . import workloads  # noqa: F401  (seeded input generators)
 
 __all__ = ["forward", "prefill_state", "decode_step", "forward_state",
-           "forward_gated", "decode_gated", "status_string",
+           "forward_gated", "decode_gated", "favor_features", "forward_favor",
+           "status_string",
            "device_wait_timeouts", "causal_kernel",
            "load_library", "library_path", "LinAttnError", "workloads"]
 
@@ -77,6 +80,11 @@ def load_library() -> ctypes.CDLL:
             lib.la_forward_gated.restype = I
             lib.la_decode_gated.argtypes = [P, P, P, P, P, P, P, I, I, I, I, F, I, P]
             lib.la_decode_gated.restype = I
+            lib.la_favor_features.argtypes = [P, P, P, I, I, I, I, P]
+            lib.la_favor_features.restype = I
+            lib.la_forward_favor.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, FP, F,
+                                             I, P]
+            lib.la_forward_favor.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
             lib.la_device_wait_timeouts.argtypes = [I]
@@ -323,4 +331,53 @@ def decode_gated(q, k, v, a, S, z, eps=1e-6, out=None):
         _check("la_decode_gated", lib.la_decode_gated(
             _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(S), _ptr(z), _ptr(out), B, H, D,
             Dv, float(eps), _dtype_code(q), _stream(dev)))
+    return out
+
+
+def favor_features(x, W, out=None):
+    """Performer random features phi(x) = r^(-1/2) exp(W x - |x|^2 / 2) of
+    every row of x [..., D] with the directions W [r, D] (same dtype, CUDA).
+    Returns [..., r]."""
+    lib = load_library()
+    _contig("x", x)
+    _contig("W", W)
+    if W.dim() != 2 or W.shape[1] != x.shape[-1] or W.dtype != x.dtype:
+        raise ValueError("W must be [r, D] with the dtype of x")
+    D, r = x.shape[-1], W.shape[0]
+    rows = x.numel() // D if D else 0
+    dev = x.device
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty(x.shape[:-1] + (r,), dtype=x.dtype, device=dev)
+        _contig("out", out)
+        _check("la_favor_features", lib.la_favor_features(
+            _ptr(x), _ptr(W), _ptr(out), rows, D, r, _dtype_code(x), _stream(dev)))
+    return out
+
+
+def forward_favor(q, k, v, W, causal=True, gamma=None, eps=1e-6, out=None):
+    """Performer attention: the random features of q and k with the
+    directions W [r, D], then linear attention over them (causal with
+    optional per-head decay, or non-causal).  q, k: [B, H, N, D]; v:
+    [B, H, N, Dv]; all CUDA tensors of one dtype.  Returns o [B, H, N, Dv]."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("W", W)):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if not (q.dtype == k.dtype == v.dtype == W.dtype):
+        raise TypeError("q, k, v and W must share one dtype")
+    if W.dim() != 2 or W.shape[1] != q.shape[-1]:
+        raise ValueError("W must be [r, D]")
+    B, H, N, D = q.shape
+    Dv, r = v.shape[-1], W.shape[0]
+    dev = q.device
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
+        _contig("out", out)
+        _check("la_forward_favor", lib.la_forward_favor(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(W), _ptr(out), B, H, N, D, Dv, r,
+            1 if causal else 0, _gamma_arg(gamma, H), float(eps), _dtype_code(q),
+            _stream(dev)))
     return out

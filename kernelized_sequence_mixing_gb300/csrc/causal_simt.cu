@@ -42,7 +42,7 @@ struct SimtLayout {
   static constexpr size_t bytes = sizeof(float) * total;
 };
 
-template <int D, int DV, bool DECAY, typename T>
+template <int D, int DV, bool DECAY, bool IDENT, typename T>
 __global__ void __launch_bounds__(kThreads)
     causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                        const T *__restrict__ v, T *__restrict__ o, int H,
@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(kThreads)
       const int t = i / D, d = i % D;
       float xq = 0.f, xk = 0.f;
       if (t < nv) {
-        xq = phi_f32(io<T>::load(qh + (int64_t)(c0 + t) * D + d));
-        xk = phi_f32(io<T>::load(kh + (int64_t)(c0 + t) * D + d));
+        xq = feat_f32<IDENT>(io<T>::load(qh + (int64_t)(c0 + t) * D + d));
+        xk = feat_f32<IDENT>(io<T>::load(kh + (int64_t)(c0 + t) * D + d));
       }
       fqT[d * kLd + t] = xq;
       fkT[d * kLd + t] = xk;
@@ -201,9 +201,9 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int D, int DV, bool DECAY, typename T>
+template <int D, int DV, bool DECAY, bool IDENT, typename T>
 cudaError_t launch_typed(const Problem &p, const Gammas &g, cudaStream_t s) {
-  auto kern = causal_simt_kernel<D, DV, DECAY, T>;
+  auto kern = causal_simt_kernel<D, DV, DECAY, IDENT, T>;
   const size_t smem = SimtLayout<D>::bytes;
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -217,8 +217,11 @@ cudaError_t launch_typed(const Problem &p, const Gammas &g, cudaStream_t s) {
 
 template <int D, int DV, typename T>
 cudaError_t launch_decay(const Problem &p, const Gammas &g, cudaStream_t s) {
-  return p.decay ? launch_typed<D, DV, true, T>(p, g, s)
-                 : launch_typed<D, DV, false, T>(p, g, s);
+  if (p.ident)
+    return p.decay ? launch_typed<D, DV, true, true, T>(p, g, s)
+                   : launch_typed<D, DV, false, true, T>(p, g, s);
+  return p.decay ? launch_typed<D, DV, true, false, T>(p, g, s)
+                 : launch_typed<D, DV, false, false, T>(p, g, s);
 }
 
 template <typename T>

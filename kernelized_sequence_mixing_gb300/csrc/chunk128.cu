@@ -147,31 +147,33 @@ struct Chunk128Params {
 
 // phi and the row scale in place on one box row: 8 chunks of 16 bytes of
 // row r of a 128-byte-swizzled box.
+template <bool IDENT>
 __device__ __forceinline__ void map_row(uint8_t *box, int r, uint32_t sc) {
   uint4 x[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) x[c] = *reinterpret_cast<const uint4 *>(box + sw128_off(r, 16 * c));
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    x[c].x = phi_scale_bf16x2(x[c].x, sc);
-    x[c].y = phi_scale_bf16x2(x[c].y, sc);
-    x[c].z = phi_scale_bf16x2(x[c].z, sc);
-    x[c].w = phi_scale_bf16x2(x[c].w, sc);
+    x[c].x = feat_scale_bf16x2<IDENT>(x[c].x, sc);
+    x[c].y = feat_scale_bf16x2<IDENT>(x[c].y, sc);
+    x[c].z = feat_scale_bf16x2<IDENT>(x[c].z, sc);
+    x[c].w = feat_scale_bf16x2<IDENT>(x[c].w, sc);
     *reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * c)) = x[c];
   }
 }
 
 // The same on chunks [c0, c0 + 4) of the row.
+template <bool IDENT>
 __device__ __forceinline__ void map_row4(uint8_t *box, int r, int c0, uint32_t sc) {
   uint4 x[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) x[c] = *reinterpret_cast<const uint4 *>(box + sw128_off(r, 16 * (c0 + c)));
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    x[c].x = phi_scale_bf16x2(x[c].x, sc);
-    x[c].y = phi_scale_bf16x2(x[c].y, sc);
-    x[c].z = phi_scale_bf16x2(x[c].z, sc);
-    x[c].w = phi_scale_bf16x2(x[c].w, sc);
+    x[c].x = feat_scale_bf16x2<IDENT>(x[c].x, sc);
+    x[c].y = feat_scale_bf16x2<IDENT>(x[c].y, sc);
+    x[c].z = feat_scale_bf16x2<IDENT>(x[c].z, sc);
+    x[c].w = feat_scale_bf16x2<IDENT>(x[c].w, sc);
     *reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * (c0 + c))) = x[c];
   }
 }
@@ -189,7 +191,7 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
   tmem_st16(taddr, f);
 }
 
-template <bool DECAY>
+template <bool DECAY, bool IDENT>
 __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_constant__ Chunk128Params p) {
   constexpr size_t kRec = static_cast<size_t>(kD) * kDV + kD;
   extern __shared__ uint8_t smem_raw[];
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
       const int nv = min(kC, N - (cbA + ia) * kC);
       const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
-      map_row4(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
+      map_row4<IDENT>(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kKMapped + sl]);
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int jw = i % WC;  // chunk within its decay window
       // kh_s = gamma^(E - s) phi(k_s), rows past the sequence end zero
       if (!warp_wait(&bar[kKFull + sl], (c >> 1) & 1, abort_flag, p.timeouts)) break;
-      map_row(sm + kOffK + sl * kKSlot + h * kKBox, r,
+      map_row<IDENT>(sm + kOffK + sl * kKSlot + h * kKBox, r,
               r < nv ? scale2(static_cast<float>(W - 1 - kC * jw - r)) : 0u);
       fence_async_smem();
       __syncwarp();
@@ -580,10 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           x[q] = *reinterpret_cast<const uint4 *>(sm + kOffQ + h * kKBox + sw128_off(r, 16 * q));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          qh[4 * q + 0] = phi_scale_bf16x2(x[q].x, sc);
-          qh[4 * q + 1] = phi_scale_bf16x2(x[q].y, sc);
-          qh[4 * q + 2] = phi_scale_bf16x2(x[q].z, sc);
-          qh[4 * q + 3] = phi_scale_bf16x2(x[q].w, sc);
+          qh[4 * q + 0] = feat_scale_bf16x2<IDENT>(x[q].x, sc);
+          qh[4 * q + 1] = feat_scale_bf16x2<IDENT>(x[q].y, sc);
+          qh[4 * q + 2] = feat_scale_bf16x2<IDENT>(x[q].z, sc);
+          qh[4 * q + 3] = feat_scale_bf16x2<IDENT>(x[q].w, sc);
         }
       }
       __syncwarp();
@@ -845,7 +847,8 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
     cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  auto kern = p.decay ? chunk128_kernel<true> : chunk128_kernel<false>;
+  auto kern = p.ident ? (p.decay ? chunk128_kernel<true, true> : chunk128_kernel<false, true>)
+                      : (p.decay ? chunk128_kernel<true, false> : chunk128_kernel<false, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (err != cudaSuccess) return err;
   kern<<<BH * P, kThreads, kAlloc, s>>>(prm);

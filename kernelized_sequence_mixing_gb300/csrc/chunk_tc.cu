@@ -156,7 +156,7 @@ struct ChunkParams {
 // phi and the row scales in place on NB boxes of 64 rows x 128 bytes.  Thread
 // tp (0..127) handles the 16-byte chunks tp + 128 m of every box, which lie in
 // rows (tp / 8) + 16 m, m = 0..3.
-template <int NB>
+template <int NB, bool IDENT>
 __device__ __forceinline__ void map_boxes(uint8_t *box0, const uint32_t sc[4], int tp) {
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
@@ -165,10 +165,10 @@ __device__ __forceinline__ void map_boxes(uint8_t *box0, const uint32_t sc[4], i
     for (int m = 0; m < 4; ++m) x[m] = reinterpret_cast<const uint4 *>(box0 + b * kBox)[tp + 128 * m];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      x[m].x = phi_scale_bf16x2(x[m].x, sc[m]);
-      x[m].y = phi_scale_bf16x2(x[m].y, sc[m]);
-      x[m].z = phi_scale_bf16x2(x[m].z, sc[m]);
-      x[m].w = phi_scale_bf16x2(x[m].w, sc[m]);
+      x[m].x = feat_scale_bf16x2<IDENT>(x[m].x, sc[m]);
+      x[m].y = feat_scale_bf16x2<IDENT>(x[m].y, sc[m]);
+      x[m].z = feat_scale_bf16x2<IDENT>(x[m].z, sc[m]);
+      x[m].w = feat_scale_bf16x2<IDENT>(x[m].w, sc[m]);
       reinterpret_cast<uint4 *>(box0 + b * kBox)[tp + 128 * m] = x[m];
     }
   }
@@ -179,7 +179,7 @@ __device__ __forceinline__ void map_boxes(uint8_t *box0, const uint32_t sc[4], i
 // lo0, so that an MMA pair over both carries about 16 significant bits.  Here
 // 512 threads share the boxes: thread tp handles chunk tp of every box, all
 // in row tp / 8, with the row scale sc.
-template <int NB>
+template <int NB, bool IDENT>
 __device__ __forceinline__ void map_boxes_split(uint8_t *box0, uint8_t *lo0, float sc, int tp) {
   uint4 x[NB];
 #pragma unroll
@@ -194,7 +194,7 @@ __device__ __forceinline__ void map_boxes_split(uint8_t *box0, uint8_t *lo0, flo
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float a = __uint_as_float(h ? (w[k] & 0xffff0000u) : (w[k] << 16));
-          v[h] = (__expf(fminf(a, 0.f)) + fmaxf(a, 0.f)) * sc;
+          v[h] = (IDENT ? a : __expf(fminf(a, 0.f)) + fmaxf(a, 0.f)) * sc;
         }
         hi[k] = pack_bf16x2(v[0], v[1]);
         const float h0 = __uint_as_float(hi[k] << 16), h1 = __uint_as_float(hi[k] & 0xffff0000u);
@@ -206,7 +206,7 @@ __device__ __forceinline__ void map_boxes_split(uint8_t *box0, uint8_t *lo0, flo
   }
 }
 
-template <int D, int DV, int MODE, bool DECAY>
+template <int D, int DV, int MODE, bool DECAY, bool IDENT>
 __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_constant__ ChunkParams p) {
   using L = Lay<D, DV, MODE>;
   constexpr int S = L::kStages;
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         const int row = tp >> 3;
         float f = DECAY ? exp2f(static_cast<float>(e0 - row) * lg) : 1.f;
         if (row >= nv) f = 0.f;
-        map_boxes_split<L::KB>(st + L::kOffK, st + L::kOffKlo, f, tp);
+        map_boxes_split<L::KB, IDENT>(st + L::kOffK, st + L::kOffKlo, f, tp);
       } else {
         uint32_t sc[4];
 #pragma unroll
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
           if (t >= nv) f = 0.f;
           sc[m] = pack_bf16x2(f, f);
         }
-        map_boxes<L::KB>(st + L::kOffK, sc, tp);
+        map_boxes<L::KB, IDENT>(st + L::kOffK, sc, tp);
       }
       fence_async_smem();
       __syncwarp();
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
           if (t >= nv) f = 0.f;
           sc[m] = pack_bf16x2(f, f);
         }
-        map_boxes<L::KB>(st + L::kOffK, sc, tp);
+        map_boxes<L::KB, IDENT>(st + L::kOffK, sc, tp);
       }
       {
         // qh_t = gamma^(t - E) phi(q_t)
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
           const float f = DECAY ? exp2f(static_cast<float>(e0 + r0 + 16 * m) * lg) : 1.f;
           sc[m] = pack_bf16x2(f, f);
         }
-        map_boxes<L::KB>(st + L::kOffQ, sc, tp);
+        map_boxes<L::KB, IDENT>(st + L::kOffQ, sc, tp);
       }
       fence_async_smem();
       __syncwarp();
@@ -920,9 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int D, int DV, int MODE, bool DECAY>
+template <int D, int DV, int MODE, bool DECAY, bool IDENT>
 cudaError_t launch_typed(const ChunkParams &prm, int grid, cudaStream_t s) {
-  auto kern = chunk_tc_kernel<D, DV, MODE, DECAY>;
+  auto kern = chunk_tc_kernel<D, DV, MODE, DECAY, IDENT>;
   const int smem = Lay<D, DV, MODE>::kAlloc;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
@@ -930,19 +930,23 @@ cudaError_t launch_typed(const ChunkParams &prm, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int MODE, bool DECAY>
+template <int MODE, bool DECAY, bool IDENT>
 cudaError_t launch_dims(const ChunkParams &prm, int D, int DV, int grid, cudaStream_t s) {
   if (D == 64)
-    return DV == 64 ? launch_typed<64, 64, MODE, DECAY>(prm, grid, s)
-                    : launch_typed<64, 128, MODE, DECAY>(prm, grid, s);
-  return DV == 64 ? launch_typed<128, 64, MODE, DECAY>(prm, grid, s)
-                  : launch_typed<128, 128, MODE, DECAY>(prm, grid, s);
+    return DV == 64 ? launch_typed<64, 64, MODE, DECAY, IDENT>(prm, grid, s)
+                    : launch_typed<64, 128, MODE, DECAY, IDENT>(prm, grid, s);
+  return DV == 64 ? launch_typed<128, 64, MODE, DECAY, IDENT>(prm, grid, s)
+                  : launch_typed<128, 128, MODE, DECAY, IDENT>(prm, grid, s);
 }
 
 template <int MODE>
-cudaError_t launch_mode(const ChunkParams &prm, bool decay, int D, int DV, int grid, cudaStream_t s) {
-  return decay ? launch_dims<MODE, true>(prm, D, DV, grid, s)
-               : launch_dims<MODE, false>(prm, D, DV, grid, s);
+cudaError_t launch_mode(const ChunkParams &prm, bool decay, bool ident, int D, int DV, int grid,
+                        cudaStream_t s) {
+  if (ident)
+    return decay ? launch_dims<MODE, true, true>(prm, D, DV, grid, s)
+                 : launch_dims<MODE, false, true>(prm, D, DV, grid, s);
+  return decay ? launch_dims<MODE, true, false>(prm, D, DV, grid, s)
+               : launch_dims<MODE, false, false>(prm, D, DV, grid, s);
 }
 
 int num_sms() {
@@ -1052,7 +1056,7 @@ cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int
     cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
   }
-  return launch_mode<kCausal>(prm, p.decay, p.D, p.Dv, BH * P, s);
+  return launch_mode<kCausal>(prm, p.decay, p.ident, p.D, p.Dv, BH * P, s);
 }
 
 cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
@@ -1066,7 +1070,7 @@ cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *
   prm.P = P;
   prm.rec_parts = P;
   prm.rec = static_cast<float *>(ws);
-  cudaError_t e = launch_mode<kState>(prm, decay, D, Dv, BH * P, s);
+  cudaError_t e = launch_mode<kState>(prm, decay, false, D, Dv, BH * P, s);
   if (e != cudaSuccess) return e;
   return launch_part_scan(prm.rec, BH, H, P, N, D, Dv, prm.lg, kScanFinal, S, z, s);
 }
@@ -1084,12 +1088,12 @@ cudaError_t launch_noncausal_chunk(const Problem &p, void *ws, int Ps, int Pa, c
   prm.rec = static_cast<float *>(ws);
   prm.rec_parts = Ps;
   prm.P = Ps;
-  cudaError_t e = launch_mode<kState>(prm, false, p.D, p.Dv, BH * Ps, s);
+  cudaError_t e = launch_mode<kState>(prm, false, p.ident, p.D, p.Dv, BH * Ps, s);
   if (e == cudaSuccess)
     e = launch_part_scan(prm.rec, BH, p.H, Ps, p.N, p.D, p.Dv, prm.lg, kScanSum, nullptr, nullptr, s);
   if (e != cudaSuccess) return e;
   prm.P = Pa;
-  return launch_mode<kApply>(prm, false, p.D, p.Dv, BH * Pa, s);
+  return launch_mode<kApply>(prm, false, p.ident, p.D, p.Dv, BH * Pa, s);
 }
 
 }  // namespace linattn

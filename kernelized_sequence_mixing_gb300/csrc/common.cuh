@@ -14,6 +14,14 @@ __device__ __forceinline__ float phi_f32(float x) {
   return x > 0.f ? x + 1.f : expf(x);
 }
 
+// The feature map a kernel applies to its q, k inputs: phi, or the identity
+// when the inputs already are features.
+template <bool IDENT>
+__device__ __forceinline__ float feat_f32(float x) {
+  if constexpr (IDENT) return x;
+  else return phi_f32(x);
+}
+
 template <typename T> struct io;
 template <> struct io<float> {
   static __device__ __forceinline__ float load(const float *p) { return *p; }

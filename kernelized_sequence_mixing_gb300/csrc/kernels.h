@@ -21,6 +21,9 @@ struct Problem {
   bool decay;  // any gamma != 1
   float eps;
   Dtype dtype;
+  // q, k already are features (the Performer path computes them first): the
+  // kernels use them as they are instead of applying phi = elu + 1
+  bool ident = false;
 };
 
 // Causal forward on CUDA cores (fp32 FFMA): any dtype.
@@ -73,10 +76,11 @@ cudaError_t launch_part_scan(float *rec, int BH, int H, int P, int N, int D, int
 // directly.  Then a fixed-order reduction into S [BH][D][Dv], z [BH][D].
 int kv_state_num_splits(int BH, int N);
 size_t kv_state_workspace_bytes(int BH, int N, int D, int Dv);
+// ident: k already holds features (no phi).
 cudaError_t launch_kv_state(const void *k, const void *v, float *S, float *z,
                             float *partials, int B, int H, int N, int D,
                             int Dv, bool decay, const Gammas &g, Dtype dt,
-                            cudaStream_t s);
+                            cudaStream_t s, bool ident = false);
 
 // The same reduction (no decay) with a caller-chosen number of splits
 // (partials [nsplit][BH][D*Dv + D] in `partials` when nsplit > 1).
@@ -88,7 +92,7 @@ cudaError_t launch_kv_state_splits(const void *k, const void *v, float *S, float
 cudaError_t launch_noncausal_apply(const void *q, const float *S,
                                    const float *z, void *o, int BH, int N,
                                    int D, int Dv, float eps, Dtype dt,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool ident = false);
 
 // One decode step in place on S, z.
 cudaError_t launch_decode_step(const void *q, const void *k, const void *v,
@@ -111,5 +115,13 @@ int gla_parts(int BH, int N, int Dv);
 size_t gla_workspace_bytes(int BH, int P, int D, int Dv);
 cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, float *S_out,
                             float *z_out, cudaStream_t s);
+
+// Performer random-feature map (favor.cu): fq = phi(q), fk = phi(k) for
+// `rows` rows of q and k [rows][D], directions W [R][D], outputs [rows][R],
+// all of dtype dt; phi(x) = R^(-1/2) exp(W x - |x|^2 / 2).  D, R in {64, 128}.
+// k = nullptr: q only (fk unused).
+cudaError_t launch_favor_features(const void *q, const void *k, const void *W, void *fq,
+                                  void *fk, long long rows, int D, int R, Dtype dt,
+                                  cudaStream_t s);
 
 }  // namespace linattn

@@ -22,7 +22,7 @@ constexpr int kTok = 32;            // tokens staged per tile
 constexpr int kSplitTokens = 4096;  // tokens per split of the reduction
 
 // grid (BH, nsplit); S_out/z_out indexed by (split * BH + bh).
-template <int D, int DV, bool DECAY, typename T>
+template <int D, int DV, bool DECAY, bool IDENT, typename T>
 __global__ void __launch_bounds__(kThreads)
     kv_partial_kernel(const T *__restrict__ k, const T *__restrict__ v,
                       float *__restrict__ S_out, float *__restrict__ z_out,
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kThreads)
       const int t = i / D, d = i % D;
       float x = 0.f;
       if (t < nv) {
-        x = phi_f32(io<T>::load(kh + (int64_t)(t0 + t) * D + d));
+        x = feat_f32<IDENT>(io<T>::load(kh + (int64_t)(t0 + t) * D + d));
         if (DECAY) x *= wt[t];
       }
       fk[t][d] = x;
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kRowTile = 64;
 constexpr int kRowsPerCta = 256;
 
-template <int D, int DV, typename T>
+template <int D, int DV, bool IDENT, typename T>
 __global__ void __launch_bounds__(kThreads)
     nc_apply_kernel(const T *__restrict__ q, const float *__restrict__ S,
                     const float *__restrict__ z, T *__restrict__ o, int N,
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     for (int i = tid; i < kRowTile * D; i += kThreads) {
       const int t = i / D, d = i % D;
-      fq[t * (D + 1) + d] = t < nv ? phi_f32(io<T>::load(qh + (int64_t)(r0 + t) * D + d)) : 0.f;
+      fq[t * (D + 1) + d] = t < nv ? feat_f32<IDENT>(io<T>::load(qh + (int64_t)(r0 + t) * D + d)) : 0.f;
     }
     __syncthreads();
     float acc[RT][RE] = {};
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int D, int DV, bool DECAY, typename T>
+template <int D, int DV, bool DECAY, bool IDENT, typename T>
 cudaError_t kv_typed(const void *k, const void *v, float *S, float *z,
                      float *part, int BH, int H, int N, const Gammas &g,
                      cudaStream_t s) {
@@ -174,7 +174,7 @@ cudaError_t kv_typed(const void *k, const void *v, float *S, float *z,
   float *So = nsplit == 1 ? S : part;
   float *zo = nsplit == 1 ? z : part + (int64_t)nsplit * nS;
   dim3 grid((unsigned)BH, (unsigned)nsplit);
-  kv_partial_kernel<D, DV, DECAY, T><<<grid, kThreads, 0, s>>>(
+  kv_partial_kernel<D, DV, DECAY, IDENT, T><<<grid, kThreads, 0, s>>>(
       static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N,
       kSplitTokens, g);
   cudaError_t err = cudaGetLastError();
@@ -188,27 +188,30 @@ cudaError_t kv_typed(const void *k, const void *v, float *S, float *z,
 
 template <int D, int DV, typename T>
 cudaError_t kv_decay(const void *k, const void *v, float *S, float *z,
-                     float *part, int BH, int H, int N, bool decay,
+                     float *part, int BH, int H, int N, bool decay, bool ident,
                      const Gammas &g, cudaStream_t s) {
-  return decay ? kv_typed<D, DV, true, T>(k, v, S, z, part, BH, H, N, g, s)
-               : kv_typed<D, DV, false, T>(k, v, S, z, part, BH, H, N, g, s);
+  if (ident)
+    return decay ? kv_typed<D, DV, true, true, T>(k, v, S, z, part, BH, H, N, g, s)
+                 : kv_typed<D, DV, false, true, T>(k, v, S, z, part, BH, H, N, g, s);
+  return decay ? kv_typed<D, DV, true, false, T>(k, v, S, z, part, BH, H, N, g, s)
+               : kv_typed<D, DV, false, false, T>(k, v, S, z, part, BH, H, N, g, s);
 }
 
 template <typename T>
 cudaError_t kv_shape(const void *k, const void *v, float *S, float *z,
                      float *part, int BH, int H, int N, int D, int Dv,
-                     bool decay, const Gammas &g, cudaStream_t s) {
-  if (D == 64 && Dv == 64) return kv_decay<64, 64, T>(k, v, S, z, part, BH, H, N, decay, g, s);
-  if (D == 64 && Dv == 128) return kv_decay<64, 128, T>(k, v, S, z, part, BH, H, N, decay, g, s);
-  if (D == 128 && Dv == 64) return kv_decay<128, 64, T>(k, v, S, z, part, BH, H, N, decay, g, s);
-  if (D == 128 && Dv == 128) return kv_decay<128, 128, T>(k, v, S, z, part, BH, H, N, decay, g, s);
+                     bool decay, bool ident, const Gammas &g, cudaStream_t s) {
+  if (D == 64 && Dv == 64) return kv_decay<64, 64, T>(k, v, S, z, part, BH, H, N, decay, ident, g, s);
+  if (D == 64 && Dv == 128) return kv_decay<64, 128, T>(k, v, S, z, part, BH, H, N, decay, ident, g, s);
+  if (D == 128 && Dv == 64) return kv_decay<128, 64, T>(k, v, S, z, part, BH, H, N, decay, ident, g, s);
+  if (D == 128 && Dv == 128) return kv_decay<128, 128, T>(k, v, S, z, part, BH, H, N, decay, ident, g, s);
   return cudaErrorNotSupported;
 }
 
-template <int D, int DV, typename T>
+template <int D, int DV, bool IDENT, typename T>
 cudaError_t apply_typed(const void *q, const float *S, const float *z, void *o,
                         int BH, int N, float eps, cudaStream_t s) {
-  auto kern = nc_apply_kernel<D, DV, T>;
+  auto kern = nc_apply_kernel<D, DV, IDENT, T>;
   const size_t smem = sizeof(float) * ((size_t)D * DV + D + kRowTile * (D + 1));
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -219,14 +222,14 @@ cudaError_t apply_typed(const void *q, const float *S, const float *z, void *o,
   return cudaGetLastError();
 }
 
-template <typename T>
+template <bool IDENT, typename T>
 cudaError_t apply_shape(const void *q, const float *S, const float *z, void *o,
                         int BH, int N, int D, int Dv, float eps,
                         cudaStream_t s) {
-  if (D == 64 && Dv == 64) return apply_typed<64, 64, T>(q, S, z, o, BH, N, eps, s);
-  if (D == 64 && Dv == 128) return apply_typed<64, 128, T>(q, S, z, o, BH, N, eps, s);
-  if (D == 128 && Dv == 64) return apply_typed<128, 64, T>(q, S, z, o, BH, N, eps, s);
-  if (D == 128 && Dv == 128) return apply_typed<128, 128, T>(q, S, z, o, BH, N, eps, s);
+  if (D == 64 && Dv == 64) return apply_typed<64, 64, IDENT, T>(q, S, z, o, BH, N, eps, s);
+  if (D == 64 && Dv == 128) return apply_typed<64, 128, IDENT, T>(q, S, z, o, BH, N, eps, s);
+  if (D == 128 && Dv == 64) return apply_typed<128, 64, IDENT, T>(q, S, z, o, BH, N, eps, s);
+  if (D == 128 && Dv == 128) return apply_typed<128, 128, IDENT, T>(q, S, z, o, BH, N, eps, s);
   return cudaErrorNotSupported;
 }
 
@@ -238,7 +241,7 @@ cudaError_t kv_typed_n(const void *k, const void *v, float *S, float *z, float *
   float *So = nsplit == 1 ? S : part;
   float *zo = nsplit == 1 ? z : part + (int64_t)nsplit * nS;
   dim3 grid((unsigned)BH, (unsigned)nsplit);
-  kv_partial_kernel<D, DV, DECAY, T><<<grid, kThreads, 0, s>>>(
+  kv_partial_kernel<D, DV, DECAY, false, T><<<grid, kThreads, 0, s>>>(
       static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N, split_len, g);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || nsplit == 1) return err;
@@ -287,20 +290,23 @@ size_t kv_state_workspace_bytes(int BH, int N, int D, int Dv) {
 cudaError_t launch_kv_state(const void *k, const void *v, float *S, float *z,
                             float *partials, int B, int H, int N, int D,
                             int Dv, bool decay, const Gammas &g, Dtype dt,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool ident) {
   const int BH = B * H;
   return dt == kF32
-             ? kv_shape<float>(k, v, S, z, partials, BH, H, N, D, Dv, decay, g, s)
-             : kv_shape<__nv_bfloat16>(k, v, S, z, partials, BH, H, N, D, Dv, decay, g, s);
+             ? kv_shape<float>(k, v, S, z, partials, BH, H, N, D, Dv, decay, ident, g, s)
+             : kv_shape<__nv_bfloat16>(k, v, S, z, partials, BH, H, N, D, Dv, decay, ident, g, s);
 }
 
 cudaError_t launch_noncausal_apply(const void *q, const float *S,
                                    const float *z, void *o, int BH, int N,
                                    int D, int Dv, float eps, Dtype dt,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, bool ident) {
+  if (ident)
+    return dt == kF32 ? apply_shape<true, float>(q, S, z, o, BH, N, D, Dv, eps, s)
+                      : apply_shape<true, __nv_bfloat16>(q, S, z, o, BH, N, D, Dv, eps, s);
   return dt == kF32
-             ? apply_shape<float>(q, S, z, o, BH, N, D, Dv, eps, s)
-             : apply_shape<__nv_bfloat16>(q, S, z, o, BH, N, D, Dv, eps, s);
+             ? apply_shape<false, float>(q, S, z, o, BH, N, D, Dv, eps, s)
+             : apply_shape<false, __nv_bfloat16>(q, S, z, o, BH, N, D, Dv, eps, s);
 }
 
 }  // namespace linattn

@@ -58,6 +58,8 @@ la_status_t from_cuda(cudaError_t e) {
   return LA_ERR_CUDA;
 }
 
+la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStream_t s);
+
 }  // namespace
 
 extern "C" {
@@ -118,10 +120,24 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
   if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv))
     return LA_ERR_INVALID_ARG;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   Problem p{q, k, v, o, B, H, N, D, Dv, decay, eps,
             dtype == LA_F32 ? kF32 : kBF16};
-  const int BH = B * H;
+  return run_forward(p, g, causal, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The forward pass of a validated problem: picks the kernel, takes and
+// returns the stream-ordered workspace.  p.ident: q, k already are features.
+la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStream_t s) {
+  const int BH = p.B * p.H;
+  const int N = p.N, D = p.D, Dv = p.Dv;
+  const void *k = p.k, *v = p.v, *q = p.q;
+  void *o = p.o;
+  const float eps = p.eps;
+  const int B = p.B, H = p.H;
   if (causal) {
     if (chunk128_supported(p, g)) {
       // 128-token chunks (D = Dv = 128); parts as below
@@ -168,13 +184,17 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
   float *S = static_cast<float *>(ws);
   float *z = S + (size_t)BH * D * Dv;
   float *part = part_bytes ? z + (size_t)BH * D : nullptr;
-  e = launch_kv_state(k, v, S, z, part, B, H, N, D, Dv, false, g, p.dtype, s);
+  e = launch_kv_state(k, v, S, z, part, B, H, N, D, Dv, false, g, p.dtype, s, p.ident);
   if (e == cudaSuccess)
-    e = launch_noncausal_apply(q, S, z, o, BH, N, D, Dv, eps, p.dtype, s);
+    e = launch_noncausal_apply(q, S, z, o, BH, N, D, Dv, eps, p.dtype, s, p.ident);
   cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(ef);
 }
+
+}  // namespace
+
+extern "C" {
 
 la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
                              int B, int H, int N, int D, int Dv,
@@ -370,6 +390,62 @@ la_status_t la_decode_gated(const void *q, const void *k, const void *v, const f
   return from_cuda(launch_decode_gated(q, k, v, a, S, z, o, B, H, D, Dv, eps,
                                        dtype == LA_F32 ? kF32 : kBF16,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+la_status_t la_favor_features(const void *x, const void *W, void *phi, int rows, int D,
+                              int r, la_dtype_t dtype, void *stream) {
+  if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+  if (rows < 0 || D <= 0 || r <= 0) return LA_ERR_INVALID_ARG;
+  if (!supported_dim(D) || !supported_dim(r)) return LA_ERR_UNSUPPORTED;
+  if (rows == 0) return LA_OK;
+  if (!x || !W || !phi || !aligned16(x) || !aligned16(W) || !aligned16(phi))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nx = (size_t)rows * D * es, nW = (size_t)r * D * es, nf = (size_t)rows * r * es;
+  if (overlaps(phi, nf, x, nx) || overlaps(phi, nf, W, nW)) return LA_ERR_INVALID_ARG;
+  return from_cuda(launch_favor_features(x, nullptr, W, phi, nullptr, rows, D, r,
+                                         dtype == LA_F32 ? kF32 : kBF16,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+la_status_t la_forward_favor(const void *q, const void *k, const void *v, const void *W, void *o,
+                             int B, int H, int N, int D, int Dv, int r, int causal,
+                             const float *gamma, float eps, la_dtype_t dtype, void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (r <= 0) return LA_ERR_INVALID_ARG;
+  if (!supported_dim(r)) return LA_ERR_UNSUPPORTED;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  if (!causal && decay) return LA_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)B * H * N;
+  if (rows == 0) return LA_OK;
+  if (!q || !k || !v || !W || !o) return LA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(W) || !aligned16(o))
+    return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)rows * D * es, nv = (size_t)rows * Dv * es, nW = (size_t)r * D * es;
+  if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv) ||
+      overlaps(o, nv, W, nW))
+    return LA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dtype dt = dtype == LA_F32 ? kF32 : kBF16;
+  // the features of q and k, [B][H][N][r] each, in a stream-ordered workspace
+  const size_t nf = (((size_t)rows * r * es) + 255) & ~(size_t)255;
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, 2 * nf, s) != cudaSuccess) return LA_ERR_CUDA;
+  void *fq = ws, *fk = static_cast<uint8_t *>(ws) + nf;
+  la_status_t out = from_cuda(launch_favor_features(q, k, W, fq, fk, rows, D, r, dt, s));
+  if (out == LA_OK) {
+    Problem p{fq, fk, v, o, B, H, N, r, Dv, decay, eps, dt};
+    p.ident = true;
+    out = run_forward(p, g, causal, s);
+  }
+  const cudaError_t ef = cudaFreeAsync(ws, s);
+  if (out != LA_OK) return out;
+  return from_cuda(ef);
 }
 
 }  // extern "C"

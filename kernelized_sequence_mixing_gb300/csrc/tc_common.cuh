@@ -325,6 +325,19 @@ __device__ __forceinline__ uint32_t phi_scale_bf16x2(uint32_t w, uint32_t scale2
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// phi (IDENT = false) or the identity (inputs already features), times the
+// per-row scale, on a pair of bf16 values.
+template <bool IDENT>
+__device__ __forceinline__ uint32_t feat_scale_bf16x2(uint32_t w, uint32_t scale2) {
+  if constexpr (IDENT) {
+    const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&w),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&scale2));
+    return *reinterpret_cast<const uint32_t *>(&r);
+  } else {
+    return phi_scale_bf16x2(w, scale2);
+  }
+}
+
 // ---- swizzled shared-memory addressing ---------------------------------------
 // Byte offset of (row, byte-in-row) in a tile of 128-byte rows with the
 // 128-byte swizzle (16-byte chunk index XOR row % 8); tile 1024-byte aligned.

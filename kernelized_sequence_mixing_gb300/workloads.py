@@ -38,6 +38,9 @@ class Workload:
     # gated workloads: fp32 gates a [B, H, N, D] uniform in [gate_lo, 1)
     gated: bool = False
     gate_lo: float = 0.9
+    # Performer workloads: r random features from block-orthogonal
+    # directions drawn with seed + 2
+    favor_r: int = 0
 
     @property
     def tokens(self) -> int:
@@ -79,6 +82,11 @@ WORKLOADS = {
     # D=Dv=128, gates U[0.9, 1) from seed 5 + 1
     "gla_bf16_n16384": Workload("gla_bf16_n16384", True, 2, 16, 16384, 128,
                                 128, torch.bfloat16, 0.5, 5, gated=True),
+    # Performer (FAVOR+) causal, bf16, B2 H16 N16384 D=Dv=128, r = 128
+    # block-orthogonal features; q, k ~ N(0, 1) * D^(-1/4) (the usual
+    # softmax temperature folded into the inputs)
+    "favor_bf16_n16384": Workload("favor_bf16_n16384", True, 2, 16, 16384, 128,
+                                  128, torch.bfloat16, 128 ** -0.25, 6, favor_r=128),
     "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
                                 128, torch.bfloat16, 0.5, 4, steps=1024,
                                 step_seed0=1000),
@@ -160,3 +168,8 @@ def favor_matrix(r, D, seed=0, orthogonal=True, dtype=torch.float32, device="cpu
         norms = torch.randn((r, D), generator=g, dtype=torch.float64).norm(dim=1)
         W = W * norms[:, None]
     return W.to(dtype).to(device)
+
+
+def workload_favor_matrix(w: Workload, device="cpu"):
+    """The block-orthogonal directions [r, D] of a Performer workload."""
+    return favor_matrix(w.favor_r, w.D, w.seed + 2, True, w.dtype, device)

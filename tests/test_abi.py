@@ -35,7 +35,7 @@ def declared_symbols():
 def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
-              "la_forward_gated", "la_decode_gated",
+              "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -187,6 +187,35 @@ def test_decode_gated_rejects_bad_arguments(lib):
     assert call(eps=-1.0) == INVALID
     assert call(Dv=32) == UNSUPPORTED
     assert call(B=0, p=[None] * 7) == OK
+
+
+def test_favor_rejects_bad_arguments(lib):
+    Ff = lib.la_favor_features
+    Ff.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    x, W, f = A, A + STEP, A + 2 * STEP
+    assert Ff(x, W, None, 100, 128, 128, BF16, None) == INVALID
+    assert Ff(x, W, x + 256, 100, 128, 128, BF16, None) == INVALID   # phi overlaps x
+    assert Ff(x, W + 8, f, 100, 128, 128, BF16, None) == INVALID     # misaligned W
+    assert Ff(x, W, f, 100, 96, 128, BF16, None) == UNSUPPORTED
+    assert Ff(x, W, f, 100, 128, 32, BF16, None) == UNSUPPORTED
+    assert Ff(x, W, f, -1, 128, 128, BF16, None) == INVALID
+    assert Ff(None, None, None, 0, 128, 128, BF16, None) == OK
+    Fw = lib.la_forward_favor
+    Fw.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_float,
+                                                                ctypes.c_int, ctypes.c_void_p]
+    q, k, v, Wd, o = (A + i * STEP for i in range(5))
+
+    def call(qq=q, kk=k, vv=v, WW=Wd, oo=o, B=1, H=2, N=8, D=128, Dv=128, r=128, causal=1,
+             g=None, eps=1e-6, dt=BF16):
+        return Fw(qq, kk, vv, WW, oo, B, H, N, D, Dv, r, causal, g, eps, dt, None)
+
+    assert call(WW=None) == INVALID
+    assert call(oo=Wd) == INVALID               # o aliases W
+    assert call(r=100) == UNSUPPORTED
+    assert call(r=0) == INVALID
+    assert call(causal=0, g=(ctypes.c_float * 2)(0.5, 1.0)) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(B=0, qq=None, kk=None, vv=None, WW=None, oo=None) == OK
 
 
 def test_causal_kernel_dispatch(lib):
