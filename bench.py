@@ -39,6 +39,7 @@ METRICS = {
     "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
     "gated": "gated linear-attn fwd tokens/s and % fp32 ALU roofline, 1×GB300",
     "favor": "Performer (FAVOR+) causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
+    "backward": "causal linear-attn bwd (dq, dk, dv) tokens/s and % fp32 ALU roofline, 1×GB300",
 }
 
 
@@ -49,6 +50,8 @@ def workload_metric(w):
         return METRICS["gated"]
     if w.favor_r:
         return METRICS["favor"]
+    if w.backward:
+        return METRICS["backward"]
     return METRIC if w.causal else METRICS["noncausal"]
 DEFAULT_WORKLOAD = "causal_decay_bf16_n16384"
 FALLBACK_HBM_GBS = 6800.0  # profiling recipe fallback, used only if absent
@@ -62,9 +65,9 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 # ncu capture, keyed by workload, with the hash of the kernel source the
 # capture was taken on; reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/chunk128_causal_decay_bf16_n16384.md: 582.895872 MB read +
-    # 113.363712 MB written in one launch of the full workload
-    "causal_decay_bf16_n16384": {"bytes": 696259584, "source": "a75b560b07b7b88c"},
+    # profiles/chunk128_causal_decay_bf16_n16384.md: 583.994624 MB read +
+    # 113.507584 MB written in one launch of the full workload
+    "causal_decay_bf16_n16384": {"bytes": 697502208, "source": "5a8f3373f880ae5b"},
 }
 
 
@@ -135,6 +138,12 @@ def algorithmic_work(w):
         r = w.favor_r
         byts += r * w.D * es
         flops = units * (2 * (2 * w.D * r + 2 * w.D + r) + 4 * r * w.Dv + 3 * r + w.Dv)
+    if w.backward:
+        # read q, k, v, dL/do, write dq, dk, dv; recurrent-form flops: the
+        # forward (4 D Dv) plus dphi(q) = S gt - c z, the reverse state
+        # U = sum phi(q) gt^T, dv = U^T phi(k), dphi(k) = U v - u (2 D Dv each)
+        byts = units * (4 * w.D + 3 * w.Dv) * es
+        flops = units * (12 * w.D * w.Dv + 10 * w.D + 4 * w.Dv)
     return byts, flops
 
 
@@ -154,6 +163,8 @@ KERNEL_SOURCES = ("chunk128.cu", "chunk_tc.cu", "tc_common.cuh", "common.cuh")
 GATED_SOURCES = ("gla_simt.cu", "common.cuh")
 # sources of the Performer path (feature kernel, then the causal kernel)
 FAVOR_SOURCES = ("favor.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
+# sources of the backward pass
+BACKWARD_SOURCES = ("backward_simt.cu", "common.cuh")
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES):
@@ -241,6 +252,9 @@ def oracle_sample(w, heads_per_pass):
     if w.favor_r:  # the random directions in place of per-head decays
         from kernelized_sequence_mixing_gb300.workloads import workload_favor_matrix
         return f(q), f(k), f(v), workload_favor_matrix(w).float().numpy()
+    if w.backward:  # the upstream gradient in place of per-head decays
+        from kernelized_sequence_mixing_gb300.workloads import workload_upstream
+        return f(q), f(k), f(v), f(workload_upstream(w))
     g = w.gamma()
     gu = None
     if g is not None:
@@ -260,6 +274,10 @@ def time_oracle(w, heads_per_pass, passes):
         elif w.favor_r:
             from oracle import favor as fv
             fv.favor(qs, ks, vs, gu, causal=True, eps=w.eps)
+        elif w.backward:
+            from oracle import backward as bw
+            for u in range(qs.shape[0]):
+                bw.causal_backward(qs[u], ks[u], vs[u], gu[u], None, w.eps)
         elif w.causal:
             oracle.causal(qs, ks, vs, gamma=gu, eps=w.eps, nthreads=threads)
         else:
@@ -337,6 +355,8 @@ def workload_config(w):
     if w.gated:
         cfg["gates"] = (f"fp32 a [B][H][N][D] uniform in [{w.gate_lo}, 1), one per key "
                         "feature and token")
+    if w.backward:
+        cfg["pass"] = "backward: dq, dk, dv from q, k, v and dL/do ~ N(0, 1)"
     if w.favor_r:
         cfg["features"] = (f"Performer, r = {w.favor_r} block-orthogonal directions; q, k "
                            f"~ N(0, 1) * {w.scale:.4f} (D^-1/4)")
@@ -358,7 +378,7 @@ def run_ours(args, w):
 
     ws, rank, local = dist_env()
     final_state = bool(getattr(args, "final_state", False))
-    if final_state and (w.steps or not w.causal or w.gated or w.favor_r):
+    if final_state and (w.steps or not w.causal or w.gated or w.favor_r or w.backward):
         raise SystemExit("--final-state applies to the causal forward workloads")
     if ws > 1:
         import torch.distributed as dist
@@ -422,6 +442,37 @@ def run_ours(args, w):
             ad.copy_(ah, non_blocking=True)
             step()
             oh.copy_(od, non_blocking=True)
+        tokens_rank = w.B * w.N
+    elif w.backward:
+        # backward: operand preparation, four chunked causal products (the
+        # forward's n and d, dphi(q), dv, dphi(k)), the middle and final
+        # elementwise kernels
+        from kernelized_sequence_mixing_gb300.workloads import workload_upstream
+        q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
+        do = workload_upstream(w)
+        qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+        grads = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
+        od = grads[2]
+        ncopy = 1
+        launches_per_step = 7
+
+        def step():
+            la.backward(qd, kd, vd, dod, eps=w.eps, dq=grads[0], dk=grads[1], dv=grads[2])
+
+        grads_host = []
+
+        def e2e_step(qh, kh, vh, oh, doh=None):
+            # all three gradients come back to pinned host memory
+            if not grads_host:
+                grads_host.extend(torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                                  for t in grads)
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            dod.copy_(doh, non_blocking=True)
+            step()
+            for hst, dvc in zip(grads_host, grads):
+                hst.copy_(dvc, non_blocking=True)
         tokens_rank = w.B * w.N
     elif w.favor_r:
         # Performer: the feature kernel (q and k in one launch), then the
@@ -530,7 +581,8 @@ def run_ours(args, w):
     if not args.quick:
         qh, kh, vh = (t.pin_memory() for t in (q, k, v))
         oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-        extra = {"ah": a.pin_memory()} if w.gated else {}
+        extra = ({"ah": a.pin_memory()} if w.gated else
+                 {"doh": do.pin_memory()} if w.backward else {})
         e2e_step(qh, kh, vh, oh, **extra)
         torch.cuda.synchronize(dev)
         e2e_steps = max(1, min(args.steps, 10))
@@ -541,8 +593,9 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         e2e_s = reduce_max((time.perf_counter() - t0) / e2e_steps, ws)
     es = q.element_size()
-    h2d = (q.numel() + k.numel() + v.numel()) * es + (a.numel() * 4 if w.gated else 0)
-    d2h = od.numel() * es
+    h2d = (q.numel() + k.numel() + v.numel()) * es + (a.numel() * 4 if w.gated else 0) + (
+        do.numel() * es if w.backward else 0)
+    d2h = (sum(t.numel() for t in grads) if w.backward else od.numel()) * es
 
     if rank != 0:
         return 0
@@ -554,7 +607,8 @@ def run_ours(args, w):
     launch_ms = statistics.mean(per_launch)  # the whole step's launches
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
     src_hash = kernel_source_hash(GATED_SOURCES if w.gated else
-                                  FAVOR_SOURCES if w.favor_r else KERNEL_SOURCES)
+                                  FAVOR_SOURCES if w.favor_r else
+                                  BACKWARD_SOURCES if w.backward else KERNEL_SOURCES)
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes"] if tr and tr.get("source") == src_hash and not final_state else None
 
@@ -569,7 +623,8 @@ def run_ours(args, w):
             sample = (f"{heads} of {w.B * w.H} (sequence, head) units, one decode "
                       f"step, best of 3 ({t:.2f} s wall)")
         else:
-            heads = min(w.B * w.H, 32)
+            # the quadratic gradient oracle is O(N^2) per unit: 4 units
+            heads = min(w.B * w.H, 4 if w.backward else 32)
             tokens, times, threads = time_oracle(w, heads, 1)
             t = times[0]
             sample = (f"{heads} of {w.B * w.H} (b,h) units, all {w.N} "
@@ -614,7 +669,7 @@ def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traff
     tflops = flops / (launch_ms / 1e3) / 1e12
     hbm_src = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                else "fallback")
-    if w.gated:
+    if w.gated or w.backward:
         return {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
                 "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",

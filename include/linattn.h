@@ -217,6 +217,30 @@ LA_API la_status_t la_forward_favor(const void *q, const void *k, const void *v,
                                     la_dtype_t dtype, void *stream);
 
 /*
+ * Backward pass of the causal form (with the per-head decay): given the
+ * upstream gradient dO = dL/do of o = la_forward(q, k, v, causal = 1, gamma,
+ * eps), writes dq = dL/dq, dk = dL/dk, dv = dL/dv.  With
+ * w_ij = gamma^(i-j) phi(q_i).phi(k_j) (j <= i), d_i = sum_j w_ij + eps,
+ * gt_i = dO_i / d_i and c_i = gt_i . o_i, the chain rule through
+ * o_i = sum_j w_ij v_j / d_i gives dL/dw_ij = gt_i . v_j - c_i, and
+ *   dv_j = sum_(i>=j) w_ij gt_i,
+ *   dq_i = phi'(q_i) * sum_(j<=i) gamma^(i-j) (dL/dw_ij) phi(k_j),
+ *   dk_j = phi'(k_j) * sum_(i>=j) gamma^(i-j) (dL/dw_ij) phi(q_i),
+ * phi'(x) = 1 for x > 0, exp(x) otherwise.  The "parallel training" half
+ * of the duality on "Linear Attention Mechanisms" (dileepadev.github.io),
+ * "Recurrent Reformulation"; the forward it differentiates is la_forward's.
+ * The library recomputes o and d itself (the caller keeps no forward
+ * state).  q, k, dq, dk: [B][H][N][D]; v, dO, dv: [B][H][N][Dv]; all of
+ * `dtype`; fp32 arithmetic on CUDA cores in a stream-ordered workspace of
+ * B*H*N*(4D + 6Dv + 16)*4 bytes (cudaMallocAsync on `stream`).  No gradient
+ * may overlap an input or another gradient.  Errors as la_forward.
+ */
+LA_API la_status_t la_backward(const void *q, const void *k, const void *v, const void *dO,
+                               void *dq, void *dk, void *dv, int B, int H, int N, int D,
+                               int Dv, const float *gamma, float eps, la_dtype_t dtype,
+                               void *stream);
+
+/*
  * Which kernel la_forward would run for a causal call with these arguments:
  * 2 = the tcgen05 tensor-core kernel with 128-token chunks (bf16,
  * D = Dv = 128, every gamma >= 0.61), 1 = the tcgen05 tensor-core kernel with

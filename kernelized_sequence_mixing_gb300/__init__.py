@@ -16,6 +16,7 @@ Functions (same names as the C entry points, minus the ``la_`` prefix):
   decode_gated(q, k, v, a, S, z, eps=1e-6, out=None)
   favor_features(x, W, out=None)
   forward_favor(q, k, v, W, causal=True, gamma=None, eps=1e-6, out=None)
+  backward(q, k, v, do, gamma=None, eps=1e-6)
 """
 from __future__ import annotations
 
@@ -28,7 +29,7 @@ import torch
 from . import workloads  # noqa: F401  (seeded input generators)
 
 __all__ = ["forward", "prefill_state", "decode_step", "forward_state",
-           "forward_gated", "decode_gated", "favor_features", "forward_favor",
+           "forward_gated", "decode_gated", "favor_features", "forward_favor", "backward",
            "status_string",
            "device_wait_timeouts", "causal_kernel",
            "load_library", "library_path", "LinAttnError", "workloads"]
@@ -85,6 +86,8 @@ def load_library() -> ctypes.CDLL:
             lib.la_forward_favor.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, FP, F,
                                              I, P]
             lib.la_forward_favor.restype = I
+            lib.la_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, FP, F, I, P]
+            lib.la_backward.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
             lib.la_device_wait_timeouts.argtypes = [I]
@@ -381,3 +384,29 @@ def forward_favor(q, k, v, W, causal=True, gamma=None, eps=1e-6, out=None):
             1 if causal else 0, _gamma_arg(gamma, H), float(eps), _dtype_code(q),
             _stream(dev)))
     return out
+
+
+def backward(q, k, v, do, gamma=None, eps=1e-6, dq=None, dk=None, dv=None):
+    """Gradients (dq, dk, dv) of the causal forward o = forward(q, k, v,
+    causal=True, gamma, eps) for the upstream gradient do = dL/do.  q, k:
+    [B, H, N, D]; v, do: [B, H, N, Dv]; CUDA tensors of one dtype."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or do.shape != v.shape:
+        raise ValueError("expected q, k: [B, H, N, D] and v, do: [B, H, N, Dv]")
+    if not (q.dtype == k.dtype == v.dtype == do.dtype):
+        raise TypeError("q, k, v and do must share one dtype")
+    B, H, N, D = q.shape
+    Dv = v.shape[-1]
+    dev = q.device
+    with torch.cuda.device(dev):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            _contig(n, t)
+        _check("la_backward", lib.la_backward(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, D, Dv,
+            _gamma_arg(gamma, H), float(eps), _dtype_code(q), _stream(dev)))
+    return dq, dk, dv

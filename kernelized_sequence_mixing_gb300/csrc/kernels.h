@@ -124,4 +124,11 @@ cudaError_t launch_favor_features(const void *q, const void *k, const void *W, v
                                   void *fk, long long rows, int D, int R, Dtype dt,
                                   cudaStream_t s);
 
+// Backward of the causal form (backward_simt.cu): dq, dk, dv (dtype of p)
+// from q, k, v of p and the upstream gradient dO [B*H][N][Dv]; fp32 on CUDA
+// cores in a workspace of backward_workspace_bytes().
+size_t backward_workspace_bytes(int BH, int N, int D, int Dv);
+cudaError_t launch_backward(const Problem &p, const void *dO, void *dq, void *dk, void *dv,
+                            const Gammas &g, void *ws, cudaStream_t s);
+
 }  // namespace linattn

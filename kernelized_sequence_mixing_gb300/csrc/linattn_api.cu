@@ -448,4 +448,43 @@ la_status_t la_forward_favor(const void *q, const void *k, const void *v, const 
   return from_cuda(ef);
 }
 
+la_status_t la_backward(const void *q, const void *k, const void *v, const void *dO, void *dq,
+                        void *dk, void *dv, int B, int H, int N, int D, int Dv,
+                        const float *gamma, float eps, la_dtype_t dtype, void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  const int64_t rows = (int64_t)B * H * N;
+  if (rows == 0) return LA_OK;
+  const void *ins[4] = {q, k, v, dO};
+  void *outs[3] = {dq, dk, dv};
+  for (const void *x : ins)
+    if (!x || !aligned16(x)) return LA_ERR_INVALID_ARG;
+  for (void *x : outs)
+    if (!x || !aligned16(x)) return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)rows * D * es, nv = (size_t)rows * Dv * es;
+  const size_t insz[4] = {nqk, nqk, nv, nv};
+  const size_t outsz[3] = {nqk, nqk, nv};
+  // the gradients may overlap no input and no other gradient
+  for (int w = 0; w < 3; ++w) {
+    for (int i = 0; i < 4; ++i)
+      if (overlaps(outs[w], outsz[w], ins[i], insz[i])) return LA_ERR_INVALID_ARG;
+    for (int u = w + 1; u < 3; ++u)
+      if (overlaps(outs[w], outsz[w], outs[u], outsz[u])) return LA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Problem p{q, k, v, nullptr, B, H, N, D, Dv, decay, eps, dtype == LA_F32 ? kF32 : kBF16};
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, backward_workspace_bytes(B * H, N, D, Dv), s) != cudaSuccess)
+    return LA_ERR_CUDA;
+  const cudaError_t e = launch_backward(p, dO, dq, dk, dv, g, ws, s);
+  const cudaError_t ef = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(ef);
+}
+
 }  // extern "C"

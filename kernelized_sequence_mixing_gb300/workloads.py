@@ -41,6 +41,9 @@ class Workload:
     # Performer workloads: r random features from block-orthogonal
     # directions drawn with seed + 2
     favor_r: int = 0
+    # backward workloads: one la_backward over the causal form, with an
+    # upstream gradient dL/do ~ N(0, 1) drawn with seed + 3
+    backward: bool = False
 
     @property
     def tokens(self) -> int:
@@ -87,6 +90,10 @@ WORKLOADS = {
     # softmax temperature folded into the inputs)
     "favor_bf16_n16384": Workload("favor_bf16_n16384", True, 2, 16, 16384, 128,
                                   128, torch.bfloat16, 128 ** -0.25, 6, favor_r=128),
+    # backward of the causal form, bf16, B4 H8 N4096 D=Dv=64 (the training
+    # shape of the causal configurations), gamma = 1
+    "backward_bf16_n4096": Workload("backward_bf16_n4096", True, 4, 8, 4096, 64, 64,
+                                    torch.bfloat16, 0.5, 7, backward=True),
     "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
                                 128, torch.bfloat16, 0.5, 4, steps=1024,
                                 step_seed0=1000),
@@ -173,3 +180,11 @@ def favor_matrix(r, D, seed=0, orthogonal=True, dtype=torch.float32, device="cpu
 def workload_favor_matrix(w: Workload, device="cpu"):
     """The block-orthogonal directions [r, D] of a Performer workload."""
     return favor_matrix(w.favor_r, w.D, w.seed + 2, True, w.dtype, device)
+
+
+def workload_upstream(w: Workload, device="cpu"):
+    """The upstream gradient dL/do [B, H, N, Dv] of a backward workload:
+    N(0, 1) from seed + 3, rounded once to the workload dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed + 3))
+    return torch.randn((w.B, w.H, w.N, w.Dv), generator=g).to(w.dtype).to(device)

@@ -36,6 +36,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
+              "la_backward",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -216,6 +217,25 @@ def test_favor_rejects_bad_arguments(lib):
     assert call(causal=0, g=(ctypes.c_float * 2)(0.5, 1.0)) == INVALID
     assert call(eps=-1.0) == INVALID
     assert call(B=0, qq=None, kk=None, vv=None, WW=None, oo=None) == OK
+
+
+def test_backward_rejects_bad_arguments(lib):
+    Fb = lib.la_backward
+    Fb.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_float,
+                                                                ctypes.c_int, ctypes.c_void_p]
+    q, k, v, do, dq, dk, dv = (A + i * STEP for i in range(7))
+
+    def call(p=(q, k, v, do, dq, dk, dv), B=1, H=2, N=8, D=64, Dv=64, g=None, eps=1e-6, dt=F32):
+        return Fb(*p, B, H, N, D, Dv, g, eps, dt, None)
+
+    assert call(p=(q, k, v, None, dq, dk, dv)) == INVALID      # no upstream gradient
+    assert call(p=(q, k, v, do, q, dk, dv)) == INVALID         # dq aliases q
+    assert call(p=(q, k, v, do, dq, dq + 64, dv)) == INVALID   # dk inside dq
+    assert call(p=(q, k, v, do + 4, dq, dk, dv)) == INVALID    # misaligned
+    assert call(eps=-1.0) == INVALID
+    assert call(g=(ctypes.c_float * 2)(0.5, 2.0)) == INVALID
+    assert call(D=32) == UNSUPPORTED
+    assert call(B=0, p=(None,) * 7) == OK
 
 
 def test_causal_kernel_dispatch(lib):

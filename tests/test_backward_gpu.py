@@ -1,0 +1,138 @@
+"""GPU parity of the backward pass against the fp64 gradient oracle
+(oracle/backward.py), on seeded inputs and upstream gradients.
+
+Errors are normwise per (batch, head) unit and tensor, measured against the
+larger of the gradient's own size and the size of the terms summed into it:
+max |x - r| / max(max |r|, max T), where T is the same sum over the absolute
+values of its terms.  The rounding error of an fp32 sum is bounded by the
+unit roundoff times the sum of |terms|, and a gradient can be a near-total
+cancellation of large terms (dq of a single token: the output depends on q
+only through eps, so gt . v - c is almost exactly 0), so the error bound
+scales with T, not with the result.  fp32 inputs: 2e-4; bf16 inputs: 1e-2
+(the inputs are widened exactly, the arithmetic is fp32 and the gradients
+are rounded once to bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import to_np
+
+pytestmark = pytest.mark.gpu
+
+BWD_TOL = {torch.float32: 2e-4, torch.bfloat16: 1e-2}
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kernelized_sequence_mixing_gb300 import build
+    build.build()
+    import kernelized_sequence_mixing_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def bw():
+    from oracle import backward
+    return backward
+
+
+def unit_err(x, r, scale=None):
+    x = np.asarray(x, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    ax = (-2, -1)
+    den = np.abs(r).max(axis=ax)
+    if scale is not None:
+        den = np.maximum(den, np.asarray(scale, dtype=np.float64).max(axis=ax))
+    return float((np.abs(x - r).max(axis=ax) / np.maximum(den, 1e-30)).max())
+
+
+def term_sizes(q, k, v, do, gamma, eps):
+    """Per unit, the gradients' sums taken over absolute values of their
+    terms (|dL/dw_ij| <= |gt_i| . |v_j| + |c_i|): the scale of their fp32
+    rounding error.  q, k [N, D]; v, do [N, Dv]; fp64."""
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    fq = np.where(q > 0, q + 1, np.exp(np.minimum(q, 0)))
+    fk = np.where(k > 0, k + 1, np.exp(np.minimum(k, 0)))
+    N = q.shape[0]
+    i, j = np.arange(N)[:, None], np.arange(N)[None, :]
+    g = 1.0 if gamma is None else float(np.float32(gamma))
+    G = np.where(j <= i, np.power(g, np.where(j <= i, i - j, 0).astype(np.float64)), 0.0)
+    Wm = (fq @ fk.T) * G
+    d = Wm.sum(1) + eps
+    o = (Wm @ v) / d[:, None]
+    gt = do / d[:, None]
+    c = np.abs(np.sum(gt * o, axis=1))
+    T = (np.abs(gt) @ np.abs(v).T + c[:, None]) * G
+    return (T @ fk) * np.minimum(fq, 1), (T.T @ fq) * np.minimum(fk, 1), Wm.T @ np.abs(gt)
+
+
+def inputs(B, H, N, D, Dv, dtype, seed):
+    from kernelized_sequence_mixing_gb300.workloads import make_qkv
+    q, k, v = make_qkv(B, H, N, D, Dv, dtype, seed, 0.5)
+    g = torch.Generator().manual_seed(seed + 99)
+    do = torch.randn((B, H, N, Dv), generator=g).to(dtype)
+    return q, k, v, do
+
+
+BWD_CASES = [
+    # (B, H, N, D, Dv, gammas)
+    (1, 1, 1, 64, 64, None),
+    (1, 2, 63, 64, 128, None),
+    (2, 2, 333, 128, 64, [0.9, 1.0]),
+    (1, 3, 700, 128, 128, [0.5, 0.97, 0.999]),
+    (1, 1, 1000, 64, 64, [0.0]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "x".join(map(str, c[:5])))
+def test_backward(la, bw, dtype, case):
+    B, H, N, D, Dv, gl = case
+    q, k, v, do = inputs(B, H, N, D, Dv, dtype, N + D + Dv)
+    g = None if gl is None else torch.tensor([gl[h % len(gl)] for h in range(H)],
+                                             dtype=torch.float32)
+    dq, dk, dv = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), gamma=g)
+    torch.cuda.synchronize()
+    gu = None if g is None else np.tile(g.numpy(), B).reshape(B, H)
+    rq, rk, rv = bw.causal_backward_units(to_np(q), to_np(k), to_np(v), to_np(do), gu, 1e-6)
+    sizes = [np.zeros_like(r) for r in (rq, rk, rv)]
+    for b in range(B):
+        for h in range(H):
+            ts = term_sizes(to_np(q[b, h]), to_np(k[b, h]), to_np(v[b, h]), to_np(do[b, h]),
+                            None if gu is None else gu[b, h], 1e-6)
+            for arr, t in zip(sizes, ts):
+                arr[b, h] = t
+    tol = BWD_TOL[dtype]
+    for name, got, ref, sz in (("dq", dq, rq, sizes[0]), ("dk", dk, rk, sizes[1]),
+                               ("dv", dv, rv, sizes[2])):
+        err = unit_err(to_np(got), ref, sz)
+        assert err < tol, (name, err)
+
+
+def test_backward_repeatable_and_empty(la):
+    q, k, v, do = inputs(1, 2, 500, 64, 64, torch.bfloat16, 3)
+    a1 = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda())
+    a2 = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda())
+    assert all(torch.equal(x, y) for x, y in zip(a1, a2))
+    e = torch.empty((1, 2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    dq, dk, dv = la.backward(e, e, e, e)
+    assert dq.numel() == 0
+
+
+def test_backward_bf16_n4096_sampled_units(la, bw):
+    """The backward workload at full size (B4 H8 N4096 D=Dv=64), in the
+    launch configuration the benchmark times; whole units sampled."""
+    from kernelized_sequence_mixing_gb300.workloads import WORKLOADS, workload_inputs, workload_upstream
+    w = WORKLOADS["backward_bf16_n4096"]
+    q, k, v = workload_inputs(w)
+    do = workload_upstream(w)
+    dq, dk, dv = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), eps=w.eps)
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (3, 5)):
+        args = (to_np(q[b, h]), to_np(k[b, h]), to_np(v[b, h]), to_np(do[b, h]), None, w.eps)
+        refs = bw.causal_backward(*args)
+        for name, got, ref, sz in zip(("dq", "dk", "dv"), (dq, dk, dv), refs, term_sizes(*args)):
+            err = unit_err(to_np(got[b, h]), ref, sz)
+            assert err < 1e-2, (b, h, name, err)
