@@ -444,9 +444,9 @@ def run_ours(args, w):
             oh.copy_(od, non_blocking=True)
         tokens_rank = w.B * w.N
     elif w.backward:
-        # backward: operand preparation, four chunked causal products (the
-        # forward's n and d, dphi(q), dv, dphi(k)), the middle and final
-        # elementwise kernels
+        # backward: operand preparation, the forward's n and d (one chunked
+        # causal product), the middle elementwise kernel, the three gradient
+        # products in one launch, the final elementwise kernel
         from kernelized_sequence_mixing_gb300.workloads import workload_upstream
         q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.Dv, w.dtype, seed, w.scale)
         do = workload_upstream(w)
@@ -454,7 +454,7 @@ def run_ours(args, w):
         grads = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
         od = grads[2]
         ncopy = 1
-        launches_per_step = 7
+        launches_per_step = 5
 
         def step():
             la.backward(qd, kd, vd, dod, eps=w.eps, dq=grads[0], dk=grads[1], dv=grads[2])

@@ -36,131 +36,235 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kThreads = 256;
-constexpr int kLd = kC + 4;
-constexpr int kCs = 32;  // columns of c per CTA
+constexpr int kLdA = kC + 4;  // row stride of the transposed A tile
+constexpr int kCs = 32;       // columns of c per CTA
 
 template <int DA>
 struct ProdLayout {
-  static constexpr int aT = DA * kLd, bT = DA * kLd, A = kC * (kC + 1), cs = kC * kCs,
-                       H = DA * kCs, G = kC + 4;
+  static constexpr int aT = DA * kC, bT = DA * kC, A = kC * kLdA, cs = kC * kCs, H = DA * kCs,
+                       G = kC + 4;
   static constexpr size_t bytes = sizeof(float) * (aT + bT + A + cs + H + G);
 };
 
-// grid: x = (batch, head), y = ceil(DC / 32).  a, b: [BH][N][DA]; c, y:
-// [BH][N][DC], fp32.
-template <int DA, int DC, bool REV>
-__global__ void __launch_bounds__(kThreads)
-    causal_product_kernel(const float *__restrict__ a, const float *__restrict__ b,
-                          const float *__restrict__ c, float *__restrict__ y, int H, int N,
-                          const __grid_constant__ Gammas gam) {
-  extern __shared__ float4 smem4[];
-  using L = ProdLayout<DA>;
-  float *aT = reinterpret_cast<float *>(smem4);  // [DA][kLd]
-  float *bT = aT + L::aT;                        // [DA][kLd]
-  float *As = bT + L::bT;                        // [kC][kC+1]
-  float *cs = As + L::A;                         // [kC][kCs]
-  float *Hs = cs + L::cs;                        // [DA][kCs]
-  float *G = Hs + L::H;                          // gamma^k, k = 0..kC
+struct ProdArgs {
+  const float *a, *b, *c;
+  float *y;
+};
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// One CTA of the product over a (batch, head) and 32-column slice of c:
+// a, b [BH][N][DA]; c, y [BH][N][DC], fp32.  Per 64-token chunk:
+//   load   item (t = i mod 64, column quad i / 64): 16-byte loads of a row's
+//          quad, stored transposed ([column][token]) by consecutive lanes at
+//          consecutive tokens;
+//   A      16 x 16 threads, 4 x 4 register tiles of a b^T, masked and decayed,
+//          stored transposed ([s][t]);
+//   y      4 tokens x 2 columns per thread: y = A c + gamma^k a^T H;
+//   H      4 rows x 4 columns per item: H = gamma^nv H + sum_s gamma^k b_s c_s^T.
+template <int DA, int DC, bool REV>
+__device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int H, int N,
+                                             const Gammas &gam, float *smem) {
+  using L = ProdLayout<DA>;
+  float *aT = smem;          // [DA][kC]
+  float *bT = aT + L::aT;    // [DA][kC]
+  float *AT = bT + L::bT;    // [kC][kLdA]
+  float *cs = AT + L::A;     // [kC][kCs]
+  float *Hs = cs + L::cs;    // [DA][kCs]
+  float *G = Hs + L::H;      // gamma^k, k = 0..kC
+  constexpr int DQ = DA / 4;
+
+  const int tid = threadIdx.x;
   const int64_t bh = blockIdx.x;
-  const int e0 = blockIdx.y * kCs;
+  const int e0 = slice * kCs;
   const int ncol = min(kCs, DC - e0);
-  const float *ah = a + bh * N * DA;
-  const float *bh_ = b + bh * N * DA;
-  const float *ch = c + bh * N * DC;
-  float *yh = y + bh * N * DC;
+  const float *ah = pa.a + bh * N * DA;
+  const float *bhp = pa.b + bh * N * DA;
+  const float *ch = pa.c + bh * N * DC;
+  float *yh = pa.y + bh * N * DC;
 
   for (int i = tid; i < DA * kCs; i += kThreads) Hs[i] = 0.f;
   if (tid == 0) build_pow_table(G, kC, gam.g[bh % H]);
   __syncthreads();
 
-  const int ty = tid >> 4, tx = tid & 15;
   const int nch = (N + kC - 1) / kC;
   for (int ci = 0; ci < nch; ++ci) {
     const int cidx = REV ? nch - 1 - ci : ci;
     const int c0 = cidx * kC, nv = min(kC, N - c0);
-    for (int i = tid; i < kC * DA; i += kThreads) {
-      const int t = i / DA, d = i % DA;
-      float xa = 0.f, xb = 0.f;
+    for (int i = tid; i < kC * DQ; i += kThreads) {
+      const int t = i & (kC - 1), q4 = i >> 6;
+      float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
       if (t < nv) {
-        xa = ah[(int64_t)(c0 + t) * DA + d];
-        xb = bh_[(int64_t)(c0 + t) * DA + d];
+        xa = *reinterpret_cast<const float4 *>(ah + (int64_t)(c0 + t) * DA + 4 * q4);
+        xb = *reinterpret_cast<const float4 *>(bhp + (int64_t)(c0 + t) * DA + 4 * q4);
       }
-      aT[d * kLd + t] = xa;
-      bT[d * kLd + t] = xb;
+      aT[(4 * q4 + 0) * kC + t] = xa.x;
+      aT[(4 * q4 + 1) * kC + t] = xa.y;
+      aT[(4 * q4 + 2) * kC + t] = xa.z;
+      aT[(4 * q4 + 3) * kC + t] = xa.w;
+      bT[(4 * q4 + 0) * kC + t] = xb.x;
+      bT[(4 * q4 + 1) * kC + t] = xb.y;
+      bT[(4 * q4 + 2) * kC + t] = xb.z;
+      bT[(4 * q4 + 3) * kC + t] = xb.w;
     }
-    for (int i = tid; i < kC * kCs; i += kThreads) {
-      const int t = i / kCs, e = i % kCs;
-      cs[i] = (t < nv && e < ncol) ? ch[(int64_t)(c0 + t) * DC + e0 + e] : 0.f;
+    for (int i = tid; i < kC * (kCs / 4); i += kThreads) {
+      const int t = i >> 3, q4 = i & 7;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < nv && 4 * q4 < ncol) {
+        const float *src = ch + (int64_t)(c0 + t) * DC + e0 + 4 * q4;
+        if (DC % 4 == 0) {
+          x = *reinterpret_cast<const float4 *>(src);
+        } else {
+          x.x = src[0];
+          if (4 * q4 + 1 < ncol) x.y = src[1];
+          if (4 * q4 + 2 < ncol) x.z = src[2];
+          if (4 * q4 + 3 < ncol) x.w = src[3];
+        }
+      }
+      *reinterpret_cast<float4 *>(cs + t * kCs + 4 * q4) = x;
     }
     __syncthreads();
     // A_ts = gamma^|t-s| a_t . b_s on s <= t (forward) or s >= t (reversed)
     {
+      const int ty = tid >> 4, tx = tid & 15;
       float acc[4][4] = {};
+      if (REV ? tx >= ty : tx <= ty) {
 #pragma unroll 4
-      for (int d = 0; d < DA; ++d) {
-        const float4 x = *reinterpret_cast<const float4 *>(aT + d * kLd + ty * 4);
-        const float4 w = *reinterpret_cast<const float4 *>(bT + d * kLd + tx * 4);
-        const float xv[4] = {x.x, x.y, x.z, x.w};
+        for (int d = 0; d < DA; ++d) {
+          const float4 x = *reinterpret_cast<const float4 *>(aT + d * kC + 4 * ty);
+          const float4 w = *reinterpret_cast<const float4 *>(bT + d * kC + 4 * tx);
+          const float xv[4] = {x.x, x.y, x.z, x.w};
+          const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float col[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = 4 * ty + i, sidx = 4 * tx + j;
+          const bool in = REV ? sidx >= t : sidx <= t;
+          col[i] = in ? acc[i][j] * G[REV ? sidx - t : t - sidx] : 0.f;
+        }
+        *reinterpret_cast<float4 *>(AT + (4 * tx + j) * kLdA + 4 * ty) =
+            make_float4(col[0], col[1], col[2], col[3]);
+      }
+    }
+    __syncthreads();
+    // y_t = A_t. c + gamma^k a_t^T H, k = t + 1 (forward) or nv - t (reversed)
+    {
+      const int ep = tid & 15, tg = tid >> 4;
+      float acc[4][2] = {};
+      const int s0 = REV ? 4 * tg : 0, s1 = REV ? kC : 4 * tg + 4;
+      for (int sidx = s0; sidx < s1; ++sidx) {
+        const float4 w = *reinterpret_cast<const float4 *>(AT + sidx * kLdA + 4 * tg);
+        const float2 x = *reinterpret_cast<const float2 *>(cs + sidx * kCs + 2 * ep);
         const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int t = ty * 4 + i, s = tx * 4 + j;
-          const bool in = REV ? s >= t : s <= t;
-          As[t * (kC + 1) + s] = in ? acc[i][j] * G[REV ? s - t : t - s] : 0.f;
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] = fmaf(wv[i], x.x, acc[i][0]);
+          acc[i][1] = fmaf(wv[i], x.y, acc[i][1]);
         }
-    }
-    __syncthreads();
-    // y_t = A_t. c + gamma^k a_t^T H, k = t + 1 (forward) or nv - t (reversed);
-    // warp w owns rows 8w..8w+7, lane owns column e0 + lane
-    {
-      constexpr int R = kC / 8;
-      const int t0 = warp * R;
-      float num[R], inter[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) num[r] = inter[r] = 0.f;
-      for (int s = 0; s < kC; ++s) {
-        const float cv = cs[s * kCs + lane];
-#pragma unroll
-        for (int r = 0; r < R; ++r) num[r] = fmaf(As[(t0 + r) * (kC + 1) + s], cv, num[r]);
       }
+      float inter[4][2] = {};
 #pragma unroll 4
       for (int d = 0; d < DA; ++d) {
-        const float hv = Hs[d * kCs + lane];
-        const float4 f0 = *reinterpret_cast<const float4 *>(aT + d * kLd + t0);
-        const float4 f1 = *reinterpret_cast<const float4 *>(aT + d * kLd + t0 + 4);
-        const float fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        const float4 f = *reinterpret_cast<const float4 *>(aT + d * kC + 4 * tg);
+        const float2 hv = *reinterpret_cast<const float2 *>(Hs + d * kCs + 2 * ep);
+        const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-        for (int r = 0; r < R; ++r) inter[r] = fmaf(fv[r], hv, inter[r]);
+        for (int i = 0; i < 4; ++i) {
+          inter[i][0] = fmaf(fv[i], hv.x, inter[i][0]);
+          inter[i][1] = fmaf(fv[i], hv.y, inter[i][1]);
+        }
       }
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int t = t0 + r;
-        if (t < nv && lane < ncol)
-          yh[(int64_t)(c0 + t) * DC + e0 + lane] = fmaf(G[REV ? nv - t : t + 1], inter[r], num[r]);
+      for (int i = 0; i < 4; ++i) {
+        const int t = 4 * tg + i;
+        if (t >= nv) continue;
+        const float gk = G[REV ? nv - t : t + 1];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+          if (2 * ep + jj < ncol)
+            yh[(int64_t)(c0 + t) * DC + e0 + 2 * ep + jj] = fmaf(gk, inter[i][jj], acc[i][jj]);
       }
     }
     __syncthreads();
-    // H = gamma^nv H + sum_s gamma^k b_s c_s^T, k = nv - 1 - s (forward) or s
-    // (reversed: H relative to the chunk's first token)
+    // H = gamma^nv H + sum_s w_s b_s c_s^T, w_s = gamma^(nv-1-s) (forward) or
+    // gamma^s (reversed: H relative to the chunk's first token)
     {
       const float gn = G[nv];
-      for (int d = warp; d < DA; d += 8) {
-        float acc = 0.f;
-        for (int s = 0; s < nv; ++s)
-          acc = fmaf(bT[d * kLd + s] * G[REV ? s : nv - 1 - s], cs[s * kCs + lane], acc);
-        Hs[d * kCs + lane] = fmaf(gn, Hs[d * kCs + lane], acc);
+      for (int it = tid; it < DQ * (kCs / 4); it += kThreads) {
+        const int dq = it >> 3, eq = it & 7;
+        float acc[4][4] = {};
+        for (int sidx = 0; sidx < kC; sidx += 4) {
+          float4 kb[4], vv[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            kb[r] = *reinterpret_cast<const float4 *>(bT + (4 * dq + r) * kC + sidx);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            vv[j] = *reinterpret_cast<const float4 *>(cs + (sidx + j) * kCs + 4 * eq);
+          float wgt[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int sj = sidx + j;
+            wgt[j] = sj < nv ? G[REV ? sj : nv - 1 - sj] : 0.f;
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float kr[4] = {kb[r].x * wgt[0], kb[r].y * wgt[1], kb[r].z * wgt[2],
+                                 kb[r].w * wgt[3]};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              acc[r][0] = fmaf(kr[j], vv[j].x, acc[r][0]);
+              acc[r][1] = fmaf(kr[j], vv[j].y, acc[r][1]);
+              acc[r][2] = fmaf(kr[j], vv[j].z, acc[r][2]);
+              acc[r][3] = fmaf(kr[j], vv[j].w, acc[r][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          float4 *hp = reinterpret_cast<float4 *>(Hs + (4 * dq + r) * kCs + 4 * eq);
+          float4 h = *hp;
+          h.x = fmaf(gn, h.x, acc[r][0]);
+          h.y = fmaf(gn, h.y, acc[r][1]);
+          h.z = fmaf(gn, h.z, acc[r][2]);
+          h.w = fmaf(gn, h.w, acc[r][3]);
+          *hp = h;
+        }
       }
     }
     __syncthreads();
+  }
+}
+
+// One product per launch: grid x = (batch, head), y = ceil(DC / 32).
+template <int DA, int DC, bool REV>
+__global__ void __launch_bounds__(kThreads, 2)
+    causal_product_kernel(ProdArgs pa, int H, int N, const __grid_constant__ Gammas gam) {
+  extern __shared__ float4 smem4[];
+  product_body<DA, DC, REV>(pa, blockIdx.y, H, N, gam, reinterpret_cast<float *>(smem4));
+}
+
+// The three gradient products in one launch (grid z = 0, 1, 2):
+//   dphi(q) <DV4, D, forward>, dv <D, DV, reversed>, dphi(k) <DV4, D, reversed>.
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads, 2)
+    gradient_products_kernel(ProdArgs p0, ProdArgs p1, ProdArgs p2, int H, int N,
+                             const __grid_constant__ Gammas gam) {
+  extern __shared__ float4 smem4[];
+  float *sm = reinterpret_cast<float *>(smem4);
+  constexpr int DV4 = DV + 4;
+  if (blockIdx.z == 0) {
+    if (blockIdx.y < (D + kCs - 1) / kCs) product_body<DV4, D, false>(p0, blockIdx.y, H, N, gam, sm);
+  } else if (blockIdx.z == 1) {
+    if (blockIdx.y < (DV + kCs - 1) / kCs) product_body<D, DV, true>(p1, blockIdx.y, H, N, gam, sm);
+  } else {
+    if (blockIdx.y < (D + kCs - 1) / kCs) product_body<DV4, D, true>(p2, blockIdx.y, H, N, gam, sm);
   }
 }
 
@@ -171,7 +275,8 @@ cudaError_t product_launch(const float *a, const float *b, const float *c, float
   const size_t smem = ProdLayout<DA>::bytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3((unsigned)BH, (DC + kCs - 1) / kCs), kThreads, smem, s>>>(a, b, c, y, H, N, g);
+  kern<<<dim3((unsigned)BH, (DC + kCs - 1) / kCs), kThreads, smem, s>>>(ProdArgs{a, b, c, y}, H,
+                                                                          N, g);
   return cudaGetLastError();
 }
 
@@ -266,9 +371,18 @@ cudaError_t backward_typed(const Problem &p, const void *dO, void *dq, void *dk,
   bwd_mid_kernel<T><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, s>>>(
       nd, static_cast<const T *>(dO), gc, gt, rows, DV, p.eps);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = product_launch<DV4, D, false>(gc, vm, fk, dfq, BH, p.H, p.N, g, s)) != cudaSuccess) return e;
-  if ((e = product_launch<D, DV, true>(fk, fq, gt, dvf, BH, p.H, p.N, g, s)) != cudaSuccess) return e;
-  if ((e = product_launch<DV4, D, true>(vm, gc, fq, dfk, BH, p.H, p.N, g, s)) != cudaSuccess) return e;
+  {
+    // dphi(q), dv and dphi(k) are independent: one launch, grid z selects
+    auto kern = gradient_products_kernel<D, DV>;
+    const size_t smem = ProdLayout<(DV4 > D ? DV4 : D)>::bytes;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return e;
+    const unsigned ny = ((D > DV ? D : DV) + kCs - 1) / kCs;
+    kern<<<dim3((unsigned)BH, ny, 3), kThreads, smem, s>>>(
+        ProdArgs{gc, vm, fk, dfq}, ProdArgs{fk, fq, gt, dvf}, ProdArgs{vm, gc, fq, dfk}, p.H, p.N, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   {
     const int64_t n = rows * (2 * D + DV);
     bwd_final_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
