@@ -454,7 +454,7 @@ def run_ours(args, w):
         grads = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
         od = grads[2]
         ncopy = 1
-        launches_per_step = 5
+        launches_per_step = la.backward_launches(w.B, w.H, w.N, w.D, w.Dv)
 
         def step():
             la.backward(qd, kd, vd, dod, eps=w.eps, dq=grads[0], dk=grads[1], dv=grads[2])

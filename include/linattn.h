@@ -232,13 +232,22 @@ LA_API la_status_t la_forward_favor(const void *q, const void *k, const void *v,
  * The library recomputes o and d itself (the caller keeps no forward
  * state).  q, k, dq, dk: [B][H][N][D]; v, dO, dv: [B][H][N][Dv]; all of
  * `dtype`; fp32 arithmetic on CUDA cores in a stream-ordered workspace of
- * B*H*N*(4D + 6Dv + 16)*4 bytes (cudaMallocAsync on `stream`).  No gradient
- * may overlap an input or another gradient.  Errors as la_forward.
+ * B*H*N*(4D + 6Dv + 16)*4 bytes plus the per-part states of the sequence
+ * split (cudaMallocAsync on `stream`).  No gradient may overlap an input or
+ * another gradient.  Errors as la_forward.
  */
 LA_API la_status_t la_backward(const void *q, const void *k, const void *v, const void *dO,
                                void *dq, void *dk, void *dv, int B, int H, int N, int D,
                                int Dv, const float *gamma, float eps, la_dtype_t dtype,
                                void *stream);
+
+/*
+ * Number of kernels one la_backward call with these sizes launches (it
+ * depends on how the sequence is split across the current device's SMs), 0
+ * for an empty call, or a negative la_status_t (negated) for invalid sizes.
+ * Host-only apart from reading the current device's SM count.
+ */
+LA_API int la_backward_launches(int B, int H, int N, int D, int Dv);
 
 /*
  * Which kernel la_forward would run for a causal call with these arguments:

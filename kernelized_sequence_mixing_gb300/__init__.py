@@ -88,6 +88,8 @@ def load_library() -> ctypes.CDLL:
             lib.la_forward_favor.restype = I
             lib.la_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, FP, F, I, P]
             lib.la_backward.restype = I
+            lib.la_backward_launches.argtypes = [I, I, I, I, I]
+            lib.la_backward_launches.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
             lib.la_device_wait_timeouts.argtypes = [I]
@@ -410,3 +412,12 @@ def backward(q, k, v, do, gamma=None, eps=1e-6, dq=None, dk=None, dv=None):
             _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, D, Dv,
             _gamma_arg(gamma, H), float(eps), _dtype_code(q), _stream(dev)))
     return dq, dk, dv
+
+
+def backward_launches(B, H, N, D, Dv) -> int:
+    """Kernels one backward() call with these sizes launches on the current
+    device."""
+    n = load_library().la_backward_launches(B, H, N, D, Dv)
+    if n < 0:
+        raise LinAttnError("la_backward_launches", -n)
+    return int(n)

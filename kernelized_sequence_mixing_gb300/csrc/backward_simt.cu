@@ -49,7 +49,14 @@ struct ProdLayout {
 struct ProdArgs {
   const float *a, *b, *c;
   float *y;
+  float *rec;  // per-part states [B*H][P][DA][DC] (P > 1)
 };
+
+enum { kPassOut = 0, kPassState = 1 };
+
+__host__ __device__ inline int part_chunk(int p, int P, int nch) {
+  return static_cast<int>((static_cast<long long>(p) * nch) / P);
+}
 
 // One CTA of the product over a (batch, head) and 32-column slice of c:
 // a, b [BH][N][DA]; c, y [BH][N][DC], fp32.  Per 64-token chunk:
@@ -60,9 +67,14 @@ struct ProdArgs {
 //          stored transposed ([s][t]);
 //   y      4 tokens x 2 columns per thread: y = A c + gamma^k a^T H;
 //   H      4 rows x 4 columns per item: H = gamma^nv H + sum_s gamma^k b_s c_s^T.
-template <int DA, int DC, bool REV>
-__device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int H, int N,
-                                             const Gammas &gam, float *smem) {
+// Sequence parts: part `part` of P covers whole chunks [cb, ce).  The output
+// pass starts from the state the scan left for it (forward: the state after
+// part - 1; reversed: the state before part + 1) and the state pass only
+// carries H from zero over its part and stores it.
+template <int DA, int DC, bool REV, int PASS>
+__device__ __forceinline__ void product_body(const ProdArgs &pa, int64_t bh, int part, int P,
+                                             int slice, int H, int N, const Gammas &gam,
+                                             float *smem) {
   using L = ProdLayout<DA>;
   float *aT = smem;          // [DA][kC]
   float *bT = aT + L::aT;    // [DA][kC]
@@ -73,7 +85,6 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
   constexpr int DQ = DA / 4;
 
   const int tid = threadIdx.x;
-  const int64_t bh = blockIdx.x;
   const int e0 = slice * kCs;
   const int ncol = min(kCs, DC - e0);
   const float *ah = pa.a + bh * N * DA;
@@ -81,25 +92,39 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
   const float *ch = pa.c + bh * N * DC;
   float *yh = pa.y + bh * N * DC;
 
-  for (int i = tid; i < DA * kCs; i += kThreads) Hs[i] = 0.f;
+  const size_t rstride = static_cast<size_t>(DA) * DC;
+  const int pin = REV ? part + 1 : part - 1;  // the part whose scanned state starts this one
+  if (PASS == kPassOut && pin >= 0 && pin < P) {
+    const float *r = pa.rec + (static_cast<size_t>(bh) * P + pin) * rstride;
+    for (int i = tid; i < DA * kCs; i += kThreads) {
+      const int d = i / kCs, e = i % kCs;
+      Hs[i] = e < ncol ? r[d * DC + e0 + e] : 0.f;
+    }
+  } else {
+    for (int i = tid; i < DA * kCs; i += kThreads) Hs[i] = 0.f;
+  }
   if (tid == 0) build_pow_table(G, kC, gam.g[bh % H]);
   __syncthreads();
 
-  const int nch = (N + kC - 1) / kC;
-  for (int ci = 0; ci < nch; ++ci) {
-    const int cidx = REV ? nch - 1 - ci : ci;
+  const int nch_all = (N + kC - 1) / kC;
+  const int cb = part_chunk(part, P, nch_all), ce = part_chunk(part + 1, P, nch_all);
+  for (int ci = 0; ci < ce - cb; ++ci) {
+    const int cidx = REV ? ce - 1 - ci : cb + ci;
     const int c0 = cidx * kC, nv = min(kC, N - c0);
     for (int i = tid; i < kC * DQ; i += kThreads) {
       const int t = i & (kC - 1), q4 = i >> 6;
       float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
       if (t < nv) {
-        xa = *reinterpret_cast<const float4 *>(ah + (int64_t)(c0 + t) * DA + 4 * q4);
+        if (PASS == kPassOut)
+          xa = *reinterpret_cast<const float4 *>(ah + (int64_t)(c0 + t) * DA + 4 * q4);
         xb = *reinterpret_cast<const float4 *>(bhp + (int64_t)(c0 + t) * DA + 4 * q4);
       }
-      aT[(4 * q4 + 0) * kC + t] = xa.x;
-      aT[(4 * q4 + 1) * kC + t] = xa.y;
-      aT[(4 * q4 + 2) * kC + t] = xa.z;
-      aT[(4 * q4 + 3) * kC + t] = xa.w;
+      if (PASS == kPassOut) {
+        aT[(4 * q4 + 0) * kC + t] = xa.x;
+        aT[(4 * q4 + 1) * kC + t] = xa.y;
+        aT[(4 * q4 + 2) * kC + t] = xa.z;
+        aT[(4 * q4 + 3) * kC + t] = xa.w;
+      }
       bT[(4 * q4 + 0) * kC + t] = xb.x;
       bT[(4 * q4 + 1) * kC + t] = xb.y;
       bT[(4 * q4 + 2) * kC + t] = xb.z;
@@ -123,7 +148,7 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
     }
     __syncthreads();
     // A_ts = gamma^|t-s| a_t . b_s on s <= t (forward) or s >= t (reversed)
-    {
+    if (PASS == kPassOut) {
       const int ty = tid >> 4, tx = tid & 15;
       float acc[4][4] = {};
       if (REV ? tx >= ty : tx <= ty) {
@@ -152,9 +177,9 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
             make_float4(col[0], col[1], col[2], col[3]);
       }
     }
-    __syncthreads();
+    if (PASS == kPassOut) __syncthreads();
     // y_t = A_t. c + gamma^k a_t^T H, k = t + 1 (forward) or nv - t (reversed)
-    {
+    if (PASS == kPassOut) {
       const int ep = tid & 15, tg = tid >> 4;
       float acc[4][2] = {};
       const int s0 = REV ? 4 * tg : 0, s1 = REV ? kC : 4 * tg + 4;
@@ -191,7 +216,7 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
             yh[(int64_t)(c0 + t) * DC + e0 + 2 * ep + jj] = fmaf(gk, inter[i][jj], acc[i][jj]);
       }
     }
-    __syncthreads();
+    if (PASS == kPassOut) __syncthreads();
     // H = gamma^nv H + sum_s w_s b_s c_s^T, w_s = gamma^(nv-1-s) (forward) or
     // gamma^s (reversed: H relative to the chunk's first token)
     {
@@ -240,43 +265,166 @@ __device__ __forceinline__ void product_body(const ProdArgs &pa, int slice, int 
     }
     __syncthreads();
   }
+  if (PASS == kPassState) {
+    float *r = pa.rec + (static_cast<size_t>(bh) * P + part) * rstride;
+    for (int i = tid; i < DA * kCs; i += kThreads) {
+      const int d = i / kCs, e = i % kCs;
+      if (e < ncol) r[d * DC + e0 + e] = Hs[i];
+    }
+  }
 }
 
-// One product per launch: grid x = (batch, head), y = ceil(DC / 32).
+// The scan over parts of one product, in place over the records of one
+// (batch, head): forward, record p (the state of part p from zero, relative
+// to its last token) becomes the state after parts 0..p, S(p) =
+// gamma^len(p) S(p-1) + rec(p), for p < P - 1; reversed, record p (relative
+// to its first token) becomes the state of parts p..P-1, for p > 0.
+constexpr int kMaxParts = 64;
+
+// gamma^len(p) for every part, once per CTA (one fp64 power per part, from
+// threads 0..P-1).
+__device__ __forceinline__ void part_weights(float *w, int P, int N, float gamma) {
+  const int nch_all = (N + kC - 1) / kC;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int t0 = part_chunk(p, P, nch_all) * kC;
+    const int t1 = min(N, part_chunk(p + 1, P, nch_all) * kC);
+    w[p] = static_cast<float>(pow(static_cast<double>(gamma), static_cast<double>(t1 - t0)));
+  }
+  __syncthreads();
+}
+
 template <int DA, int DC, bool REV>
+__device__ __forceinline__ void scan_body(float *rec, int64_t bh, int P, const float *w) {
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;
+  if (i >= DA * DC) return;
+  const size_t rstride = static_cast<size_t>(DA) * DC;
+  float *r = rec + static_cast<size_t>(bh) * P * rstride + i;
+  float carry = 0.f;
+  for (int j = 0; j < P - 1; ++j) {
+    const int p = REV ? P - 1 - j : j;
+    carry = fmaf(w[p], carry, r[p * rstride]);
+    r[p * rstride] = carry;
+  }
+}
+
+// grid x = (batch, head) * parts of this pass + part: the output pass has P
+// parts; the state pass P - 1 (every part but the last one in scan order).
+__device__ __forceinline__ void pass_part(int PASS_, bool rev, int P, int64_t *bh, int *part) {
+  const int pg = PASS_ == kPassOut ? P : P - 1;
+  *bh = blockIdx.x / pg;
+  *part = blockIdx.x % pg + (PASS_ == kPassState && rev ? 1 : 0);
+}
+
+// One product: grid y = ceil(DC / 32) column slices.
+template <int DA, int DC, bool REV, int PASS>
 __global__ void __launch_bounds__(kThreads, 2)
-    causal_product_kernel(ProdArgs pa, int H, int N, const __grid_constant__ Gammas gam) {
+    causal_product_kernel(ProdArgs pa, int P, int H, int N, const __grid_constant__ Gammas gam) {
   extern __shared__ float4 smem4[];
-  product_body<DA, DC, REV>(pa, blockIdx.y, H, N, gam, reinterpret_cast<float *>(smem4));
+  int64_t bh;
+  int part;
+  pass_part(PASS, REV, P, &bh, &part);
+  product_body<DA, DC, REV, PASS>(pa, bh, part, P, blockIdx.y, H, N, gam,
+                                  reinterpret_cast<float *>(smem4));
 }
 
 // The three gradient products in one launch (grid z = 0, 1, 2):
 //   dphi(q) <DV4, D, forward>, dv <D, DV, reversed>, dphi(k) <DV4, D, reversed>.
-template <int D, int DV>
+template <int D, int DV, int PASS>
 __global__ void __launch_bounds__(kThreads, 2)
-    gradient_products_kernel(ProdArgs p0, ProdArgs p1, ProdArgs p2, int H, int N,
+    gradient_products_kernel(ProdArgs p0, ProdArgs p1, ProdArgs p2, int P, int H, int N,
                              const __grid_constant__ Gammas gam) {
   extern __shared__ float4 smem4[];
   float *sm = reinterpret_cast<float *>(smem4);
   constexpr int DV4 = DV + 4;
+  int64_t bh;
+  int part;
   if (blockIdx.z == 0) {
-    if (blockIdx.y < (D + kCs - 1) / kCs) product_body<DV4, D, false>(p0, blockIdx.y, H, N, gam, sm);
+    pass_part(PASS, false, P, &bh, &part);
+    if (blockIdx.y < (D + kCs - 1) / kCs)
+      product_body<DV4, D, false, PASS>(p0, bh, part, P, blockIdx.y, H, N, gam, sm);
   } else if (blockIdx.z == 1) {
-    if (blockIdx.y < (DV + kCs - 1) / kCs) product_body<D, DV, true>(p1, blockIdx.y, H, N, gam, sm);
+    pass_part(PASS, true, P, &bh, &part);
+    if (blockIdx.y < (DV + kCs - 1) / kCs)
+      product_body<D, DV, true, PASS>(p1, bh, part, P, blockIdx.y, H, N, gam, sm);
   } else {
-    if (blockIdx.y < (D + kCs - 1) / kCs) product_body<DV4, D, true>(p2, blockIdx.y, H, N, gam, sm);
+    pass_part(PASS, true, P, &bh, &part);
+    if (blockIdx.y < (D + kCs - 1) / kCs)
+      product_body<DV4, D, true, PASS>(p2, bh, part, P, blockIdx.y, H, N, gam, sm);
   }
 }
 
+// Scans: grid x = (batch, head), y = blocks of 256 state entries.
 template <int DA, int DC, bool REV>
-cudaError_t product_launch(const float *a, const float *b, const float *c, float *y, int BH,
-                           int H, int N, const Gammas &g, cudaStream_t s) {
-  auto kern = causal_product_kernel<DA, DC, REV>;
+__global__ void __launch_bounds__(256)
+    product_scan_kernel(float *rec, int P, int H, int N, const __grid_constant__ Gammas gam) {
+  __shared__ float w[kMaxParts];
+  part_weights(w, P, N, gam.g[blockIdx.x % H]);
+  scan_body<DA, DC, REV>(rec, blockIdx.x, P, w);
+}
+template <int D, int DV>
+__global__ void __launch_bounds__(256)
+    gradient_scan_kernel(float *r0, float *r1, float *r2, int P, int H, int N,
+                         const __grid_constant__ Gammas gam) {
+  constexpr int DV4 = DV + 4;
+  __shared__ float w[kMaxParts];
+  part_weights(w, P, N, gam.g[blockIdx.x % H]);
+  if (blockIdx.z == 0) scan_body<DV4, D, false>(r0, blockIdx.x, P, w);
+  else if (blockIdx.z == 1) scan_body<D, DV, true>(r1, blockIdx.x, P, w);
+  else scan_body<DV4, D, true>(r2, blockIdx.x, P, w);
+}
+
+int num_sms_bwd() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// Parts per (batch, head): the count minimising a wave model of the output
+// pass plus the state pass (measured at about 0.3 of it), with
+// waves(n) = ceil(ctas_per_part * n / (2 CTAs per SM x SMs)), plus a fixed
+// cost per part (its records, its start-up) of 0.01 of a full-sequence pass;
+// at most one part per 2 chunks and kMaxParts.
+int product_parts(long long ctas_per_part, int N) {
+  const long long nch = (N + kC - 1) / kC;
+  const long long slots = 2LL * num_sms_bwd();
+  auto waves = [&](long long n) { return (ctas_per_part * n + slots - 1) / slots; };
+  const long long pmax = nch / 2 < kMaxParts ? nch / 2 : kMaxParts;
+  long long best = 1;
+  double best_t = static_cast<double>(waves(1));
+  for (long long P = 2; P <= pmax; ++P) {
+    const double t =
+        (static_cast<double>(waves(P)) + 0.3 * static_cast<double>(waves(P - 1))) / P + 0.01 * P;
+    if (t < best_t * 0.97) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return static_cast<int>(best);
+}
+
+template <int DA, int DC, bool REV>
+cudaError_t product_launch(const float *a, const float *b, const float *c, float *y, float *rec,
+                           int P, int BH, int H, int N, const Gammas &g, cudaStream_t s) {
   const size_t smem = ProdLayout<DA>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3((unsigned)BH, (DC + kCs - 1) / kCs), kThreads, smem, s>>>(ProdArgs{a, b, c, y}, H,
-                                                                          N, g);
+  const unsigned ny = (DC + kCs - 1) / kCs;
+  const ProdArgs pa{a, b, c, y, rec};
+  cudaError_t e;
+  if (P > 1) {
+    auto ks = causal_product_kernel<DA, DC, REV, kPassState>;
+    if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return e;
+    ks<<<dim3((unsigned)(BH * (P - 1)), ny), kThreads, smem, s>>>(pa, P, H, N, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    product_scan_kernel<DA, DC, REV><<<dim3((unsigned)BH, (DA * DC + 255) / 256), 256, 0, s>>>(
+        rec, P, H, N, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto ko = causal_product_kernel<DA, DC, REV, kPassOut>;
+  if ((e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+    return e;
+  ko<<<dim3((unsigned)(BH * P), ny), kThreads, smem, s>>>(pa, P, H, N, g);
   return cudaGetLastError();
 }
 
@@ -350,6 +498,27 @@ __global__ void bwd_final_kernel(const float *__restrict__ dfq, const float *__r
   }
 }
 
+// Parts of the forward-recompute product and of the gradient products, and
+// the floats of their per-part records.
+struct BwdPlan {
+  int P_nd, P_g;
+  size_t rec_nd, rec_g0, rec_g1, rec_g2;
+};
+
+BwdPlan bwd_plan(int BH, int N, int D, int Dv) {
+  BwdPlan pl;
+  const int Dv4 = Dv + 4;
+  const int ny = ((D > Dv ? D : Dv) + kCs - 1) / kCs;
+  pl.P_nd = product_parts(static_cast<long long>(BH) * ((Dv4 + kCs - 1) / kCs), N);
+  pl.P_g = product_parts(static_cast<long long>(BH) * ny * 3, N);
+  const size_t bn = static_cast<size_t>(BH) * pl.P_nd, bg = static_cast<size_t>(BH) * pl.P_g;
+  pl.rec_nd = pl.P_nd > 1 ? bn * D * Dv4 : 0;
+  pl.rec_g0 = pl.P_g > 1 ? bg * Dv4 * D : 0;
+  pl.rec_g1 = pl.P_g > 1 ? bg * D * Dv : 0;
+  pl.rec_g2 = pl.rec_g0;
+  return pl;
+}
+
 template <int D, int DV, typename T>
 cudaError_t backward_typed(const Problem &p, const void *dO, void *dq, void *dk, void *dv,
                            const Gammas &g, float *ws, cudaStream_t s) {
@@ -359,6 +528,9 @@ cudaError_t backward_typed(const Problem &p, const void *dO, void *dq, void *dk,
   float *fq = ws, *fk = fq + rows * D, *vp = fk + rows * D, *vm = vp + rows * DV4,
         *nd = vm + rows * DV4, *gc = nd + rows * DV4, *gt = gc + rows * DV4,
         *dfq = gt + rows * DV, *dfk = dfq + rows * D, *dvf = dfk + rows * D;
+  const BwdPlan pl = bwd_plan(BH, p.N, D, DV);
+  float *rec_nd = dvf + rows * DV, *rec_g0 = rec_nd + pl.rec_nd, *rec_g1 = rec_g0 + pl.rec_g0,
+        *rec_g2 = rec_g1 + pl.rec_g1;
   cudaError_t e;
   {
     const int64_t n = rows * (D + DV + 4);
@@ -367,20 +539,37 @@ cudaError_t backward_typed(const Problem &p, const void *dO, void *dq, void *dk,
         fk, vp, vm, rows, D, DV);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = product_launch<D, DV4, false>(fq, fk, vp, nd, BH, p.H, p.N, g, s)) != cudaSuccess) return e;
+  if ((e = product_launch<D, DV4, false>(fq, fk, vp, nd, rec_nd, pl.P_nd, BH, p.H, p.N, g, s)) !=
+      cudaSuccess)
+    return e;
   bwd_mid_kernel<T><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, s>>>(
       nd, static_cast<const T *>(dO), gc, gt, rows, DV, p.eps);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
-    // dphi(q), dv and dphi(k) are independent: one launch, grid z selects
-    auto kern = gradient_products_kernel<D, DV>;
+    // dphi(q), dv and dphi(k) are independent: one launch per pass, grid z
+    // selects the product
     const size_t smem = ProdLayout<(DV4 > D ? DV4 : D)>::bytes;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+    const unsigned ny = ((D > DV ? D : DV) + kCs - 1) / kCs;
+    const ProdArgs a0{gc, vm, fk, dfq, rec_g0}, a1{fk, fq, gt, dvf, rec_g1},
+        a2{vm, gc, fq, dfk, rec_g2};
+    const int P = pl.P_g;
+    if (P > 1) {
+      auto ks = gradient_products_kernel<D, DV, kPassState>;
+      if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+        return e;
+      ks<<<dim3((unsigned)(BH * (P - 1)), ny, 3), kThreads, smem, s>>>(a0, a1, a2, P, p.H, p.N, g);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      constexpr int kMaxEntries = (DV4 * D > D * DV ? DV4 * D : D * DV);
+      gradient_scan_kernel<D, DV><<<dim3((unsigned)BH, (kMaxEntries + 255) / 256, 3), 256, 0, s>>>(
+          rec_g0, rec_g1, rec_g2, P, p.H, p.N, g);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    auto ko = gradient_products_kernel<D, DV, kPassOut>;
+    if ((e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
       return e;
-    const unsigned ny = ((D > DV ? D : DV) + kCs - 1) / kCs;
-    kern<<<dim3((unsigned)BH, ny, 3), kThreads, smem, s>>>(
-        ProdArgs{gc, vm, fk, dfq}, ProdArgs{fk, fq, gt, dvf}, ProdArgs{vm, gc, fq, dfk}, p.H, p.N, g);
+    ko<<<dim3((unsigned)(BH * P), ny, 3), kThreads, smem, s>>>(a0, a1, a2, P, p.H, p.N, g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -406,7 +595,14 @@ cudaError_t backward_shape(const Problem &p, const void *dO, void *dq, void *dk,
 
 size_t backward_workspace_bytes(int BH, int N, int D, int Dv) {
   const size_t rows = static_cast<size_t>(BH) * N;
-  return sizeof(float) * rows * (4 * static_cast<size_t>(D) + 4 * (Dv + 4) + 2 * Dv);
+  const BwdPlan pl = bwd_plan(BH, N, D, Dv);
+  return sizeof(float) * (rows * (4 * static_cast<size_t>(D) + 4 * (Dv + 4) + 2 * Dv) +
+                          pl.rec_nd + pl.rec_g0 + pl.rec_g1 + pl.rec_g2);
+}
+
+int backward_launches(int BH, int N, int D, int Dv) {
+  const BwdPlan pl = bwd_plan(BH, N, D, Dv);
+  return 3 + (pl.P_nd > 1 ? 3 : 1) + (pl.P_g > 1 ? 3 : 1);
 }
 
 cudaError_t launch_backward(const Problem &p, const void *dO, void *dq, void *dk, void *dv,

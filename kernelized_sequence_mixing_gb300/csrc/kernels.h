@@ -128,6 +128,7 @@ cudaError_t launch_favor_features(const void *q, const void *k, const void *W, v
 // from q, k, v of p and the upstream gradient dO [B*H][N][Dv]; fp32 on CUDA
 // cores in a workspace of backward_workspace_bytes().
 size_t backward_workspace_bytes(int BH, int N, int D, int Dv);
+int backward_launches(int BH, int N, int D, int Dv);  // kernels one call launches
 cudaError_t launch_backward(const Problem &p, const void *dO, void *dq, void *dk, void *dv,
                             const Gammas &g, void *ws, cudaStream_t s);
 

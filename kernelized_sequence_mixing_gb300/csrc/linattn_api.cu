@@ -487,4 +487,11 @@ la_status_t la_backward(const void *q, const void *k, const void *v, const void 
   return from_cuda(ef);
 }
 
+int la_backward_launches(int B, int H, int N, int D, int Dv) {
+  const la_status_t st = check_sizes(B, H, N, D, Dv, LA_F32);
+  if (st != LA_OK) return -static_cast<int>(st);
+  if ((int64_t)B * H * N == 0) return 0;
+  return backward_launches(B * H, N, D, Dv);
+}
+
 }  // extern "C"

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
-              "la_backward",
+              "la_backward", "la_backward_launches",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
