@@ -14,7 +14,8 @@
 // by TMA into a 3-stage ring (W is loaded once per CTA), warp 5 issues the
 // MMAs into one of two TMEM accumulators, warps 0-3 take |x|^2 of their row
 // from the staged tile and turn their row of U into phi:
-//   phi = exp2(u log2(e) - |x|^2 log2(e) / 2 - log2(r) / 2), rounded to bf16.
+//   phi = exp2(u log2(e) - |x|^2 log2(e) / 2 - log2(r) / 2), rounded to bf16,
+// staged per warp in 32 x 32 boxes and written by TMA tile stores.
 // fp32: the same map on CUDA cores in fp32 (the tensor cores' tf32 operands
 // would cost the exponent ~1e-3 of relative accuracy).
 #include "common.cuh"
@@ -41,9 +42,12 @@ struct FavorLayout {
   static constexpr int kXStage = (D / 64) * kXBox;
   static constexpr int kWBox = R * 128;            // 64 columns x R rows
   static constexpr int kW = (D / 64) * kWBox;
+  static constexpr int kStgBox = 32 * 64;          // 32 rows x 32 bf16, SW64
+  static constexpr int kStgWarp = (R / 32) * kStgBox;
   static constexpr int kOffW = 0;
   static constexpr int kOffX = kOffW + kW;
-  static constexpr int kOffBar = kOffX + kStages * kXStage;
+  static constexpr int kOffStg = kOffX + kStages * kXStage;  // phi staging, per warp
+  static constexpr int kOffBar = kOffStg + 4 * kStgWarp;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr int kTmemCols = 2 * R;              // two accumulators
@@ -52,7 +56,7 @@ struct FavorLayout {
 struct FavorParams {
   CUtensorMap tmX[2];  // rows of q, rows of k: [rows][D] bf16
   CUtensorMap tmW;     // [R][D] bf16
-  __nv_bfloat16 *out[2];
+  CUtensorMap tmO[2];  // phi of q, of k: [rows][R] bf16, 32 x 32 boxes, SW64
   unsigned int *timeouts;
   long long rows;  // rows of each input
   int tiles1;      // tiles per input
@@ -165,13 +169,15 @@ __global__ void __launch_bounds__(kThreads, 1) favor_tc_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ---------------- epilogue: warp w owns rows 32 w .. 32 w + 31 ----------------
+    // phi goes out through the warp's staging boxes (one per 32 columns) by
+    // TMA tile stores; rows past the end are clipped by the store itself
     const int r = 32 * warp + lane;
+    uint8_t *stg = sm + L::kOffStg + warp * L::kStgWarp;
     for (int j = 0; j < my; ++j) {
       const int s = j % kStages, b = j & 1;
       int which;
       long long row0;
       tile_of(j, &which, &row0);
-      const long long row = row0 + r;
       if (!warp_wait(&bar[kXFull + s], (j / kStages) & 1, abort_flag, p.timeouts)) break;
       // |x|^2 of the row from the staged tile (bf16 values, fp32 sums)
       float sq = 0.f;
@@ -194,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) favor_tc_kernel(const __grid_cons
       if (!warp_wait(&bar[kAccFull + b], (j >> 1) & 1, abort_flag, p.timeouts)) break;
       tc_fence_after();
       const float cst = fmaf(-0.5f * kLog2e, sq, p.cst);
-      __nv_bfloat16 *dst = p.out[which] + row * R;
+      if (lane == 0) bulk_wait_group_read0();  // the previous tile's stores have read stg
+      __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < R / 32; ++cc) {
         float x[32];
@@ -205,17 +212,26 @@ __global__ void __launch_bounds__(kThreads, 1) favor_tc_kernel(const __grid_cons
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(exp2f(fmaf(x[2 * i], kLog2e, cst)),
                               exp2f(fmaf(x[2 * i + 1], kLog2e, cst)));
-        if (row < p.rows) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * cc);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4 *>(stg + cc * L::kStgBox + sw64_off(lane, 16 * i)) =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
       tc_fence_before();
+      fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kAccEmpty + b]);
+      if (lane == 0) {
+        mbar_arrive(&bar[kAccEmpty + b]);
+        if (row0 + 32 * warp < p.rows) {  // a box past the last row is not stored
+#pragma unroll
+          for (int cc = 0; cc < R / 32; ++cc)
+            tma_store_3d(&p.tmO[which], stg + cc * L::kStgBox, 32 * cc,
+                         static_cast<int>(row0) + 32 * warp, 0);
+        }
+        bulk_commit_group();
+      }
     }
+    if (lane == 0) bulk_wait_group0();  // every store complete before the CTA exits
   }
   __syncwarp();
   tc_fence_before();
@@ -298,10 +314,10 @@ cudaError_t favor_tc_launch(const void *q, const void *k, const void *W, void *f
   prm.nin = k ? 2 : 1;
   if (!make_tmap_3d_bf16(&prm.tmX[0], q, D, rows, 1, 64, kRows, 128) ||
       !make_tmap_3d_bf16(&prm.tmX[1], k ? k : q, D, rows, 1, 64, kRows, 128) ||
-      !make_tmap_3d_bf16(&prm.tmW, W, D, R, 1, 64, R, 128))
+      !make_tmap_3d_bf16(&prm.tmW, W, D, R, 1, 64, R, 128) ||
+      !make_tmap_3d_bf16(&prm.tmO[0], fq, R, rows, 1, 32, 32, 64) ||
+      !make_tmap_3d_bf16(&prm.tmO[1], k ? fk : fq, R, rows, 1, 32, 32, 64))
     return cudaErrorInvalidValue;
-  prm.out[0] = static_cast<__nv_bfloat16 *>(fq);
-  prm.out[1] = static_cast<__nv_bfloat16 *>(fk);
   prm.timeouts = wait_timeout_counter();
   if (!prm.timeouts) return cudaErrorInvalidValue;
   prm.rows = rows;
