@@ -37,7 +37,7 @@ METRIC = ("causal linear-attn fwd tokens/s and % roofline "
 METRICS = {
     "noncausal": "non-causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
-    "gated": "gated linear-attn fwd tokens/s and % fp32 ALU roofline, 1×GB300",
+    "gated": "gated linear-attn fwd tokens/s and % roofline (HBM, or fp32 ALU on CUDA cores), 1×GB300",
     "favor": "Performer (FAVOR+) causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "backward": "causal linear-attn bwd (dq, dk, dv) tokens/s and % fp32 ALU roofline, 1×GB300",
 }
@@ -160,7 +160,7 @@ def measured_peaks():
 # sources the causal tensor-core kernel is compiled from
 KERNEL_SOURCES = ("chunk128.cu", "chunk_tc.cu", "tc_common.cuh", "common.cuh")
 # sources of the gated CUDA-core kernel
-GATED_SOURCES = ("gla_simt.cu", "common.cuh")
+GATED_SOURCES = ("gla_simt.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 # sources of the Performer path (feature kernel, then the causal kernel)
 FAVOR_SOURCES = ("favor.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 # sources of the backward pass
@@ -377,6 +377,7 @@ def run_ours(args, w):
     from kernelized_sequence_mixing_gb300.workloads import make_qkv
 
     ws, rank, local = dist_env()
+    gated_tc = False
     final_state = bool(getattr(args, "final_state", False))
     if final_state and (w.steps or not w.causal or w.gated or w.favor_r or w.backward):
         raise SystemExit("--final-state applies to the causal forward workloads")
@@ -426,11 +427,17 @@ def run_ours(args, w):
         ncopy = 1
         step_bytes = sum(t.numel() * t.element_size() for t in (qd, kd, vd, ad, od))
         assert step_bytes > L2_BYTES, "gated workloads are sized above L2"
-        # three launches whenever the sequence splits into parts, which the
-        # library does for every gated workload here (long sequences, fewer
-        # (b, h) x Dv-slice CTAs than two per SM)
+        # the CUDA-core form: three launches whenever the sequence splits into
+        # parts, which the library does for every gated workload here (long
+        # sequences, fewer (b, h) x Dv-slice CTAs than two per SM); the
+        # tensor-core form adds its prep kernel and the causal kernel in
+        # front (the CUDA-core launches then return at once unless some
+        # chunk forgot too hard)
         nsm = torch.cuda.get_device_properties(dev).multi_processor_count
         launches_per_step = 3 if w.B * w.H * (w.Dv // 32) < 2 * nsm and w.N > 64 else 1
+        gated_tc = la.gated_kernel(w.B, w.H, w.N, w.D, w.Dv, w.dtype) == "tensor-core"
+        if gated_tc:
+            launches_per_step += 2
 
         def step():
             la.forward_gated(qd, kd, vd, ad, eps=w.eps, out=od)
@@ -647,7 +654,8 @@ def run_ours(args, w):
                           (f"working set {byts / 1e6:.0f} MB < L2: steps rotate "
                            f"over {ncopy} input/output copies")),
         "roofline": roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src,
-                                   tc_peak, traffic, launches_per_step),
+                                   tc_peak, traffic, launches_per_step,
+                                   gated_tc=bool(w.gated and gated_tc)),
         "cpu_baseline": cpu,
         "e2e": None if e2e_s is None else {
             "value": tokens_rank * ws / e2e_s, "unit": "tokens/s",
@@ -661,7 +669,7 @@ def run_ours(args, w):
 
 
 def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traffic,
-                   launches):
+                   launches, gated_tc=False):
     """HBM roofline for the forward and decode kernels; for the gated
     CUDA-core kernel, the fp32 ALU roofline (its bound), with the HBM figure
     beside it.  Timed over the whole step (all of its launches)."""
@@ -669,7 +677,7 @@ def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traff
     tflops = flops / (launch_ms / 1e3) / 1e12
     hbm_src = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                else "fallback")
-    if w.gated or w.backward:
+    if (w.gated and not gated_tc) or w.backward:
         return {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
                 "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",

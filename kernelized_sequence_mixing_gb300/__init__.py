@@ -88,6 +88,8 @@ def load_library() -> ctypes.CDLL:
             lib.la_forward_favor.restype = I
             lib.la_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, FP, F, I, P]
             lib.la_backward.restype = I
+            lib.la_gated_kernel.argtypes = [I, I, I, I, I, I, I]
+            lib.la_gated_kernel.restype = I
             lib.la_backward_launches.argtypes = [I, I, I, I, I]
             lib.la_backward_launches.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
@@ -421,3 +423,13 @@ def backward_launches(B, H, N, D, Dv) -> int:
     if n < 0:
         raise LinAttnError("la_backward_launches", -n)
     return int(n)
+
+
+def gated_kernel(B, H, N, D, Dv, dtype=torch.bfloat16, want_state=False) -> str:
+    """Which form forward_gated runs: "tensor-core" (it still falls back to
+    the CUDA-core form at run time when some chunk's gates forget harder
+    than 2^-93) or "cuda-core".  Host-only query."""
+    code = load_library().la_gated_kernel(B, H, N, D, Dv, _DTYPES[dtype], 1 if want_state else 0)
+    if code < 0:
+        raise LinAttnError("la_gated_kernel", -code)
+    return "tensor-core" if code == 1 else "cuda-core"

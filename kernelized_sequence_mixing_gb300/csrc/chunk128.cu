@@ -140,6 +140,12 @@ struct Chunk128Params {
   // optional: the state after the last token, S [B*H][D][Dv] and z [B*H][D]
   // fp32, written by the CTA of the last part (nullptr: not written)
   float *S_out, *z_out;
+  // gated mode: the state is rescaled row by row at every chunk boundary by
+  // the chunk's gate products gate_prod [B*H][chunks][D] (q, k arrive
+  // already scaled); nonzero *skip: some chunk forgets too hard for this
+  // form, the launch does nothing
+  const float *gate_prod;
+  const int *skip;
   int BH, H, N, P;
   float eps;
   Gammas lg;  // log2(gamma) per head
@@ -191,8 +197,9 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t *v) {
   tmem_st16(taddr, f);
 }
 
-template <bool DECAY, bool IDENT>
+template <bool DECAY, bool IDENT, bool GATED = false>
 __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_constant__ Chunk128Params p) {
+  if (GATED && *p.skip) return;  // uniform: every thread reads the same flag
   constexpr size_t kRec = static_cast<size_t>(kD) * kDV + kD;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -630,7 +637,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
             !warp_wait(&bar[kInterDone], static_cast<uint32_t>((i - 1) & 1), abort_flag, p.timeouts))
           break;
         tc_fence_after();
-        const bool rebase = DECAY && (i % WC == 0);
+        const bool rebase = (DECAY && (i % WC == 0)) || GATED;
+        // gated: row d of T times the gate product of chunk i
+        const float fr =
+            GATED ? __ldg(p.gate_prod + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cb + i) * kD + d)
+                  : gW;
 #pragma unroll 1
         for (int cc = 0; cc < kDV / 32; cc += 2) {
           float x0[32], x1[32];
@@ -640,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           if (rebase) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              x0[e] *= gW;
-              x1[e] *= gW;
+              x0[e] *= fr;
+              x1[e] *= fr;
             }
             tmem_st32(tT + 32 * cc, x0);
             tmem_st32(tT + 32 * cc + 32, x1);
@@ -655,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           tmem_wait_ld();
           if (rebase) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x0[e] *= gW;
+            for (int e = 0; e < 16; ++e) x0[e] *= fr;
             tmem_st16(tT + kDV, x0);
           }
           put_sop16(sop, kSopAtom, kDV / 32, d, x0);
@@ -852,6 +863,35 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (err != cudaSuccess) return err;
   kern<<<BH * P, kThreads, kAlloc, s>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const int *skip,
+                                  cudaStream_t s) {
+  if (p.dtype != kBF16 || p.D != kD || p.Dv != kDV || p.N <= 0 || !p.ident) return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  Chunk128Params prm = {};
+  if (!make_tmap_3d_bf16(&prm.tmQ, p.q, kD, p.N, BH, 64, kC, 128) ||
+      !make_tmap_3d_bf16(&prm.tmK, p.k, kD, p.N, BH, 64, kC, 128) ||
+      !make_tmap_3d_bf16(&prm.tmV, p.v, kDV, p.N, BH, 64, kC, 128) ||
+      !make_tmap_3d_bf16(&prm.tmO, p.o, kDV, p.N, BH, 32, 32, 64))
+    return cudaErrorNotSupported;
+  prm.timeouts = wait_timeout_counter();
+  if (!prm.timeouts) return cudaErrorNotSupported;
+  prm.BH = BH;
+  prm.H = p.H;
+  prm.N = p.N;
+  prm.P = 1;  // one part per (batch, head): no phase A, no look-back
+  prm.eps = p.eps;
+  prm.gate_prod = gate_prod;
+  prm.skip = skip;
+  Gammas ones;
+  for (int h = 0; h < kMaxHeads; ++h) ones.g[h] = 1.f;
+  prm.lg = log2_gammas(ones, p.H, false);
+  auto kern = chunk128_kernel<false, true, true>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (err != cudaSuccess) return err;
+  kern<<<BH, kThreads, kAlloc, s>>>(prm);
   return cudaGetLastError();
 }
 

@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const T *__restrict__ v, const float *__restrict__ a,
                     T *__restrict__ o, float *__restrict__ rec,
                     float *__restrict__ S_out, float *__restrict__ z_out, int N,
-                    int P, int Pg, float eps) {
+                    int P, int Pg, float eps, const int *__restrict__ only_if) {
+  if (only_if && *only_if == 0) return;  // uniform: the tensor-core form ran
   constexpr int NG = D / 64;  // feature groups of 8 per warp
   constexpr int RD = D / 32;  // state rows per thread
   extern __shared__ float4 smem4[];
@@ -474,7 +475,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 // after part p, S_after(p) = g_p (.) S_after(p-1) + A_p (rows scaled by g_p).
 // grid: x = (batch, head), y = blocks over the D*Dv + D state entries.
 template <int D, int DV>
-__global__ void __launch_bounds__(256) gla_scan_kernel(float *__restrict__ rec, int P) {
+__global__ void __launch_bounds__(256) gla_scan_kernel(float *__restrict__ rec, int P,
+                                                      const int *__restrict__ only_if) {
+  if (only_if && *only_if == 0) return;
   constexpr size_t R = record_floats<D, DV>();
   const int i = blockIdx.y * blockDim.x + threadIdx.x;
   if (i >= D * DV + D) return;
@@ -498,7 +501,7 @@ int num_sms_gla() {
 
 template <int D, int DV, typename T>
 cudaError_t gla_typed(const Problem &p, const float *a, float *ws, int P, float *S_out,
-                      float *z_out, cudaStream_t s) {
+                      float *z_out, const int *only_if, cudaStream_t s) {
   const int BH = p.B * p.H;
   const size_t smem = GlaLayout<D>::bytes;
   auto kst = gla_simt_kernel<D, DV, kPassState, T>;
@@ -513,24 +516,67 @@ cudaError_t gla_typed(const Problem &p, const float *a, float *ws, int P, float 
   T *o = static_cast<T *>(p.o);
   if (P > 1) {
     kst<<<dim3((unsigned)(BH * (P - 1)), DV / kDvs), kThreads, smem, s>>>(
-        q, k, v, a, o, ws, nullptr, nullptr, p.N, P, P - 1, p.eps);
+        q, k, v, a, o, ws, nullptr, nullptr, p.N, P, P - 1, p.eps, only_if);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    gla_scan_kernel<D, DV><<<dim3((unsigned)BH, (D * DV + D + 255) / 256), 256, 0, s>>>(ws, P);
+    gla_scan_kernel<D, DV><<<dim3((unsigned)BH, (D * DV + D + 255) / 256), 256, 0, s>>>(ws, P,
+                                                                                      only_if);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   kout<<<dim3((unsigned)(BH * P), DV / kDvs), kThreads, smem, s>>>(
-      q, k, v, a, o, ws, S_out, z_out, p.N, P, P, p.eps);
+      q, k, v, a, o, ws, S_out, z_out, p.N, P, P, p.eps, only_if);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t gla_shape(const Problem &p, const float *a, float *ws, int P, float *S_out,
-                      float *z_out, cudaStream_t s) {
-  if (p.D == 64 && p.Dv == 64) return gla_typed<64, 64, T>(p, a, ws, P, S_out, z_out, s);
-  if (p.D == 64 && p.Dv == 128) return gla_typed<64, 128, T>(p, a, ws, P, S_out, z_out, s);
-  if (p.D == 128 && p.Dv == 64) return gla_typed<128, 64, T>(p, a, ws, P, S_out, z_out, s);
-  if (p.D == 128 && p.Dv == 128) return gla_typed<128, 128, T>(p, a, ws, P, S_out, z_out, s);
+                      float *z_out, const int *only_if, cudaStream_t s) {
+  if (p.D == 64 && p.Dv == 64) return gla_typed<64, 64, T>(p, a, ws, P, S_out, z_out, only_if, s);
+  if (p.D == 64 && p.Dv == 128) return gla_typed<64, 128, T>(p, a, ws, P, S_out, z_out, only_if, s);
+  if (p.D == 128 && p.Dv == 64) return gla_typed<128, 64, T>(p, a, ws, P, S_out, z_out, only_if, s);
+  if (p.D == 128 && p.Dv == 128) return gla_typed<128, 128, T>(p, a, ws, P, S_out, z_out, only_if, s);
   return cudaErrorNotSupported;
+}
+
+// The operands of the gated tensor-core form (D = 128): per 128-token chunk
+// and feature d, with the suffix products r_t = a_(t+1) ... a_(last token of
+// the chunk),
+//   qh_t = phi(q_t) / r_t,   kh_t = phi(k_t) r_t   (bf16),
+// and the chunk's gate product a_(first) ... a_(last) (fp32), so that within
+// a chunk qh_t . kh_s = sum_d phi(q_t)[d] phi(k_s)[d] prod_(u=s+1..t) a_u[d]
+// for s <= t, and the state carried from the previous chunk enters token t
+// as qh_t . (gate product) S.  A chunk whose gate product falls below 2^-93
+// in some feature (r_t could leave the bf16 range) sets *hard.
+// grid: (batch, head) x 128-token chunks, 64 threads; thread j owns
+// features 2j and 2j + 1 (4-byte bf16 pairs and 8-byte gate pairs, so every
+// warp access is a full 128-byte line).
+__global__ void __launch_bounds__(64)
+    gla_tc_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                       const float *__restrict__ a, __nv_bfloat16 *__restrict__ qh,
+                       __nv_bfloat16 *__restrict__ kh, float *__restrict__ gp,
+                       int *__restrict__ hard, int N) {
+  constexpr int kD128 = 128, kC128 = 128;
+  const int j = threadIdx.x;
+  const int nch = (N + kC128 - 1) / kC128;
+  const int64_t bh = blockIdx.x / nch;
+  const int c = static_cast<int>(blockIdx.x % nch);
+  const int c0 = c * kC128, nv = min(kC128, N - c0);
+  const int64_t base = (bh * N + c0) * kD128 + 2 * j;
+  float r0 = 1.f, r1 = 1.f;
+#pragma unroll 8
+  for (int t = nv - 1; t >= 0; --t) {
+    const int64_t off = base + static_cast<int64_t>(t) * kD128;
+    const float2 xq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(q + off));
+    const float2 xk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(k + off));
+    const float2 ga = *reinterpret_cast<const float2 *>(a + off);
+    *reinterpret_cast<__nv_bfloat162 *>(qh + off) =
+        __floats2bfloat162_rn(phi_f32(xq.x) / r0, phi_f32(xq.y) / r1);
+    *reinterpret_cast<__nv_bfloat162 *>(kh + off) =
+        __floats2bfloat162_rn(phi_f32(xk.x) * r0, phi_f32(xk.y) * r1);
+    r0 *= ga.x;
+    r1 *= ga.y;
+  }
+  *reinterpret_cast<float2 *>(gp + (bh * nch + c) * kD128 + 2 * j) = make_float2(r0, r1);
+  if (!(r0 >= 0x1p-93f) || !(r1 >= 0x1p-93f)) *hard = 1;
 }
 
 }  // namespace
@@ -566,11 +612,49 @@ size_t gla_workspace_bytes(int BH, int P, int D, int Dv) {
 }
 
 cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, float *S_out,
-                            float *z_out, cudaStream_t s) {
+                            float *z_out, cudaStream_t s, const int *only_if) {
   if (P < 1 || (P > 1 && !ws)) return cudaErrorInvalidValue;
   float *w = static_cast<float *>(ws);
-  return p.dtype == kF32 ? gla_shape<float>(p, a, w, P, S_out, z_out, s)
-                         : gla_shape<__nv_bfloat16>(p, a, w, P, S_out, z_out, s);
+  return p.dtype == kF32 ? gla_shape<float>(p, a, w, P, S_out, z_out, only_if, s)
+                         : gla_shape<__nv_bfloat16>(p, a, w, P, S_out, z_out, only_if, s);
+}
+
+bool gla_tc_supported(const Problem &p, bool want_state) {
+  return !want_state && p.dtype == kBF16 && p.D == 128 && p.Dv == 128 && p.N > 0 &&
+         static_cast<long long>(p.B) * p.H >= 8;
+}
+
+size_t gla_tc_workspace_bytes(int BH, int N) {
+  const size_t rows = static_cast<size_t>(BH) * N;
+  const size_t nch = (static_cast<size_t>(N) + 127) / 128;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return 256 + 2 * up(rows * 128 * 2) + up(static_cast<size_t>(BH) * nch * 128 * 4);
+}
+
+cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
+                          const int **hard_out) {
+  if (!gla_tc_supported(p, false)) return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  const size_t rows = static_cast<size_t>(BH) * p.N;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  int *hard = reinterpret_cast<int *>(w);
+  __nv_bfloat16 *qh = reinterpret_cast<__nv_bfloat16 *>(w + 256);
+  __nv_bfloat16 *kh = reinterpret_cast<__nv_bfloat16 *>(w + 256 + up(rows * 128 * 2));
+  float *gp = reinterpret_cast<float *>(w + 256 + 2 * up(rows * 128 * 2));
+  cudaError_t e = cudaMemsetAsync(hard, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  const int nch = (p.N + 127) / 128;
+  gla_tc_prep_kernel<<<(unsigned)(static_cast<long long>(BH) * nch), 64, 0, s>>>(
+      static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), a, qh, kh,
+      gp, hard, p.N);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  Problem pf = p;
+  pf.q = qh;
+  pf.k = kh;
+  pf.ident = true;
+  *hard_out = hard;
+  return launch_gated_chunk128(pf, gp, hard, s);
 }
 
 }  // namespace linattn

@@ -113,8 +113,22 @@ cudaError_t launch_decode_gated(const void *q, const void *k, const void *v, con
 // token, [B*H][D][Dv] and [B*H][D] fp32.
 int gla_parts(int BH, int N, int Dv);
 size_t gla_workspace_bytes(int BH, int P, int D, int Dv);
+// only_if (optional): the kernels do nothing unless *only_if is nonzero
 cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, float *S_out,
-                            float *z_out, cudaStream_t s);
+                            float *z_out, cudaStream_t s, const int *only_if = nullptr);
+// The gated tensor-core form (bf16, D = Dv = 128, no final state, B*H >= 8):
+// a prep kernel scales q, k per 128-token chunk by gate suffix products,
+// then the 128-token causal kernel runs with one part per (batch, head) and
+// rescales its state by each chunk's gate products.  *hard_out receives a
+// device flag that is nonzero when some chunk forgets too hard for this form
+// (the causal kernel then does nothing and the caller runs the CUDA-core
+// form with only_if = the flag).
+bool gla_tc_supported(const Problem &p, bool want_state);
+size_t gla_tc_workspace_bytes(int BH, int N);
+cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
+                          const int **hard_out);
+cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const int *skip,
+                                  cudaStream_t s);
 
 // Performer random-feature map (favor.cu): fq = phi(q), fk = phi(k) for
 // `rows` rows of q and k [rows][D], directions W [R][D], outputs [rows][R],

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
-              "la_backward", "la_backward_launches",
+              "la_backward", "la_backward_launches", "la_gated_kernel",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -217,6 +217,16 @@ def test_favor_rejects_bad_arguments(lib):
     assert call(causal=0, g=(ctypes.c_float * 2)(0.5, 1.0)) == INVALID
     assert call(eps=-1.0) == INVALID
     assert call(B=0, qq=None, kk=None, vv=None, WW=None, oo=None) == OK
+
+
+def test_gated_kernel_dispatch(lib):
+    Gk = lib.la_gated_kernel
+    assert Gk(2, 4, 1000, 128, 128, BF16, 0) == 1      # tensor cores
+    assert Gk(2, 4, 1000, 128, 128, BF16, 1) == 0      # final state wanted
+    assert Gk(1, 4, 1000, 128, 128, BF16, 0) == 0      # B*H < 8
+    assert Gk(2, 4, 1000, 64, 128, BF16, 0) == 0       # D = 64
+    assert Gk(2, 4, 1000, 128, 128, F32, 0) == 0       # fp32
+    assert Gk(2, 4, 1000, 96, 128, BF16, 0) == -UNSUPPORTED
 
 
 def test_backward_rejects_bad_arguments(lib):

@@ -36,6 +36,8 @@ def inputs(B, H, N, D, Dv, dtype, seed, gates):
     q, k, v = make_qkv(B, H, N, D, Dv, dtype, seed, 0.5)
     if gates == "mild":
         a = make_gates(B, H, N, D, seed + 1, 0.9, 1.0)
+    elif gates == "strong":     # per-chunk products down to ~2^-53, no fallback
+        a = make_gates(B, H, N, D, seed + 1, 0.5, 1.0)
     elif gates == "wide":       # strong forgetting: exact zeros and ones
         a = make_gates(B, H, N, D, seed + 1, 0.0, 1.0, zero_frac=0.01, one_frac=0.05)
     elif gates == "ones":
@@ -75,6 +77,33 @@ def test_gated_small(la, ora, dtype, gates, shape):
     assert state_error(to_np(S), S_ref) < 1e-4
     assert state_error(to_np(z)[..., None], z_ref[..., None]) < 1e-4
     # without the state the output is the same
+    o2 = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6)
+    assert torch.equal(o, o2)
+
+
+# The tensor-core form: bf16, D = Dv = 128, B*H >= 8, no final state.  Wide
+# gates (exact zeros) make it fall back to the CUDA-core form at run time.
+GATED_TC = [
+    (2, 4, 1000, 128, 128),
+    (1, 8, 333, 128, 128),
+    (4, 4, 128, 128, 128),
+    (1, 8, 1, 128, 128),
+    (2, 8, 4099, 128, 128),
+]
+
+
+@pytest.mark.parametrize("gates", ["mild", "strong", "ones", "wide"])
+@pytest.mark.parametrize("shape", GATED_TC, ids=lambda s: "x".join(map(str, s)))
+def test_gated_tensor_core(la, ora, gates, shape):
+    B, H, N, D, Dv = shape
+    assert la.gated_kernel(B, H, N, D, Dv) == "tensor-core"
+    assert la.gated_kernel(B, H, N, D, Dv, want_state=True) == "cuda-core"
+    q, k, v, a = inputs(B, H, N, D, Dv, torch.bfloat16, 13 * N + H, gates)
+    o = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6)
+    torch.cuda.synchronize()
+    ref = ora.gated(to_np(q), to_np(k), to_np(v), a.numpy(), eps=1e-6)
+    err = max_row_error(to_np(o), ref)
+    assert err < 2e-2, err
     o2 = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6)
     assert torch.equal(o, o2)
 
