@@ -125,10 +125,7 @@ enum Bar : int {
 // p >= 2 waits for the sums of all earlier parts, so the slowest phase A
 // sets the start of its phase C: equal parts keep those equal.
 __host__ __device__ __forceinline__ int part_begin(int p, int P, int nch_all) {
-  if (p <= 0) return 0;
-  if (p >= P) return nch_all;
-  const int base = nch_all / P, rem = nch_all % P;
-  return p * base + (p < rem ? p : rem);
+  return chunk_part_begin(p, P, nch_all);
 }
 
 struct Chunk128Params {
@@ -145,6 +142,9 @@ struct Chunk128Params {
   // already scaled); nonzero *skip: some chunk forgets too hard for this
   // form, the launch does nothing
   const float *gate_prod;
+  // gated, P > 1: gate_suf [B*H][chunks][D], the product of gate_prod over
+  // the later chunks of the same part; gate_part [B*H][P][D], over a whole part
+  const float *gate_suf, *gate_part;
   const int *skip;
   int BH, H, N, P;
   float eps;
@@ -181,6 +181,29 @@ __device__ __forceinline__ void map_row4(uint8_t *box, int r, int c0, uint32_t s
     x[c].z = feat_scale_bf16x2<IDENT>(x[c].z, sc);
     x[c].w = feat_scale_bf16x2<IDENT>(x[c].w, sc);
     *reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * (c0 + c))) = x[c];
+  }
+}
+
+// Per-feature factors on chunks [c0, c0 + 4) of row r of a box (features
+// 8 (c0 + c) + j of the box, factors F[8 c + j]); a row past the sequence end
+// becomes 0.
+__device__ __forceinline__ void map_row4_feat(uint8_t *box, int r, int c0, const float *F,
+                                              bool valid) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * (c0 + c)));
+    uint4 x = *ptr;
+    if (valid) {
+      const float4 f0 = *reinterpret_cast<const float4 *>(F + 8 * c);
+      const float4 f1 = *reinterpret_cast<const float4 *>(F + 8 * c + 4);
+      x.x = feat_scale_bf16x2<true>(x.x, pack_bf16x2(f0.x, f0.y));
+      x.y = feat_scale_bf16x2<true>(x.y, pack_bf16x2(f0.z, f0.w));
+      x.z = feat_scale_bf16x2<true>(x.z, pack_bf16x2(f1.x, f1.y));
+      x.w = feat_scale_bf16x2<true>(x.w, pack_bf16x2(f1.z, f1.w));
+    } else {
+      x = make_uint4(0u, 0u, 0u, 0u);
+    }
+    *ptr = x;
   }
 }
 
@@ -299,8 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int sl = i & 1, ia = phase_a_chunk(i);
       if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
       const int nv = min(kC, N - (cbA + ia) * kC);
-      const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
-      map_row4<IDENT>(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
+      if (GATED) {
+        // k-hat already carries the gates up to its chunk's end; the later
+        // chunks of the previous part add their products, feature by feature
+        const float *F = p.gate_suf + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cbA + ia) * kD +
+                         64 * (quarter >> 1) + 32 * (quarter & 1);
+        map_row4_feat(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), F,
+                      r < nv);
+      } else {
+        const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
+        map_row4<IDENT>(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
+      }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kKMapped + sl]);
@@ -361,9 +393,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         }
       }
       named_sync(1, 512);
-      for (int j = 0; j < part - 1 && !*abort_flag; ++j) {
+      // gated: the weight of A_j is the product of the whole-part gate
+      // products of parts j + 1 .. part - 1, built up from j = part - 2 down
+      float wg = 1.f;
+      for (int jj = 0; jj < part - 1 && !*abort_flag; ++jj) {
+        const int j = GATED ? part - 2 - jj : jj;
+        if (GATED) wg *= __ldg(p.gate_part + (static_cast<size_t>(bh) * P + j + 1) * kD + d);
         const float wj =
-            DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1, P, nch_all)) * kC) * lg) : 1.f;
+            GATED ? wg
+                  : (DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1, P, nch_all)) * kC) * lg)
+                           : 1.f);
         const float *rec = p.rec + (static_cast<size_t>(bh) * P + j) * kRec;
         float4 v[8];
 #pragma unroll
@@ -379,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         accz = fmaf(wj, vz, accz);
       }
     }
-    const float gW = DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f;
+    // to the end of the first window (decay) or of the first chunk (gated)
+    const float gW = GATED ? __ldg(p.gate_prod + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cb) * kD + d)
+                           : (DECAY ? exp2f(static_cast<float>(W) * lg) : 1.f);
 #pragma unroll
     for (int e = 0; e < 32; ++e) acc[e] *= gW;
     tmem_st32(tS, acc);
@@ -866,9 +907,11 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const int *skip,
+cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const float *gate_suf,
+                                  const float *gate_part, const int *skip, void *ws, int P,
                                   cudaStream_t s) {
-  if (p.dtype != kBF16 || p.D != kD || p.Dv != kDV || p.N <= 0 || !p.ident) return cudaErrorNotSupported;
+  if (p.dtype != kBF16 || p.D != kD || p.Dv != kDV || p.N <= 0 || !p.ident || P < 1)
+    return cudaErrorNotSupported;
   const int BH = p.B * p.H;
   Chunk128Params prm = {};
   if (!make_tmap_3d_bf16(&prm.tmQ, p.q, kD, p.N, BH, 64, kC, 128) ||
@@ -881,17 +924,28 @@ cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, cons
   prm.BH = BH;
   prm.H = p.H;
   prm.N = p.N;
-  prm.P = 1;  // one part per (batch, head): no phase A, no look-back
+  prm.P = P;
   prm.eps = p.eps;
   prm.gate_prod = gate_prod;
+  prm.gate_suf = gate_suf;
+  prm.gate_part = gate_part;
   prm.skip = skip;
+  if (P > 1) {
+    if (!ws || !gate_suf || !gate_part) return cudaErrorInvalidValue;
+    // flags and ticket start at zero; the records need no initialisation
+    prm.ws_flag = static_cast<int *>(ws);
+    prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;
+    prm.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + flag_bytes(BH, P));
+    cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
   Gammas ones;
   for (int h = 0; h < kMaxHeads; ++h) ones.g[h] = 1.f;
   prm.lg = log2_gammas(ones, p.H, false);
   auto kern = chunk128_kernel<false, true, true>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (err != cudaSuccess) return err;
-  kern<<<BH, kThreads, kAlloc, s>>>(prm);
+  kern<<<BH * P, kThreads, kAlloc, s>>>(prm);
   return cudaGetLastError();
 }
 

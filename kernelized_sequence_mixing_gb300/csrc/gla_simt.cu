@@ -619,6 +619,28 @@ cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, f
                          : gla_shape<__nv_bfloat16>(p, a, w, P, S_out, z_out, only_if, s);
 }
 
+// The gate tables of the part split (P parts of the 128-token kernel): per
+// chunk c of part q, gsuf[c] = product of gp over the chunks after c in q;
+// gpart[q] = product of gp over q.  grid: (batch, head) x P, thread d owns
+// feature d.
+__global__ void __launch_bounds__(128)
+    gla_tc_tables_kernel(const float *__restrict__ gp, float *__restrict__ gsuf,
+                         float *__restrict__ gpart, int N, int P) {
+  constexpr int kD128 = 128;
+  const int d = threadIdx.x;
+  const int nch = (N + 127) / 128;
+  const int64_t bh = blockIdx.x / P;
+  const int q = static_cast<int>(blockIdx.x % P);
+  const int cb = chunk_part_begin(q, P, nch), ce = chunk_part_begin(q + 1, P, nch);
+  float suf = 1.f;
+  for (int c = ce - 1; c >= cb; --c) {
+    const size_t i = (static_cast<size_t>(bh) * nch + c) * kD128 + d;
+    gsuf[i] = suf;
+    suf *= gp[i];
+  }
+  gpart[(static_cast<size_t>(bh) * P + q) * kD128 + d] = suf;
+}
+
 bool gla_tc_supported(const Problem &p, bool want_state) {
   return !want_state && p.dtype == kBF16 && p.D == 128 && p.Dv == 128 && p.N > 0 &&
          static_cast<long long>(p.B) * p.H >= 8;
@@ -627,8 +649,10 @@ bool gla_tc_supported(const Problem &p, bool want_state) {
 size_t gla_tc_workspace_bytes(int BH, int N) {
   const size_t rows = static_cast<size_t>(BH) * N;
   const size_t nch = (static_cast<size_t>(N) + 127) / 128;
+  const int P = chunk128_parts(BH, N);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return 256 + 2 * up(rows * 128 * 2) + up(static_cast<size_t>(BH) * nch * 128 * 4);
+  return 256 + 2 * up(rows * 128 * 2) + 2 * up(static_cast<size_t>(BH) * nch * 128 * 4) +
+         up(static_cast<size_t>(BH) * P * 128 * 4) + up(chunk128_workspace_bytes(BH, P));
 }
 
 cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
@@ -641,20 +665,30 @@ cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream
   int *hard = reinterpret_cast<int *>(w);
   __nv_bfloat16 *qh = reinterpret_cast<__nv_bfloat16 *>(w + 256);
   __nv_bfloat16 *kh = reinterpret_cast<__nv_bfloat16 *>(w + 256 + up(rows * 128 * 2));
+  const int nch = (p.N + 127) / 128;
+  const size_t ntab = up(static_cast<size_t>(BH) * nch * 128 * 4);
+  const int P = chunk128_parts(BH, p.N);
   float *gp = reinterpret_cast<float *>(w + 256 + 2 * up(rows * 128 * 2));
+  float *gsuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(gp) + ntab);
+  float *gpart = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(gsuf) + ntab);
+  void *cws = reinterpret_cast<uint8_t *>(gpart) + up(static_cast<size_t>(BH) * P * 128 * 4);
   cudaError_t e = cudaMemsetAsync(hard, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
-  const int nch = (p.N + 127) / 128;
   gla_tc_prep_kernel<<<(unsigned)(static_cast<long long>(BH) * nch), 64, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), a, qh, kh,
       gp, hard, p.N);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (P > 1) {
+    gla_tc_tables_kernel<<<(unsigned)(static_cast<long long>(BH) * P), 128, 0, s>>>(gp, gsuf, gpart,
+                                                                                   p.N, P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   Problem pf = p;
   pf.q = qh;
   pf.k = kh;
   pf.ident = true;
   *hard_out = hard;
-  return launch_gated_chunk128(pf, gp, hard, s);
+  return launch_gated_chunk128(pf, gp, gsuf, gpart, hard, cws, P, s);
 }
 
 }  // namespace linattn

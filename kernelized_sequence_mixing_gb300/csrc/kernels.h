@@ -26,6 +26,15 @@ struct Problem {
   bool ident = false;
 };
 
+// First chunk of part p when nch chunks split into P equal parts (the
+// 128-token kernel's split; the gated form's gate tables follow it).
+__host__ __device__ inline int chunk_part_begin(int p, int P, int nch) {
+  if (p <= 0) return 0;
+  if (p >= P) return nch;
+  const int base = nch / P, rem = nch % P;
+  return p * base + (p < rem ? p : rem);
+}
+
 // Causal forward on CUDA cores (fp32 FFMA): any dtype.
 cudaError_t launch_causal_simt(const Problem &p, const Gammas &g,
                                cudaStream_t s);
@@ -127,7 +136,9 @@ bool gla_tc_supported(const Problem &p, bool want_state);
 size_t gla_tc_workspace_bytes(int BH, int N);
 cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
                           const int **hard_out);
-cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const int *skip,
+// gate_suf / gate_part: see gla_tc (P > 1); ws: chunk128_workspace_bytes(BH, P)
+cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const float *gate_suf,
+                                  const float *gate_part, const int *skip, void *ws, int P,
                                   cudaStream_t s);
 
 // Performer random-feature map (favor.cu): fq = phi(q), fk = phi(k) for
