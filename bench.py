@@ -37,6 +37,7 @@ METRIC = ("causal linear-attn fwd tokens/s and % roofline "
 METRICS = {
     "noncausal": "non-causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "decode": "recurrent decode step tokens/s and % HBM roofline, 1×GB300",
+    "decode_gated": "gated recurrent decode step tokens/s and % HBM roofline, 1×GB300",
     "gated": "gated linear-attn fwd tokens/s and % roofline (HBM, or fp32 ALU on CUDA cores), 1×GB300",
     "favor": "Performer (FAVOR+) causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
     "backward": "causal linear-attn bwd (dq, dk, dv) tokens/s and % fp32 ALU roofline, 1×GB300",
@@ -45,7 +46,7 @@ METRICS = {
 
 def workload_metric(w):
     if w.steps:
-        return METRICS["decode"]
+        return METRICS["decode_gated"] if w.gated else METRICS["decode"]
     if w.gated:
         return METRICS["gated"]
     if w.favor_r:
@@ -112,6 +113,9 @@ def decode_work(w):
     units = w.B * w.H
     byts = units * (2 * 4 * (w.D * w.Dv + w.D) + (2 * w.D + 2 * w.Dv) * es)
     flops = units * (4 * w.D * w.Dv + 3 * w.D + w.Dv)
+    if w.gated:  # the fp32 gates read once; one more multiply per state entry
+        byts += units * w.D * 4
+        flops += units * (w.D * w.Dv + w.D)
     return byts, flops
 
 
@@ -291,7 +295,8 @@ def time_oracle(w, heads_per_pass, passes):
 
 def time_oracle_decode(w, units, passes):
     """The oracle's decode step on the first `units` (sequence, head) units,
-    from a zero state (the work per step does not depend on the state)."""
+    from a zero state (the work per step does not depend on the state); for
+    the gated workload, one step of the oracle's gated recurrence."""
     import numpy as np
     import oracle
     from kernelized_sequence_mixing_gb300.workloads import decode_step_inputs
@@ -302,9 +307,16 @@ def time_oracle_decode(w, units, passes):
     z = np.zeros((units, w.D))
     threads = oracle.default_threads()
     times = []
+    if w.gated:
+        from kernelized_sequence_mixing_gb300.workloads import decode_step_gates
+        ag = decode_step_gates(w, 0).reshape(-1, w.D)[:units].numpy()[:, None, :]
     for _ in range(passes):
         t0 = time.perf_counter()
-        oracle.decode_step(q, k, v, S, z, eps=w.eps, nthreads=threads)
+        if w.gated:
+            oracle.gated(q[:, None, :], k[:, None, :], v[:, None, :], ag, eps=w.eps,
+                         nthreads=threads)
+        else:
+            oracle.decode_step(q, k, v, S, z, eps=w.eps, nthreads=threads)
         times.append(time.perf_counter() - t0)
     # a token is one position of one sequence across all H heads
     return units / w.H, times, threads
@@ -353,7 +365,8 @@ def workload_config(w):
     if w.decayed:
         cfg["gamma"] = "per head 1 - 2^(-5 - h/4)"
     if w.gated:
-        cfg["gates"] = (f"fp32 a [B][H][N][D] uniform in [{w.gate_lo}, 1), one per key "
+        cfg["gates"] = (f"fp32 a [B][H][D] per step, uniform in [{w.gate_lo}, 1)" if w.steps else
+                        f"fp32 a [B][H][N][D] uniform in [{w.gate_lo}, 1), one per key "
                         "feature and token")
     if w.backward:
         cfg["pass"] = "backward: dq, dk, dv from q, k, v and dL/do ~ N(0, 1)"
@@ -363,7 +376,8 @@ def workload_config(w):
     if w.steps:
         cfg.update(seq_len=1, prefill_len=w.N, state="fp32 S [D][Dv] and z [D] "
                    "per (sequence, head), from the prefill",
-                   step="one la_decode_step over all B*H units")
+                   step=("one la_decode_gated" if w.gated else "one la_decode_step") +
+                   " over all B*H units")
     return cfg
 
 
@@ -405,14 +419,25 @@ def run_ours(args, w):
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         od = torch.empty((w.B, w.H, w.Dv), dtype=w.dtype, device=dev)
         launches_per_step = 1
+        if w.gated:
+            # gated: a fresh fp32 gate per key feature; the prefill above is
+            # the ungated state (the work of a step does not depend on it)
+            from kernelized_sequence_mixing_gb300.workloads import decode_step_gates
+            a = decode_step_gates(w, 7919 * rank)
+            ad = a.to(dev)
 
-        def step():
-            la.decode_step(qd, kd, vd, S, z, gamma=g, eps=w.eps, out=od)
+            def step():
+                la.decode_gated(qd, kd, vd, ad, S, z, eps=w.eps, out=od)
+        else:
+            def step():
+                la.decode_step(qd, kd, vd, S, z, gamma=g, eps=w.eps, out=od)
 
-        def e2e_step(qh, kh, vh, oh):
+        def e2e_step(qh, kh, vh, oh, ah=None):
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
             vd.copy_(vh, non_blocking=True)
+            if ah is not None:
+                ad.copy_(ah, non_blocking=True)
             step()
             oh.copy_(od, non_blocking=True)
         tokens_rank = w.B
@@ -677,7 +702,7 @@ def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traff
     tflops = flops / (launch_ms / 1e3) / 1e12
     hbm_src = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                else "fallback")
-    if (w.gated and not gated_tc) or w.backward:
+    if (w.gated and not w.steps and not gated_tc) or w.backward:
         return {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
                 "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",

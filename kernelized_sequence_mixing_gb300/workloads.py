@@ -94,6 +94,11 @@ WORKLOADS = {
     # shape of the causal configurations), gamma = 1
     "backward_bf16_n4096": Workload("backward_bf16_n4096", True, 4, 8, 4096, 64, 64,
                                     torch.bfloat16, 0.5, 7, backward=True),
+    # gated decode: the decode workload's shape, a fresh fp32 gate per step
+    # and key feature, U[0.9, 1) (seed of step t: 1000 + t + 50000)
+    "decode_gated_bf16_h32": Workload("decode_gated_bf16_h32", True, 256, 32, 512, 128,
+                                      128, torch.bfloat16, 0.5, 4, steps=1024,
+                                      step_seed0=1000, gated=True),
     "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
                                 128, torch.bfloat16, 0.5, 4, steps=1024,
                                 step_seed0=1000),
@@ -188,3 +193,9 @@ def workload_upstream(w: Workload, device="cpu"):
     g = torch.Generator(device="cpu")
     g.manual_seed(int(w.seed + 3))
     return torch.randn((w.B, w.H, w.N, w.Dv), generator=g).to(w.dtype).to(device)
+
+
+def decode_step_gates(w: Workload, t: int, device="cpu"):
+    """The gates a: [B, H, D] fp32 of gated decode step t."""
+    return make_gates(w.B, w.H, 1, w.D, w.step_seed0 + t + 50000, w.gate_lo, 1.0,
+                      device=device)[:, :, 0].contiguous()

@@ -189,3 +189,31 @@ def test_gated_bf16_n16384_sampled_heads(la, ora):
                         eps=w.eps)
         err = max_row_error(to_np(o[b, h]), ref)
         assert err < 2e-2, (b, h, err)
+
+
+def test_decode_gated_h32_full_sampled(la, ora):
+    """The gated decode workload's shape (256 sequences x H32, D = Dv = 128),
+    from a zero state: M gated steps over all units, sampled units followed
+    by the oracle's gated recurrence over the same M tokens."""
+    from kernelized_sequence_mixing_gb300.workloads import (
+        WORKLOADS, decode_step_gates, decode_step_inputs)
+    w = WORKLOADS["decode_gated_bf16_h32"]
+    M = 6
+    S = torch.zeros((w.B, w.H, w.D, w.Dv), dtype=torch.float32, device="cuda")
+    z = torch.zeros((w.B, w.H, w.D), dtype=torch.float32, device="cuda")
+    units = [(0, 0), (77, 13), (255, 31)]
+    qs, ks, vs, as_, outs = [], [], [], [], []
+    for t in range(M):
+        q, k, v = decode_step_inputs(w, t)
+        a = decode_step_gates(w, t)
+        o = la.decode_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), S, z, eps=w.eps)
+        qs.append(q); ks.append(k); vs.append(v); as_.append(a); outs.append(o.cpu())
+    torch.cuda.synchronize()
+    for b, h in units:
+        seq = lambda xs: np.stack([to_np(x[b, h]) for x in xs])  # noqa: E731
+        ref, S_ref, z_ref = ora.gated(seq(qs), seq(ks), seq(vs), seq(as_), eps=w.eps,
+                                      return_state=True)
+        got = seq(outs)
+        assert max_row_error(got, ref) < 2e-2
+        assert state_error(to_np(S[b, h]), S_ref) < 1e-4
+        assert state_error(to_np(z[b, h])[None], z_ref[None]) < 1e-4
