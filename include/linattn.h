@@ -157,8 +157,8 @@ LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
  * values: outside [0, 1] the result is unspecified, a NaN gate gives NaN
  * outputs).  S: [B][H][D][Dv] fp32 and z: [B][H][D] fp32 are both NULL or
  * both set; when set they receive the state after the last token (zero for
- * N = 0).  fp32 arithmetic on CUDA cores, or for bf16 with D = Dv = 128,
- * no state and B*H >= 8 the tensor-core form described at la_gated_kernel
+ * N = 0).  fp32 arithmetic on CUDA cores, or for bf16 with D = Dv = 128
+ * and B*H >= 8 the tensor-core form described at la_gated_kernel
  * (bf16 operands, fp32 accumulation and state).  A workspace of about
  * B*H*(P-1)*(D*Dv + 2D)*4 bytes (P <= ceil(N/64) parts), plus for the
  * tensor-core form 2*B*H*N*D*2 + B*H*ceil(N/128)*D*4 bytes, is taken with
@@ -172,7 +172,8 @@ LA_API la_status_t la_forward_gated(const void *q, const void *k, const void *v,
 
 /*
  * Which form la_forward_gated runs for these arguments: 1 = tensor cores
- * (bf16, D = Dv = 128, no final state, B*H >= 8: q and k scaled per
+ * (bf16, D = Dv = 128, B*H >= 8, with or without the final state, which
+ * want_state no longer changes: q and k scaled per
  * 128-token chunk by gate suffix products, then the 128-token causal kernel
  * with its state rescaled by each chunk's gate products; a call whose gates
  * forget harder than 2^-93 within some chunk and feature falls back at run

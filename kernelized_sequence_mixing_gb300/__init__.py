@@ -428,7 +428,8 @@ def backward_launches(B, H, N, D, Dv) -> int:
 def gated_kernel(B, H, N, D, Dv, dtype=torch.bfloat16, want_state=False) -> str:
     """Which form forward_gated runs: "tensor-core" (it still falls back to
     the CUDA-core form at run time when some chunk's gates forget harder
-    than 2^-93) or "cuda-core".  Host-only query."""
+    than 2^-93) or "cuda-core"; the final state does not change the choice.
+    Host-only query."""
     code = load_library().la_gated_kernel(B, H, N, D, Dv, _DTYPES[dtype], 1 if want_state else 0)
     if code < 0:
         raise LinAttnError("la_gated_kernel", -code)

@@ -909,7 +909,7 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
 
 cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const float *gate_suf,
                                   const float *gate_part, const int *skip, void *ws, int P,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, float *S_out, float *z_out) {
   if (p.dtype != kBF16 || p.D != kD || p.Dv != kDV || p.N <= 0 || !p.ident || P < 1)
     return cudaErrorNotSupported;
   const int BH = p.B * p.H;
@@ -930,6 +930,10 @@ cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, cons
   prm.gate_suf = gate_suf;
   prm.gate_part = gate_part;
   prm.skip = skip;
+  // the state after the last token: T after the last chunk is relative to
+  // that chunk's last token, N - 1, so it is written as it is
+  prm.S_out = S_out;
+  prm.z_out = z_out;
   if (P > 1) {
     if (!ws || !gate_suf || !gate_part) return cudaErrorInvalidValue;
     // flags and ticket start at zero; the records need no initialisation

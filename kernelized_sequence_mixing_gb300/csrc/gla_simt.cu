@@ -641,8 +641,8 @@ __global__ void __launch_bounds__(128)
   gpart[(static_cast<size_t>(bh) * P + q) * kD128 + d] = suf;
 }
 
-bool gla_tc_supported(const Problem &p, bool want_state) {
-  return !want_state && p.dtype == kBF16 && p.D == 128 && p.Dv == 128 && p.N > 0 &&
+bool gla_tc_supported(const Problem &p) {
+  return p.dtype == kBF16 && p.D == 128 && p.Dv == 128 && p.N > 0 &&
          static_cast<long long>(p.B) * p.H >= 8;
 }
 
@@ -656,8 +656,8 @@ size_t gla_tc_workspace_bytes(int BH, int N) {
 }
 
 cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
-                          const int **hard_out) {
-  if (!gla_tc_supported(p, false)) return cudaErrorNotSupported;
+                          const int **hard_out, float *S_out, float *z_out) {
+  if (!gla_tc_supported(p)) return cudaErrorNotSupported;
   const int BH = p.B * p.H;
   const size_t rows = static_cast<size_t>(BH) * p.N;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -688,7 +688,7 @@ cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream
   pf.k = kh;
   pf.ident = true;
   *hard_out = hard;
-  return launch_gated_chunk128(pf, gp, gsuf, gpart, hard, cws, P, s);
+  return launch_gated_chunk128(pf, gp, gsuf, gpart, hard, cws, P, s, S_out, z_out);
 }
 
 }  // namespace linattn

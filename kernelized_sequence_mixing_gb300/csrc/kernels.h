@@ -125,21 +125,22 @@ size_t gla_workspace_bytes(int BH, int P, int D, int Dv);
 // only_if (optional): the kernels do nothing unless *only_if is nonzero
 cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, float *S_out,
                             float *z_out, cudaStream_t s, const int *only_if = nullptr);
-// The gated tensor-core form (bf16, D = Dv = 128, no final state, B*H >= 8):
+// The gated tensor-core form (bf16, D = Dv = 128, B*H >= 8; S_out, z_out
+// optional, the state after the last token):
 // a prep kernel scales q, k per 128-token chunk by gate suffix products,
 // then the 128-token causal kernel runs with one part per (batch, head) and
 // rescales its state by each chunk's gate products.  *hard_out receives a
 // device flag that is nonzero when some chunk forgets too hard for this form
 // (the causal kernel then does nothing and the caller runs the CUDA-core
 // form with only_if = the flag).
-bool gla_tc_supported(const Problem &p, bool want_state);
+bool gla_tc_supported(const Problem &p);
 size_t gla_tc_workspace_bytes(int BH, int N);
 cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream_t s,
-                          const int **hard_out);
+                          const int **hard_out, float *S_out = nullptr, float *z_out = nullptr);
 // gate_suf / gate_part: see gla_tc (P > 1); ws: chunk128_workspace_bytes(BH, P)
 cudaError_t launch_gated_chunk128(const Problem &p, const float *gate_prod, const float *gate_suf,
                                   const float *gate_part, const int *skip, void *ws, int P,
-                                  cudaStream_t s);
+                                  cudaStream_t s, float *S_out = nullptr, float *z_out = nullptr);
 
 // Performer random-feature map (favor.cu): fq = phi(q), fk = phi(k) for
 // `rows` rows of q and k [rows][D], directions W [R][D], outputs [rows][R],

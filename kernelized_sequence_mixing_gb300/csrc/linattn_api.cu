@@ -358,7 +358,7 @@ la_status_t la_forward_gated(const void *q, const void *k, const void *v, const 
   const Problem p{q, k, v, o, B, H, N, D, Dv, false, eps, dtype == LA_F32 ? kF32 : kBF16};
   const int P = gla_parts(BH, N, Dv);
   const size_t wsb_simt = (gla_workspace_bytes(BH, P, D, Dv) + 255) & ~(size_t)255;
-  const bool tc = gla_tc_supported(p, S != nullptr);
+  const bool tc = gla_tc_supported(p);
   const size_t wsb = wsb_simt + (tc ? gla_tc_workspace_bytes(BH, N) : 0);
   void *ws = nullptr;
   if (wsb && cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
@@ -367,7 +367,7 @@ la_status_t la_forward_gated(const void *q, const void *k, const void *v, const 
   if (tc) {
     // tensor cores; the CUDA-core form runs after it only if some chunk
     // forgot too hard for the scaled operands (a device flag decides)
-    e = launch_gla_tc(p, a, static_cast<uint8_t *>(ws) + wsb_simt, s, &hard);
+    e = launch_gla_tc(p, a, static_cast<uint8_t *>(ws) + wsb_simt, s, &hard, S, z);
   }
   if (e == cudaSuccess) e = launch_gla_simt(p, a, ws, P, S, z, s, hard);
   cudaError_t ef = ws ? cudaFreeAsync(ws, s) : cudaSuccess;
@@ -380,7 +380,8 @@ int la_gated_kernel(int B, int H, int N, int D, int Dv, la_dtype_t dtype, int wa
   if (st != LA_OK) return -static_cast<int>(st);
   const Problem p{nullptr, nullptr, nullptr, nullptr, B, H, N, D, Dv, false, 0.f,
                   dtype == LA_F32 ? kF32 : kBF16};
-  return gla_tc_supported(p, want_state != 0) ? 1 : 0;
+  (void)want_state;  // the tensor-core form writes the final state as well
+  return gla_tc_supported(p) ? 1 : 0;
 }
 
 la_status_t la_decode_gated(const void *q, const void *k, const void *v, const float *a,

@@ -222,7 +222,7 @@ def test_favor_rejects_bad_arguments(lib):
 def test_gated_kernel_dispatch(lib):
     Gk = lib.la_gated_kernel
     assert Gk(2, 4, 1000, 128, 128, BF16, 0) == 1      # tensor cores
-    assert Gk(2, 4, 1000, 128, 128, BF16, 1) == 0      # final state wanted
+    assert Gk(2, 4, 1000, 128, 128, BF16, 1) == 1      # with the final state too
     assert Gk(1, 4, 1000, 128, 128, BF16, 0) == 0      # B*H < 8
     assert Gk(2, 4, 1000, 64, 128, BF16, 0) == 0       # D = 64
     assert Gk(2, 4, 1000, 128, 128, F32, 0) == 0       # fp32

@@ -97,15 +97,23 @@ GATED_TC = [
 def test_gated_tensor_core(la, ora, gates, shape):
     B, H, N, D, Dv = shape
     assert la.gated_kernel(B, H, N, D, Dv) == "tensor-core"
-    assert la.gated_kernel(B, H, N, D, Dv, want_state=True) == "cuda-core"
+    assert la.gated_kernel(B, H, N, D, Dv, want_state=True) == "tensor-core"
     q, k, v, a = inputs(B, H, N, D, Dv, torch.bfloat16, 13 * N + H, gates)
     o = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6)
     torch.cuda.synchronize()
-    ref = ora.gated(to_np(q), to_np(k), to_np(v), a.numpy(), eps=1e-6)
+    ref, S_ref, z_ref = ora.gated(to_np(q), to_np(k), to_np(v), a.numpy(), eps=1e-6,
+                                  return_state=True)
     err = max_row_error(to_np(o), ref)
     assert err < 2e-2, err
-    o2 = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6)
+    # the same call with the final state: the same output, and the state
+    # (summed from bf16 operands like the output on the tensor-core form,
+    # so held to the bf16 bound)
+    o2, S, z = la.forward_gated(q.cuda(), k.cuda(), v.cuda(), a.cuda(), eps=1e-6,
+                                return_state=True)
     assert torch.equal(o, o2)
+    eS = state_error(to_np(S), S_ref)
+    ez = state_error(to_np(z)[..., None], z_ref[..., None])
+    assert eS < 2e-2 and ez < 2e-2, (eS, ez)
 
 
 def test_gated_ones_equals_ungated_forward(la, ora):
