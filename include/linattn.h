@@ -290,6 +290,18 @@ LA_API int la_causal_kernel(int B, int H, int N, int D, int Dv,
 LA_API int la_device_wait_timeouts(int reset);
 
 /*
+ * Diagnostic of the failure path above, without a fault: runs the kernels'
+ * own bounded mbarrier wait, with a limit of `cycles` SM clock cycles (1 to
+ * 4e9; about 0.5 ms per 1e6 cycles at 2 GHz), on a barrier that nothing
+ * arrives on.  The wait gives up, adds one to the counter that
+ * la_device_wait_timeouts reads, and *gave_up (host) becomes 1; the context
+ * stays usable.  Launches one warp on the legacy default stream of the
+ * current device and synchronises the device.  LA_ERR_INVALID_ARG for a
+ * null gave_up or cycles out of range.
+ */
+LA_API la_status_t la_wait_selftest(long long cycles, int *gave_up);
+
+/*
  * Non-causal forward without any device allocation.  No counterpart on the
  * pages: it computes exactly what la_forward(..., causal = 0, gamma = NULL,
  * ...) computes, but keeps its scratch (per-head S, z and the partial sums of

@@ -94,6 +94,8 @@ def load_library() -> ctypes.CDLL:
             lib.la_backward_launches.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
+            lib.la_wait_selftest.argtypes = [ctypes.c_longlong, ctypes.POINTER(I)]
+            lib.la_wait_selftest.restype = I
             lib.la_device_wait_timeouts.argtypes = [I]
             lib.la_device_wait_timeouts.restype = I
             lib.la_status_string.argtypes = [I]
@@ -434,3 +436,12 @@ def gated_kernel(B, H, N, D, Dv, dtype=torch.bfloat16, want_state=False) -> str:
     if code < 0:
         raise LinAttnError("la_gated_kernel", -code)
     return "tensor-core" if code == 1 else "cuda-core"
+
+
+def wait_selftest(cycles=2_000_000) -> bool:
+    """Run the kernels' bounded wait on a barrier nothing arrives on, with a
+    short limit: True if it gave up (and counted itself in
+    device_wait_timeouts), as it should.  Synchronises the device."""
+    gave_up = ctypes.c_int(0)
+    _check("la_wait_selftest", load_library().la_wait_selftest(int(cycles), ctypes.byref(gave_up)))
+    return bool(gave_up.value)

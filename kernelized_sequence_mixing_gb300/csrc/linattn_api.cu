@@ -512,4 +512,9 @@ int la_backward_launches(int B, int H, int N, int D, int Dv) {
   return backward_launches(B * H, N, D, Dv);
 }
 
+la_status_t la_wait_selftest(long long cycles, int *gave_up) {
+  if (!gave_up || cycles <= 0 || cycles > 4000000000LL) return LA_ERR_INVALID_ARG;
+  return from_cuda(wait_selftest(cycles, gave_up));
+}
+
 }  // extern "C"

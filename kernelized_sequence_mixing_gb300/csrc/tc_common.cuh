@@ -61,23 +61,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitCycles, or as soon as another thread of the CTA has given up (*abort),
-// counting its own failure in *timeouts (device memory); returns false in
-// both cases.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort,
-                                          unsigned int *timeouts) {
+// `limit` cycles, or as soon as another thread of the CTA has given up
+// (*abort), counting its own failure in *timeouts (device memory); returns
+// false in both cases.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort, unsigned int *timeouts,
+                                                long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       atomicAdd(timeouts, 1u);
       return false;
     }
   }
+}
+// The kernels' waits: the limit is kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort,
+                                          unsigned int *timeouts) {
+  return mbar_wait_limit(bar, parity, abort, timeouts, kWaitCycles);
 }
 // mbar_wait executed by a whole warp, agreeing on the outcome: if any lane
 // gave up, every lane returns false, so the warp leaves its loop together.
@@ -395,5 +401,11 @@ bool make_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t dim_x, uint6
 // Host: device address of the wait-timeout counter on the current device
 // (nullptr if it cannot be obtained).
 unsigned int *wait_timeout_counter();
+
+// Host: run the kernels' bounded mbarrier wait, with a limit of `cycles`,
+// on a barrier nothing arrives on (one CTA of one warp); *gave_up (host)
+// becomes 1 when the wait gave up and counted itself in the timeout counter.
+// Synchronises the device.
+cudaError_t wait_selftest(long long cycles, int *gave_up);
 
 }  // namespace linattn

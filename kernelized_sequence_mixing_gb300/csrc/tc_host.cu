@@ -65,4 +65,38 @@ unsigned int *wait_timeout_counter() {
   return addr[dev];
 }
 
+namespace {
+
+// One thread waits, with the kernels' own bounded wait, for phase 0 of an
+// mbarrier that nothing arrives on; it gives up after `cycles`, counts
+// itself once in the timeout counter and reports.
+__global__ void wait_selftest_kernel(long long cycles, int *result, unsigned int *timeouts) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  tc::mbar_init(&bar, 1);
+  abort_flag = 0;
+  tc::mbar_init_fence();
+  const bool ok = tc::mbar_wait_limit(&bar, 0, &abort_flag, timeouts, cycles);
+  *result = ok ? 0 : 1;
+}
+
+}  // namespace
+
+cudaError_t wait_selftest(long long cycles, int *gave_up) {
+  unsigned int *ctr = wait_timeout_counter();
+  if (!ctr) return cudaErrorInvalidValue;
+  int *d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int));
+  if (e != cudaSuccess) return e;
+  wait_selftest_kernel<<<1, 32>>>(cycles, d, ctr);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  int h = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&h, d, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(d);
+  if (e == cudaSuccess) *gave_up = h;
+  return e;
+}
+
 }  // namespace linattn

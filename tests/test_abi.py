@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
-              "la_backward", "la_backward_launches", "la_gated_kernel",
+              "la_backward", "la_backward_launches", "la_gated_kernel", "la_wait_selftest",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -217,6 +217,15 @@ def test_favor_rejects_bad_arguments(lib):
     assert call(causal=0, g=(ctypes.c_float * 2)(0.5, 1.0)) == INVALID
     assert call(eps=-1.0) == INVALID
     assert call(B=0, qq=None, kk=None, vv=None, WW=None, oo=None) == OK
+
+
+def test_wait_selftest_rejects_bad_arguments(lib):
+    St = lib.la_wait_selftest
+    St.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int)]
+    g = ctypes.c_int(0)
+    assert St(0, ctypes.byref(g)) == INVALID
+    assert St(5_000_000_000, ctypes.byref(g)) == INVALID
+    assert St(1000, None) == INVALID
 
 
 def test_gated_kernel_dispatch(lib):
