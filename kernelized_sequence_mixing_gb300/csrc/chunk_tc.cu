@@ -1002,13 +1002,50 @@ int chunk_parts(int BH, int N) {
   return P < 1 ? 1 : P;
 }
 
-int chunk_state_parts(int BH, int N) {
-  // state and apply passes: no chain, about two waves of CTAs
+namespace {
+// CTAs of the state-mode kernel that run at once on one SM: its occupancy
+// by shared memory and registers, capped by its tensor-memory columns (an
+// allocation that does not fit waits for another CTA to free its columns).
+template <int D, int DV>
+int state_ctas_per_sm() {
+  using L = Lay<D, DV, kState>;
+  auto kern = chunk_tc_kernel<D, DV, kState, false, false>;
+  int occ = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, L::kAlloc) != cudaSuccess)
+    occ = 1;
+  const int tmem_cap = static_cast<int>(512 / L::kTmemCols);
+  occ = occ < tmem_cap ? occ : tmem_cap;
+  return occ < 1 ? 1 : occ;
+}
+}  // namespace
+
+int chunk_state_parts(int BH, int N, int D, int Dv) {
+  // state and apply passes: parts are independent (no chain), each CTA's
+  // time is proportional to its part's length, and whole waves of CTAs run
+  // at once; so P minimises waves(P) / P, waves(P) = ceil(B*H*P / slots),
+  // plus a small cost per part (its record and its share of the scan)
   const int nch = (N + kC - 1) / kC;
   if (BH <= 0 || nch <= 0) return 1;
-  int P = (2 * num_sms() + BH - 1) / BH;
-  if (P > nch) P = nch;
-  return P < 1 ? 1 : P;
+  int per_sm = 1;
+  if (D == 64 && Dv == 64) per_sm = state_ctas_per_sm<64, 64>();
+  else if (D == 64) per_sm = state_ctas_per_sm<64, 128>();
+  else if (Dv == 64) per_sm = state_ctas_per_sm<128, 64>();
+  else per_sm = state_ctas_per_sm<128, 128>();
+  const long long slots = static_cast<long long>(num_sms()) * per_sm;
+  const int pmax = nch < 64 ? nch : 64;
+  int best = 1;
+  double best_t = 1e30;
+  for (int P = 1; P <= pmax; ++P) {
+    const long long waves = (static_cast<long long>(BH) * P + slots - 1) / slots;
+    const double t = static_cast<double>(waves) / P + 0.002 * P;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = P;
+    }
+  }
+  return best;
 }
 
 size_t chunk_workspace_bytes(int BH, int P, int D, int Dv) {

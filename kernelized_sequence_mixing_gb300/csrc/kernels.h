@@ -47,7 +47,7 @@ cudaError_t launch_causal_simt(const Problem &p, const Gammas &g,
 // causal launcher's workspace (flags and inclusive states; 0 for one part).
 bool chunk_tc_supported(const Problem &p, const Gammas &g);
 int chunk_parts(int BH, int N);        // causal
-int chunk_state_parts(int BH, int N);  // prefill, non-causal
+int chunk_state_parts(int BH, int N, int D, int Dv);  // prefill, non-causal
 size_t chunk_workspace_bytes(int BH, int P, int D, int Dv);
 size_t chunk_causal_workspace_bytes(int BH, int P, int D, int Dv);
 Gammas log2_gammas(const Gammas &g, int H, bool decay);

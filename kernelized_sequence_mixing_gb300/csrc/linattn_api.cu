@@ -167,7 +167,7 @@ la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStrea
   // Non-causal: reduce S, z per (b, h) into a stream-ordered workspace, then
   // apply them to every query.
   if (chunk_tc_supported(p, g)) {
-    const int P = chunk_state_parts(BH, N);
+    const int P = chunk_state_parts(BH, N, D, Dv);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, chunk_workspace_bytes(BH, P, D, Dv), s) != cudaSuccess)
       return LA_ERR_CUDA;
@@ -223,7 +223,7 @@ la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
                    dtype == LA_F32 ? kF32 : kBF16};
   if (N > 0 && chunk_tc_supported(pr, g)) {
     // tensor cores: per-part sums, then a scan over the parts
-    const int P = chunk_state_parts(BH, N);
+    const int P = chunk_state_parts(BH, N, D, Dv);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, chunk_workspace_bytes(BH, P, D, Dv), s) != cudaSuccess)
       return LA_ERR_CUDA;
