@@ -668,7 +668,7 @@ def run_ours(args, w):
         "metric": workload_metric(w), "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype.itemsize == 2 else "f32",
+        "dtype": compute_dtype(w, gated_tc),
         "data": "synthetic",
         "config": dict(workload_config(w), **({"final_state": "S [B][H][D][Dv] and z [B][H][D] "
                                                "fp32 written after the last token"}
@@ -691,6 +691,18 @@ def run_ours(args, w):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def compute_dtype(w, gated_tc=False):
+    """The arithmetic type the timed path computes in: bf16 tensor-core
+    operands (fp32 accumulation) for the bf16 forward kernels, fp32 for the
+    CUDA-core paths (fp32 inputs, the decode steps' fp32 state update, the
+    CUDA-core gated form, the backward)."""
+    if w.backward or w.steps:
+        return "f32"
+    if w.gated and not gated_tc:
+        return "f32"
+    return "bf16" if w.dtype.itemsize == 2 else "f32"
 
 
 def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traffic,
