@@ -70,3 +70,36 @@ def test_backward_of_constant_values_is_zero_for_q_and_k():
     assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
     # and dv sums to the upstream gradient row sums (o is a convex mix of v)
     assert np.allclose(dv.sum(0), do.sum(0), rtol=1e-12, atol=1e-12)
+
+
+def test_backward_units_takes_one_decay_per_head(oracle_mod):
+    """The batched wrapper over [B, H, N, D] inputs with one decay per head:
+    every unit's gradient equals central differences of the C oracle run on
+    the whole batch with the same per-head decays.  The decays differ from
+    head to head, so a unit paired with another head's decay fails."""
+    rng = np.random.default_rng(12)
+    B, H, N, D, Dv = 2, 3, 5, 3, 2
+    q = rng.normal(size=(B, H, N, D)).astype(np.float32)
+    k = rng.normal(size=(B, H, N, D)).astype(np.float32)
+    v = rng.normal(size=(B, H, N, Dv)).astype(np.float32)
+    do = rng.normal(size=(B, H, N, Dv))
+    gam = np.array([0.5, 0.8, 1.0], dtype=np.float32)
+    eps, h = 0.3, 2e-3
+    got = dict(zip("qkv", bw.causal_backward_units(q, k, v, do, gam, eps)))
+    args = {"q": q, "k": k, "v": v}
+    for name in "qkv":
+        x = args[name]
+        fd = np.zeros(x.shape)
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            vals = []
+            for s in (+1, -1):
+                x[idx] = np.float32(old + s * h)
+                step = float(np.float64(x[idx]) - np.float64(old))
+                o = oracle_mod.causal(q, k, v, gamma=gam, eps=eps)
+                vals.append((np.sum(do * o), step))
+            x[idx] = old
+            (lp, sp), (lm, sm) = vals
+            fd[idx] = (lp - lm) / (sp - sm)
+        err = np.abs(got[name] - fd).max() / np.abs(fd).max()
+        assert err < 2e-4, (name, err)
