@@ -169,6 +169,42 @@ GATED_SOURCES = ("gla_simt.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 FAVOR_SOURCES = ("favor.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 # sources of the backward pass
 BACKWARD_SOURCES = ("backward_simt.cu", "common.cuh")
+# sources of the decode step, the 64-token tensor-core kernel (causal with
+# D or Dv = 64; the non-causal sums and read-out with its part scan) and the
+# fp32 CUDA-core kernels
+DECODE_SOURCES = ("decode.cu", "common.cuh")
+CHUNK_TC_SOURCES = ("chunk_tc.cu", "tc_common.cuh", "common.cuh")
+NONCAUSAL_SOURCES = ("chunk_tc.cu", "part_scan.cu", "tc_common.cuh", "common.cuh")
+SIMT_SOURCES = ("causal_simt.cu", "common.cuh")
+NONCAUSAL_SIMT_SOURCES = ("kv_state_simt.cu", "common.cuh")
+
+
+def workload_sources(w):
+    """The device sources whose hash identifies the timed kernels of ``w``."""
+    if w.steps:
+        return DECODE_SOURCES
+    if w.gated:
+        return GATED_SOURCES
+    if w.favor_r:
+        return FAVOR_SOURCES
+    if w.backward:
+        return BACKWARD_SOURCES
+    fp32 = w.dtype.itemsize == 4
+    if not w.causal:
+        return NONCAUSAL_SIMT_SOURCES if fp32 else NONCAUSAL_SOURCES
+    if fp32:
+        return SIMT_SOURCES
+    return KERNEL_SOURCES if w.D == 128 and w.Dv == 128 else CHUNK_TC_SOURCES
+
+
+def ncu_traffic(w, src_hash, final_state=False):
+    """The captured DRAM bytes of one launch for ``w``, or None when there is
+    no capture, the kernel source has changed since it was taken, or the run
+    does extra work (the final-state write) that the capture did not."""
+    tr = NCU_TRAFFIC.get(w.name)
+    if tr and tr.get("source") == src_hash and not final_state:
+        return tr["bytes"]
+    return None
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES):
@@ -638,11 +674,8 @@ def run_ours(args, w):
         byts += w.B * w.H * (w.D * w.Dv + w.D) * 4
     launch_ms = statistics.mean(per_launch)  # the whole step's launches
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
-    src_hash = kernel_source_hash(GATED_SOURCES if w.gated else
-                                  FAVOR_SOURCES if w.favor_r else
-                                  BACKWARD_SOURCES if w.backward else KERNEL_SOURCES)
-    tr = NCU_TRAFFIC.get(w.name)
-    traffic = tr["bytes"] if tr and tr.get("source") == src_hash and not final_state else None
+    src_hash = kernel_source_hash(workload_sources(w))
+    traffic = ncu_traffic(w, src_hash, final_state)
 
     # CPU baseline: the fp64 oracle on the host cores, one pass over a bounded
     # sample (all 32 heads of the default workload, ~20 s of CPU work)
