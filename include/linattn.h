@@ -119,8 +119,9 @@ LA_API la_status_t la_prefill_state(const void *k, const void *v, float *S, floa
  * CTA of the last part writes it); otherwise the library runs the forward,
  * then the prefill reduction, on `stream`.
  * q, k: [B][H][N][D]; v, o: [B][H][N][Dv] (dtype); S: [B][H][D][Dv] fp32 and
- * z: [B][H][D] fp32 are overwritten (zero for N = 0).  No buffer may overlap
- * another.  Errors as la_forward and la_prefill_state.
+ * z: [B][H][D] fp32 are overwritten (zero for N = 0).  No written buffer (o,
+ * S, z) may overlap any other buffer; the read-only inputs may share memory.
+ * Errors as la_forward and la_prefill_state.
  * Defined on the pages "Linear Attention Mechanisms" (dileepadev.github.io),
  * "Recurrent Reformulation" (the state S_i, z_i at i = N - 1) and "Gating
  * and Selective State Updates" (the decay on both).
@@ -135,7 +136,8 @@ LA_API la_status_t la_forward_state(const void *q, const void *k, const void *v,
  *   S <- gamma S + phi(k) v^T,  z <- gamma z + phi(k),
  * then  o = phi(q)^T S / (phi(q) . z + eps)  with the updated state.
  * q, k: [B][H][D]; v, o: [B][H][Dv] (dtype); S: [B][H][D][Dv] fp32 and
- * z: [B][H][D] fp32 are read and rewritten.  No buffer may overlap another.
+ * z: [B][H][D] fp32 are read and rewritten.  No written buffer (S, z, o) may
+ * overlap any other buffer; q, k and v may share memory.
  */
 LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
                            float *S, float *z, void *o, int B, int H, int D,
@@ -190,7 +192,8 @@ LA_API int la_gated_kernel(int B, int H, int N, int D, int Dv, la_dtype_t dtype,
  * recurrence of la_forward_gated for one token).  q, k: [B][H][D]; v, o:
  * [B][H][Dv] (dtype); a: [B][H][D] fp32 gates in [0, 1] (device); S:
  * [B][H][D][Dv] fp32 and z: [B][H][D] fp32 are read and rewritten.  No
- * buffer may overlap another.  Errors as la_decode_step.
+ * written buffer (S, z, o) may overlap any other buffer.  Errors as
+ * la_decode_step.
  */
 LA_API la_status_t la_decode_gated(const void *q, const void *k, const void *v,
                                    const float *a, float *S, float *z, void *o, int B,
