@@ -164,6 +164,64 @@ def _contig(name, t):
         raise ValueError(f"{name} must be contiguous")
 
 
+# Device types whose memory the kernels may address.  The C entry points take
+# plain pointers and cannot tell a host pointer or a short buffer from a good
+# one, so every shape, dtype and device is checked here, before the call.
+_DEVICE_TYPES = ("cuda",)
+
+
+def _one_device(fn, named, allow_host=False):
+    """All tensors of ``named`` [(name, tensor or None)] on one device, of a
+    type the kernels can address (or the host, where ``allow_host``: the
+    forward copies host tensors itself)."""
+    present = [(n, t) for n, t in named if t is not None]
+    devs = {t.device for _, t in present}
+    if len(devs) > 1:
+        where = ", ".join(f"{n} on {t.device}" for n, t in present)
+        raise ValueError(f"{fn}: all tensors must be on one device ({where})")
+    dev = next(iter(devs))
+    if dev.type not in _DEVICE_TYPES and not allow_host:
+        raise ValueError(f"{fn}: tensors must be CUDA tensors, got {dev}")
+    return dev
+
+
+def _expect(fn, name, t, shape, dtype):
+    """A caller-provided buffer: exactly ``shape`` and ``dtype``, contiguous."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{fn}: {name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{fn}: {name} must be {dtype}, got {t.dtype}")
+    _contig(name, t)
+
+
+def _qkv(fn, q, k, v, extra=()):
+    """q, k: [B, H, N, D]; v: [B, H, N, Dv]; one dtype (plus ``extra`` named
+    tensors of that dtype), contiguous.  Returns (B, H, N, D, Dv)."""
+    for n, t in (("q", q), ("k", k), ("v", v)) + tuple(extra):
+        _contig(n, t)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"{fn}: expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if not all(t.dtype == q.dtype for t in (k, v) + tuple(t for _, t in extra)):
+        names = ", ".join(["q", "k", "v"] + [n for n, _ in extra])
+        raise TypeError(f"{fn}: {names} must share one dtype")
+    _dtype_code(q)
+    B, H, N, D = q.shape
+    return B, H, N, D, v.shape[-1]
+
+
+def _step_qkv(fn, q, k, v):
+    """Decode-step inputs q, k: [B, H, D]; v: [B, H, Dv]; one dtype."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _contig(n, t)
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError(f"{fn}: expected q, k: [B, H, D] and v: [B, H, Dv]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError(f"{fn}: q, k and v must share one dtype")
+    _dtype_code(q)
+    B, H, D = q.shape
+    return B, H, D, v.shape[-1]
+
+
 def _to_device(t, dev):
     if t.device.type == "cuda":
         return t
@@ -182,24 +240,20 @@ def forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None,
     result copied back to host memory (pinned).  gamma: None, a float, or H
     per-head decays in [0, 1] (causal only).  Returns o: [B, H, N, Dv].
     """
+    B, H, N, D, Dv = _qkv("forward", q, k, v)
+    src = _one_device("forward", (("q", q), ("k", k), ("v", v), ("out", out)),
+                      allow_host=True)
+    if out is not None:
+        _expect("forward", "out", out, (B, H, N, Dv), q.dtype)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _contig(n, t)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
-        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    host = q.device.type != "cuda"
+    host = src.type != "cuda"
     dev = torch.device(device or "cuda:0") if host else q.device
-    B, H, N, D = q.shape
-    Dv = v.shape[-1]
     dt = _dtype_code(q)
     g = _gamma_arg(gamma, H)
     with torch.cuda.device(dev):
         qd, kd, vd = (_to_device(t, dev) for t in (q, k, v))
         od = out if (out is not None and not host) else torch.empty(
             (B, H, N, Dv), dtype=q.dtype, device=dev)
-        _contig("out", od)
         _check("la_forward", lib.la_forward(
             _ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), B, H, N, D, Dv,
             1 if causal else 0, g, float(eps), dt, _stream(dev)))
@@ -216,14 +270,21 @@ def prefill_state(k, v, gamma=None, S=None, z=None):
     """State after a causal pass: S = sum_j gamma^(N-1-j) phi(k_j) v_j^T,
     z likewise.  k: [B, H, N, D], v: [B, H, N, Dv] CUDA tensors.  Returns
     (S [B, H, D, Dv] fp32, z [B, H, D] fp32), written into S, z if given."""
-    lib = load_library()
     _contig("k", k)
     _contig("v", v)
+    if k.dim() != 4 or v.dim() != 4 or v.shape[:3] != k.shape[:3]:
+        raise ValueError("prefill_state: expected k: [B, H, N, D] and v: [B, H, N, Dv]")
+    if k.dtype != v.dtype:
+        raise TypeError("prefill_state: k and v must share one dtype")
+    _dtype_code(k)
     B, H, N, D = k.shape
     Dv = v.shape[-1]
-    if v.shape[:3] != k.shape[:3] or k.dtype != v.dtype:
-        raise ValueError("k, v shapes/dtypes disagree")
-    dev = k.device
+    dev = _one_device("prefill_state", (("k", k), ("v", v), ("S", S), ("z", z)))
+    if S is not None:
+        _expect("prefill_state", "S", S, (B, H, D, Dv), torch.float32)
+    if z is not None:
+        _expect("prefill_state", "z", z, (B, H, D), torch.float32)
+    lib = load_library()
     with torch.cuda.device(dev):
         if S is None:
             S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
@@ -240,24 +301,22 @@ def forward_state(q, k, v, gamma=None, eps=1e-6, out=None, S=None, z=None):
     (o [B, H, N, Dv], S [B, H, D, Dv] fp32, z [B, H, D] fp32), the state the
     decode loop continues from.  q, k: [B, H, N, D]; v: [B, H, N, Dv] CUDA
     tensors of one dtype; out, S, z: optional destinations."""
+    fn = "forward_state"
+    B, H, N, D, Dv = _qkv(fn, q, k, v)
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("out", out), ("S", S), ("z", z)))
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, Dv), q.dtype)
+    if S is not None:
+        _expect(fn, "S", S, (B, H, D, Dv), torch.float32)
+    if z is not None:
+        _expect(fn, "z", z, (B, H, D), torch.float32)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _contig(n, t)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
-        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    B, H, N, D = q.shape
-    Dv = v.shape[-1]
-    dev = q.device
     with torch.cuda.device(dev):
         o = out if out is not None else torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
         if S is None:
             S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
         if z is None:
             z = torch.empty((B, H, D), dtype=torch.float32, device=dev)
-        for n, t in (("out", o), ("S", S), ("z", z)):
-            _contig(n, t)
         _check("la_forward_state", lib.la_forward_state(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(S), _ptr(z), B, H, N, D, Dv,
             _gamma_arg(gamma, H), float(eps), _dtype_code(q), _stream(dev)))
@@ -268,12 +327,14 @@ def decode_step(q, k, v, S, z, gamma=None, eps=1e-6, out=None):
     """One recurrent step in place on (S, z): update with (k, v), then read
     out with q.  q, k: [B, H, D]; v: [B, H, Dv]; S: [B, H, D, Dv] fp32;
     z: [B, H, D] fp32 (all CUDA).  Returns o: [B, H, Dv]."""
+    fn = "decode_step"
+    B, H, D, Dv = _step_qkv(fn, q, k, v)
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("S", S), ("z", z), ("out", out)))
+    _expect(fn, "S", S, (B, H, D, Dv), torch.float32)
+    _expect(fn, "z", z, (B, H, D), torch.float32)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, Dv), q.dtype)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v), ("S", S), ("z", z)):
-        _contig(n, t)
-    B, H, D = q.shape
-    Dv = v.shape[-1]
-    dev = q.device
     with torch.cuda.device(dev):
         if out is None:
             out = torch.empty((B, H, Dv), dtype=q.dtype, device=dev)
@@ -291,29 +352,26 @@ def forward_gated(q, k, v, a, eps=1e-6, out=None, return_state=False, S=None, z=
     [B, H, N, D] float32 gates in [0, 1] on the same device.  Returns o, or
     (o, S [B, H, D, Dv] fp32, z [B, H, D] fp32) with the state after the last
     token when return_state is true (or S, z are given)."""
+    fn = "forward_gated"
+    B, H, N, D, Dv = _qkv(fn, q, k, v)
+    _expect(fn, "a", a, (B, H, N, D), torch.float32)
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("a", a), ("out", out), ("S", S),
+                           ("z", z)))
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, Dv), q.dtype)
+    if S is not None:
+        _expect(fn, "S", S, (B, H, D, Dv), torch.float32)
+    if z is not None:
+        _expect(fn, "z", z, (B, H, D), torch.float32)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v), ("a", a)):
-        _contig(n, t)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
-        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
-    if a.shape != q.shape or a.dtype != torch.float32:
-        raise ValueError("a must be float32 with the shape of q")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k and v must share one dtype")
-    B, H, N, D = q.shape
-    Dv = v.shape[-1]
-    dev = q.device
     want_state = return_state or S is not None or z is not None
     with torch.cuda.device(dev):
         o = out if out is not None else torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
-        _contig("out", o)
         if want_state:
             if S is None:
                 S = torch.empty((B, H, D, Dv), dtype=torch.float32, device=dev)
             if z is None:
                 z = torch.empty((B, H, D), dtype=torch.float32, device=dev)
-            _contig("S", S)
-            _contig("z", z)
         _check("la_forward_gated", lib.la_forward_gated(
             _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(o),
             _ptr(S) if want_state else None, _ptr(z) if want_state else None,
@@ -326,14 +384,16 @@ def decode_gated(q, k, v, a, S, z, eps=1e-6, out=None):
     phi(k) v^T, z <- a * z + phi(k), then read out with q.  q, k, a: [B, H, D]
     (a float32); v: [B, H, Dv]; S: [B, H, D, Dv] fp32; z: [B, H, D] fp32 (all
     CUDA).  Returns o: [B, H, Dv]."""
+    fn = "decode_gated"
+    B, H, D, Dv = _step_qkv(fn, q, k, v)
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("a", a), ("S", S), ("z", z),
+                           ("out", out)))
+    _expect(fn, "a", a, (B, H, D), torch.float32)
+    _expect(fn, "S", S, (B, H, D, Dv), torch.float32)
+    _expect(fn, "z", z, (B, H, D), torch.float32)
+    if out is not None:
+        _expect(fn, "out", out, (B, H, Dv), q.dtype)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v), ("a", a), ("S", S), ("z", z)):
-        _contig(n, t)
-    if a.dtype != torch.float32 or a.shape != q.shape:
-        raise ValueError("a must be float32 with the shape of q")
-    B, H, D = q.shape
-    Dv = v.shape[-1]
-    dev = q.device
     with torch.cuda.device(dev):
         if out is None:
             out = torch.empty((B, H, Dv), dtype=q.dtype, device=dev)
@@ -347,18 +407,23 @@ def favor_features(x, W, out=None):
     """Performer random features phi(x) = r^(-1/2) exp(W x - |x|^2 / 2) of
     every row of x [..., D] with the directions W [r, D] (same dtype, CUDA).
     Returns [..., r]."""
-    lib = load_library()
+    fn = "favor_features"
     _contig("x", x)
     _contig("W", W)
-    if W.dim() != 2 or W.shape[1] != x.shape[-1] or W.dtype != x.dtype:
-        raise ValueError("W must be [r, D] with the dtype of x")
+    if x.dim() < 1 or W.dim() != 2 or W.shape[1] != x.shape[-1]:
+        raise ValueError(f"{fn}: W must be [r, D] for x [..., D]")
+    if W.dtype != x.dtype:
+        raise TypeError(f"{fn}: W must have the dtype of x")
+    _dtype_code(x)
     D, r = x.shape[-1], W.shape[0]
     rows = x.numel() // D if D else 0
-    dev = x.device
+    dev = _one_device(fn, (("x", x), ("W", W), ("out", out)))
+    if out is not None:
+        _expect(fn, "out", out, tuple(x.shape[:-1]) + (r,), x.dtype)
+    lib = load_library()
     with torch.cuda.device(dev):
         if out is None:
             out = torch.empty(x.shape[:-1] + (r,), dtype=x.dtype, device=dev)
-        _contig("out", out)
         _check("la_favor_features", lib.la_favor_features(
             _ptr(x), _ptr(W), _ptr(out), rows, D, r, _dtype_code(x), _stream(dev)))
     return out
@@ -369,22 +434,18 @@ def forward_favor(q, k, v, W, causal=True, gamma=None, eps=1e-6, out=None):
     directions W [r, D], then linear attention over them (causal with
     optional per-head decay, or non-causal).  q, k: [B, H, N, D]; v:
     [B, H, N, Dv]; all CUDA tensors of one dtype.  Returns o [B, H, N, Dv]."""
+    fn = "forward_favor"
+    B, H, N, D, Dv = _qkv(fn, q, k, v, extra=(("W", W),))
+    if W.dim() != 2 or W.shape[1] != D:
+        raise ValueError(f"{fn}: W must be [r, D]")
+    r = W.shape[0]
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("W", W), ("out", out)))
+    if out is not None:
+        _expect(fn, "out", out, (B, H, N, Dv), q.dtype)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v), ("W", W)):
-        _contig(n, t)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3]:
-        raise ValueError("expected q, k: [B, H, N, D] and v: [B, H, N, Dv]")
-    if not (q.dtype == k.dtype == v.dtype == W.dtype):
-        raise TypeError("q, k, v and W must share one dtype")
-    if W.dim() != 2 or W.shape[1] != q.shape[-1]:
-        raise ValueError("W must be [r, D]")
-    B, H, N, D = q.shape
-    Dv, r = v.shape[-1], W.shape[0]
-    dev = q.device
     with torch.cuda.device(dev):
         if out is None:
             out = torch.empty((B, H, N, Dv), dtype=q.dtype, device=dev)
-        _contig("out", out)
         _check("la_forward_favor", lib.la_forward_favor(
             _ptr(q), _ptr(k), _ptr(v), _ptr(W), _ptr(out), B, H, N, D, Dv, r,
             1 if causal else 0, _gamma_arg(gamma, H), float(eps), _dtype_code(q),
@@ -396,22 +457,20 @@ def backward(q, k, v, do, gamma=None, eps=1e-6, dq=None, dk=None, dv=None):
     """Gradients (dq, dk, dv) of the causal forward o = forward(q, k, v,
     causal=True, gamma, eps) for the upstream gradient do = dL/do.  q, k:
     [B, H, N, D]; v, do: [B, H, N, Dv]; CUDA tensors of one dtype."""
+    fn = "backward"
+    B, H, N, D, Dv = _qkv(fn, q, k, v, extra=(("do", do),))
+    if do.shape != v.shape:
+        raise ValueError(f"{fn}: do must have the shape of v")
+    dev = _one_device(fn, (("q", q), ("k", k), ("v", v), ("do", do), ("dq", dq), ("dk", dk),
+                           ("dv", dv)))
+    for n, t, shape in (("dq", dq, q.shape), ("dk", dk, k.shape), ("dv", dv, v.shape)):
+        if t is not None:
+            _expect(fn, n, t, shape, q.dtype)
     lib = load_library()
-    for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
-        _contig(n, t)
-    if q.dim() != 4 or k.shape != q.shape or v.shape[:3] != q.shape[:3] or do.shape != v.shape:
-        raise ValueError("expected q, k: [B, H, N, D] and v, do: [B, H, N, Dv]")
-    if not (q.dtype == k.dtype == v.dtype == do.dtype):
-        raise TypeError("q, k, v and do must share one dtype")
-    B, H, N, D = q.shape
-    Dv = v.shape[-1]
-    dev = q.device
     with torch.cuda.device(dev):
         dq = torch.empty_like(q) if dq is None else dq
         dk = torch.empty_like(k) if dk is None else dk
         dv = torch.empty_like(v) if dv is None else dv
-        for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-            _contig(n, t)
         _check("la_backward", lib.la_backward(
             _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, D, Dv,
             _gamma_arg(gamma, H), float(eps), _dtype_code(q), _stream(dev)))
