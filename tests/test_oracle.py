@@ -402,3 +402,24 @@ def test_gated_feature_gates_act_per_row_of_the_state(oracle_mod):
     assert abs(z[2] - fk9[2]) <= 1e-15 * abs(fk9[2])
     for d in (0, 1, 3):
         assert rel_err(S[d], S1[d]) < 1e-14 and abs(z[d] - z1[d]) <= 1e-14 * abs(z1[d])
+
+
+def test_gated_final_state_matches_the_unrolled_sum(oracle_mod):
+    """The state after the last token, unrolled from the gated recurrence:
+    S[d, :] = sum_s (prod_(u = s+1..N-1) a_u[d]) phi(k_s)[d] v_s and z[d]
+    the same without v_s, with random gates in [0, 1)."""
+    for N, D, Dv, lo in ((1, 3, 2, 0.0), (13, 5, 4, 0.0), (30, 4, 6, 0.7)):
+        q, k, v = rng_inputs(500 + N, N, D, Dv)
+        a = gate_inputs(600 + N, N, D, lo, 1.0)
+        _, S, z = oracle_mod.gated(q, k, v, a, return_state=True)
+        fk = phi_np(k)
+        vv = v.astype(np.float64)
+        S_ref = np.zeros((D, Dv))
+        z_ref = np.zeros(D)
+        for s in range(N):
+            w = np.ones(D)
+            for u in range(s + 1, N):
+                w = w * a[u]
+            S_ref += np.outer(w * fk[s], vv[s])
+            z_ref += w * fk[s]
+        assert rel_err(S, S_ref) < 1e-13 and rel_err(z, z_ref) < 1e-13
