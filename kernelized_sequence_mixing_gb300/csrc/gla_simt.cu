@@ -2,11 +2,12 @@
 // sequence parts.
 //
 // "Linear Attention Mechanisms" (dileepadev.github.io), "Gating and Selective
-// State Updates", gated linear attention: S_t = G_t (.) S_(t-1) + phi(k_t) v_t^T
-// with a data-dependent gate G_t in [0, 1]^(D x Dv).  The gate is one value per
-// key feature and step, G_t = a_t 1^T (row d of the state is scaled by
-// a_t[d]); the normaliser is gated the same way, z_t = a_t (.) z_(t-1) +
-// phi(k_t), and o_t = phi(q_t)^T S_t / (phi(q_t) . z_t + eps).
+// State Updates", gated linear attention: S_t = G_t (.) S_(t-1) + phi(k_t) v_t^T,
+// where G_t has the state's D x Dv shape, entries in [0, 1], and is computed
+// from step t's input.  Here the gate is one value per key feature and step,
+// G_t = a_t 1^T (row d of the state is scaled by a_t[d]); the normaliser is
+// gated the same way, z_t = a_t (.) z_(t-1) + phi(k_t), and
+// o_t = phi(q_t)^T S_t / (phi(q_t) . z_t + eps).
 //
 // Chunk form.  Within a chunk with local index t and per-feature prefix
 // products c_t = a_0 (.) ... (.) a_t, the recurrence unrolls to
