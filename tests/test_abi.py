@@ -257,6 +257,20 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(B=0, p=(None,) * 7) == OK
 
 
+def test_backward_launches_rejects_bad_sizes(lib):
+    """Host-only paths of the launch count: invalid and unsupported sizes
+    give the negated status, an empty call launches nothing.  (Valid sizes
+    read the device's SM count, so they are left to the GPU tests.)"""
+    L = lib.la_backward_launches
+    assert L(-1, 2, 8, 64, 64) == -INVALID
+    assert L(1, 2, 8, 0, 64) == -INVALID
+    assert L(1, 2, 8, 96, 64) == -UNSUPPORTED
+    assert L(1, 300, 8, 64, 64) == -UNSUPPORTED               # more heads than supported
+    assert L(1 << 16, 1 << 8, 1 << 8, 64, 64) == -UNSUPPORTED  # 2^32 tokens
+    assert L(0, 2, 8, 64, 64) == 0
+    assert L(1, 2, 0, 128, 128) == 0
+
+
 def test_causal_kernel_dispatch(lib):
     K = lib.la_causal_kernel
     g = lambda *x: (ctypes.c_float * len(x))(*x)  # noqa: E731
