@@ -61,7 +61,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        # per-process object names: concurrent builds never share a file
+        obj = os.path.join(BUILD, f"{os.path.basename(src)}.{os.getpid()}.o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         if ptxas_v:
             cmd.insert(1, "-Xptxas=-v")
@@ -79,6 +80,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False
     cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static",
            *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
+    for obj in objs:
+        os.remove(obj)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
