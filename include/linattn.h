@@ -54,6 +54,19 @@
  *   kernels round phi(q), phi(k), the decay-weighted values and the
  *   intra-chunk weights to bf16 as matrix-multiply operands; o is rounded to
  *   bf16 (round to nearest even).
+ *
+ * Example: a causal pass with one decay per head, then decode steps that
+ * continue from its state (all buffers device memory of the documented
+ * sizes; error handling shortened):
+ *
+ *   float gamma[H];                        // host, one decay per head
+ *   la_status_t st = la_forward_state(q, k, v, o, S, z, B, H, N, D, Dv,
+ *                                     gamma, 1e-6f, LA_BF16, stream);
+ *   if (st != LA_OK) fprintf(stderr, "%s\n", la_status_string(st));
+ *   for (int t = 0; t < steps; ++t)        // S, z updated in place
+ *     st = la_decode_step(q_t, k_t, v_t, S, z, o_t, B, H, D, Dv, gamma,
+ *                         1e-6f, LA_BF16, stream);
+ *   cudaStreamSynchronize(stream);         // kernel faults surface here
  */
 #ifndef LINATTN_H
 #define LINATTN_H
