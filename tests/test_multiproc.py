@@ -79,3 +79,13 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert r.returncode == 0
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 1
+    # the fields the reference line carries besides the base contract's
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["steps"] == 1 and line["warmup"] == 3
+    assert line["config"]["workload"] == "causal_f32_n256"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
