@@ -156,3 +156,37 @@ def test_each_workload_hashes_the_sources_it_runs():
         for f in bench.workload_sources(w):
             assert os.path.exists(os.path.join(ROOT, "kernelized_sequence_mixing_gb300",
                                                "csrc", f))
+
+
+def test_clock_summary():
+    """The clocks object from nvidia-smi lines: median SM clock, the highest
+    maximum clock, every throttle reason seen Active, and malformed lines
+    skipped."""
+    na = "Not Active"
+    lines = [
+        f"0, 2070, 2070, 900.1, 0x0, {na}, {na}, {na}, {na}",
+        f"0, 1980, 2070, 1390.0, 0x4, {na}, {na}, {na}, Active",
+        f"0, 2070, 2070, 1100.5, 0x0, {na}, {na}, {na}, {na}",
+        "garbage",
+        f"0, [N/A], 2070, 1100.5, 0x0, {na}, {na}, {na}, {na}",
+        f"0, 1500, 2070, 1200.0, 0x8, Active, {na}, {na}, {na}",
+    ]
+    c = bench.summarize_clocks(lines)
+    assert c["samples"] == 4
+    assert c["sm_mhz"] == 2025.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.summarize_clocks([]) == {"sm_mhz": None, "sm_max_mhz": None,
+                                          "reasons": [], "samples": 0}
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch):
+    """With no nvidia-smi on the machine the sampler reports that instead of
+    failing the run."""
+    def missing(*a, **kw):
+        raise OSError("no nvidia-smi")
+
+    monkeypatch.setattr(bench.subprocess, "Popen", missing)
+    s = bench.ClockSampler(0)
+    s.start()
+    c = s.stop()
+    assert c["samples"] == 0 and c["note"] == "nvidia-smi unavailable"
