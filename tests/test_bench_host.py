@@ -190,3 +190,20 @@ def test_clock_sampler_without_nvidia_smi(monkeypatch):
     s.start()
     c = s.stop()
     assert c["samples"] == 0 and c["note"] == "nvidia-smi unavailable"
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_config_names_the_workload(name):
+    """The config object names the workload and its sizes, and carries no
+    model keys (there is no model: the path is one operator)."""
+    w = WORKLOADS[name]
+    cfg = bench.workload_config(w)
+    assert cfg["workload"] == name and "model" not in cfg
+    assert (cfg["B"], cfg["H"], cfg["D"], cfg["Dv"]) == (w.B, w.H, w.D, w.Dv)
+    assert cfg["global_batch"] == w.B
+    # decode steps process one token per sequence after a prefill of N
+    assert cfg["seq_len"] == (1 if w.steps else w.N)
+    if w.steps:
+        assert cfg["prefill_len"] == w.N
+    assert ("gamma" in cfg) == w.decayed and ("gates" in cfg) == w.gated
+    json.dumps(cfg)   # serialisable into the JSON line
