@@ -8,6 +8,7 @@ import os
 import sys
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -207,3 +208,30 @@ def test_config_names_the_workload(name):
         assert cfg["prefill_len"] == w.N
     assert ("gamma" in cfg) == w.decayed and ("gates" in cfg) == w.gated
     json.dumps(cfg)   # serialisable into the JSON line
+
+
+def test_oracle_sample_pairs_units_with_their_decays():
+    """The CPU baseline's sample: the first units in (b, h) order, every
+    token, each with its own head's decay."""
+    import numpy as np
+    from kernelized_sequence_mixing_gb300 import workloads as wl
+    w = wl.Workload("t", True, 2, 3, 8, 64, 64, torch.float32, 1.0, 0, decayed=True)
+    q, k, v = wl.workload_inputs(w)
+    qs, ks, vs, gu = bench.oracle_sample(w, 5)
+    assert qs.shape == (5, 8, 64) and vs.shape == (5, 8, 64)
+    assert np.array_equal(qs[4], q[1, 1].numpy())          # unit 4 = (b 1, h 1)
+    g = wl.retnet_gammas(3).numpy()
+    assert np.array_equal(gu, np.array([g[0], g[1], g[2], g[0], g[1]]))
+
+
+def test_oracle_timing_counts_tokens_across_heads():
+    """A token is one position of one sequence across all H heads, so a
+    sample of u of the H heads of one sequence covers u / H of its N tokens."""
+    from kernelized_sequence_mixing_gb300 import workloads as wl
+    w = wl.Workload("t", True, 1, 4, 32, 64, 64, torch.float32, 1.0, 0)
+    tokens, times, threads = bench.time_oracle(w, 2, 1)
+    assert tokens == 2 / 4 * 32 and len(times) == 1 and times[0] > 0 and threads >= 1
+    d = wl.Workload("d", True, 4, 8, 4, 64, 64, torch.float32, 1.0, 0, steps=2,
+                    step_seed0=1000)
+    units_tokens, times, _ = bench.time_oracle_decode(d, 16, 1)
+    assert units_tokens == 16 / 8 and len(times) == 1
