@@ -109,11 +109,11 @@ def load_golden():
             elif key == "end":
                 cases.append(cur)
                 cur = None
-            elif key in ("q", "k", "v", "o"):
+            elif key in ("q", "k", "v", "o", "a", "S", "z"):
                 cur[key] = _parse_matrix(rest)
             elif key in ("gamma", "eps"):
                 cur[key] = Fraction(rest)
-            elif key == "causal":
+            elif key in ("causal", "gated"):
                 cur[key] = bool(int(rest))
     return cases
 
@@ -142,8 +142,55 @@ def exact_quadratic(case):
     return out
 
 
+def exact_gated(case):
+    """Exact rational evaluation of the gated recurrence's weighted-sum form:
+    w_ts = sum_d phi(q_t)[d] phi(k_s)[d] prod_(u=s+1..t) a_u[d] (s <= t), and
+    the final state S[d] = sum_s prod_(u=s+1..N-1) a_u[d] phi(k_s)[d] v_s."""
+    q, k, v, a, eps = case["q"], case["k"], case["v"], case["a"], case["eps"]
+    N, D, Dv = len(q), len(q[0]), len(v[0])
+
+    def carry(s, t):  # prod_(u = s+1 .. t) a_u, per feature
+        p = [Fraction(1)] * D
+        for u in range(s + 1, t + 1):
+            p = [x * y for x, y in zip(p, a[u])]
+        return p
+
+    out = []
+    for t in range(N):
+        fq = [x + 1 for x in q[t]]
+        num, den = [Fraction(0)] * Dv, Fraction(0)
+        for s in range(t + 1):
+            fk = [x + 1 for x in k[s]]
+            w = sum(x * y * c for x, y, c in zip(fq, fk, carry(s, t)))
+            num = [n + w * x for n, x in zip(num, v[s])]
+            den += w
+        out.append([n / (den + eps) for n in num])
+    S = [[Fraction(0)] * Dv for _ in range(D)]
+    z = [Fraction(0)] * D
+    for s in range(N):
+        fk = [x + 1 for x in k[s]]
+        c = carry(s, N - 1)
+        for d in range(D):
+            z[d] += c[d] * fk[d]
+            S[d] = [x + c[d] * fk[d] * y for x, y in zip(S[d], v[s])]
+    return out, S, [z]
+
+
 @pytest.mark.parametrize("case", load_golden(), ids=lambda c: c["name"])
 def test_hand_worked_examples(oracle_mod, case):
+    as_f32 = lambda m: np.array(m, dtype=np.float64).astype(np.float32)  # noqa: E731
+    as_f64 = lambda m: np.array([[float(x) for x in row] for row in m])  # noqa: E731
+    if case.get("gated"):
+        # the hand-derived values agree with exact rational arithmetic
+        o, S, z = exact_gated(case)
+        assert (o, S, z) == (case["o"], case["S"], case["z"])
+        got, gS, gz = oracle_mod.gated(as_f32(case["q"]), as_f32(case["k"]), as_f32(case["v"]),
+                                       as_f32(case["a"]), eps=float(case["eps"]),
+                                       return_state=True)
+        np.testing.assert_allclose(got, as_f64(case["o"]), rtol=1e-15, atol=1e-15)
+        np.testing.assert_allclose(gS, as_f64(case["S"]), rtol=1e-15, atol=1e-15)
+        np.testing.assert_allclose(gz, as_f64(case["z"])[0], rtol=1e-15, atol=1e-15)
+        return
     # the fixture's hand-derived values agree with exact rational arithmetic
     assert exact_quadratic(case) == case["o"]
     q = np.array(case["q"], dtype=np.float64).astype(np.float32)
