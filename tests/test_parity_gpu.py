@@ -9,7 +9,6 @@ import numpy as np
 import pytest
 import torch
 
-import helpers
 from helpers import TOL, max_row_error, state_error, to_np
 
 pytestmark = pytest.mark.gpu
