@@ -66,10 +66,15 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2070e6 / 1e12
 # ncu capture, keyed by workload, with the hash of the kernel source the
 # capture was taken on; reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/chunk128_causal_decay_bf16_n16384.md: 583.837440 MB read +
-    # 114.072832 MB written in one launch of the full workload
+    # dram__bytes_read.sum 583.837440 MB + dram__bytes_write.sum 114.072832 MB
+    # in one launch of the full workload
     "causal_decay_bf16_n16384": {"bytes": 697910272, "source": "1b0034327165b9d1"},
 }
+
+# the other configurations of the method, timed in the same process as the
+# default workload and reported in its line under "workloads"
+EXTRA_WORKLOADS = ("causal_f32_n256", "causal_bf16_n4096", "noncausal_bf16_n65536",
+                   "decode_bf16_h32")
 
 
 # ---------------------------------------------------------------------------
@@ -312,7 +317,11 @@ def oracle_sample(w, heads_per_pass):
 def time_oracle(w, heads_per_pass, passes):
     import oracle
     qs, ks, vs, gu = oracle_sample(w, heads_per_pass)
+    # the C oracle starts at most one thread per unit; the Performer and
+    # gradient oracles are numpy, whose BLAS may use every host thread
     threads = oracle.default_threads()
+    if not (w.favor_r or w.backward):
+        threads = min(threads, qs.shape[0])
     times = []
     for _ in range(passes):
         t0 = time.perf_counter()
@@ -348,7 +357,7 @@ def time_oracle_decode(w, units, passes):
     q, k, v = f(qt), f(kt), f(vt)
     S = np.zeros((units, w.D, w.Dv))
     z = np.zeros((units, w.D))
-    threads = oracle.default_threads()
+    threads = min(oracle.default_threads(), units)
     times = []
     if w.gated:
         from kernelized_sequence_mixing_gb300.workloads import decode_step_gates
@@ -375,7 +384,9 @@ def run_reference(args, w):
             time_oracle_decode(w, heads, 1)
         tokens, times, threads = time_oracle_decode(w, heads, args.steps)
     else:
-        heads = min(8, w.B * w.H)
+        # one unit per host thread (the oracle runs at most one thread per unit)
+        import oracle
+        heads = max(1, min(oracle.default_threads(), w.B * w.H))
         for _ in range(args.warmup):
             time_oracle(w, heads, 1)
         tokens, times, threads = time_oracle(w, heads, args.steps)
@@ -614,6 +625,10 @@ def run_ours(args, w):
     if w.steps:
         ncopy = 1
 
+    # a bounded device wait that gave up leaves its CTA's output incomplete
+    # (and the launch faster): the count is checked after the timed work
+    torch.cuda.synchronize(dev)
+    la.device_wait_timeouts(reset=True)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -672,10 +687,30 @@ def run_ours(args, w):
         do.numel() * es if w.backward else 0)
     d2h = (sum(t.numel() for t in grads) if w.backward else od.numel()) * es
 
+    torch.cuda.synchronize(dev)
+    gave_up = la.device_wait_timeouts(reset=True)
+    if gave_up:
+        print(json.dumps({"metric": workload_metric(w), "invalid":
+                          f"{gave_up} bounded device wait(s) gave up during the run; "
+                          "the timed outputs are incomplete"}), flush=True)
+        return 1
     if rank != 0:
         return 0
 
     hbm_peak, tc_peak, peak_src = measured_peaks()
+    extra = None
+    if ws == 1 and w.name == DEFAULT_WORKLOAD and not args.no_extra:
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            extra[name] = time_extra(la, name, dev, hbm_peak, args.quick)
+            torch.cuda.empty_cache()
+        torch.cuda.synchronize(dev)
+        gave_up = la.device_wait_timeouts(reset=True)
+        if gave_up:
+            print(json.dumps({"metric": workload_metric(w), "invalid":
+                              f"{gave_up} bounded device wait(s) gave up in the other "
+                              "configurations; their outputs are incomplete"}), flush=True)
+            return 1
     byts, flops = decode_work(w) if w.steps else algorithmic_work(w)
     if final_state:  # the state written once at the end, fp32
         byts += w.B * w.H * (w.D * w.Dv + w.D) * 4
@@ -729,8 +764,121 @@ def run_ours(args, w):
         "clocks": clocks,
         "kernel_source": src_hash,
     }
+    if extra is not None:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
     return 0
+
+
+def device_inputs(w, gen, dev, N=None):
+    """q, k, v of workload ``w`` drawn on the device (N(0, 1) times the
+    workload's scale, rounded once to its dtype) from a seeded CUDA
+    generator: the shapes and distribution of the workload's recipe, for
+    timing only (the parity tests use the CPU recipe itself)."""
+    import torch
+    N = w.N if N is None else N
+    out = []
+    for width in (w.D, w.D, w.Dv):
+        t = torch.randn((w.B, w.H, N, width), generator=gen, device=dev, dtype=torch.float32)
+        out.append((t * w.scale).to(w.dtype))
+    return out
+
+
+def time_extra(la, name, dev, hbm_peak, quick):
+    """Time one more configuration in this process: warm-up, then CUDA events
+    around each step on the launching stream; clocks sampled around it.
+    Forward configurations run ``steps`` forward passes (rotating input
+    copies when the working set fits in L2); the decode configuration runs
+    its whole loop of single-token steps, each with fresh inputs."""
+    import torch
+    from kernelized_sequence_mixing_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    stream = torch.cuda.current_stream(dev)
+    if w.steps:
+        _, kp, vp = device_inputs(w, gen, dev)
+        S, z = la.prefill_state(kp, vp, gamma=w.gamma())
+        del kp, vp
+        steps_in = [device_inputs(w, gen, dev, N=1) for _ in range(w.steps)]
+        steps_in = [tuple(t[:, :, 0].contiguous() for t in x) for x in steps_in]
+        od = torch.empty((w.B, w.H, w.Dv), dtype=w.dtype, device=dev)
+        S0, z0 = S.clone(), z.clone()
+
+        def run(i):
+            qd, kd, vd = steps_in[i % w.steps]
+            la.decode_step(qd, kd, vd, S, z, eps=w.eps, out=od)
+        nsteps, warm = w.steps, 3
+        byts, flops = decode_work(w)
+        tokens = w.B
+    else:
+        q, k, v = device_inputs(w, gen, dev)
+        od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
+        step_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, od))
+        ncopy = 1 if step_bytes > L2_BYTES else -(-2 * L2_BYTES // step_bytes)
+        copies = [(q, k, v, od)] + [(q.clone(), k.clone(), v.clone(), torch.empty_like(od))
+                                    for _ in range(ncopy - 1)]
+
+        def run(i):
+            qc, kc, vc, oc = copies[i % ncopy]
+            la.forward(qc, kc, vc, causal=w.causal, gamma=w.gamma(), eps=w.eps, out=oc)
+        nsteps = 20 if w.N * w.B * w.H >= (1 << 22) else 100
+        warm = 5
+        byts, flops = algorithmic_work(w)
+        tokens = w.B * w.N
+    for i in range(warm):
+        run(i)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    roll = 0.0 if quick else 0.5
+    if not quick:
+        sampler.start()
+    t_end = time.perf_counter() + roll
+    i = 0
+    while time.perf_counter() < t_end:
+        run(i)
+        i += 1
+        torch.cuda.synchronize(dev)
+    if w.steps:  # the decode loop starts from the prefill state
+        S.copy_(S0)
+        z.copy_(z0)
+        torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
+    ev[0].record(stream)
+    for i in range(nsteps):
+        run(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(nsteps)]
+    total = ev[0].elapsed_time(ev[-1])
+    t_end = time.perf_counter() + roll
+    i = 0
+    while time.perf_counter() < t_end:
+        run(i)
+        i += 1
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if not quick else None
+    ms = total / nsteps
+    gbs = byts / (ms / 1e3) / 1e9
+    entry = {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "tokens/s",
+             "steps": nsteps, "dtype": compute_dtype(w),
+             "config": workload_config(w),
+             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": gbs / hbm_peak, "algorithmic_bytes": byts,
+                          "tflops": flops / (ms / 1e3) / 1e12},
+             "clocks": clocks,
+             "inputs": "device-drawn from a seeded CUDA generator, same shapes and N(0,1) x "
+                       f"{w.scale} distribution as the recipe"}
+    if w.steps:
+        med = statistics.median(per)
+        entry.update(ms_per_step_median=med, ms_total=total,
+                     note=f"{nsteps} single-token steps over all {w.B}x{w.H} units, fresh "
+                          f"inputs per step, from a {w.N}-token prefill state")
+        entry["roofline"]["frac_median_step"] = byts / (med / 1e3) / 1e9 / hbm_peak
+    else:
+        entry["l2"] = ("working set larger than L2, no flush" if ncopy == 1 else
+                       f"working set below L2: steps rotate over {ncopy} input/output copies")
+    return entry
 
 
 def compute_dtype(w, gated_tc=False):
@@ -777,6 +925,9 @@ def main(argv=None):
     ap.add_argument("--final-state", action="store_true",
                     help="causal workloads: time la_forward_state (the forward "
                          "plus the state after the last token) instead")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload only: skip timing the other "
+                         "configurations reported under 'workloads'")
     ap.add_argument("--quick", action="store_true",
                     help="skip the clock-sampling window and the end-to-end "
                          "leg (few launches, for profiler runs)")

@@ -41,7 +41,8 @@
  * - gamma is a HOST array of H floats in [0, 1] (one decay per head), or
  *   NULL meaning 1 for every head.  The library copies the values during the
  *   call; the caller keeps ownership.
- * - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default stream),
+ *   so that this header needs no CUDA header to compile.
  *   Every call is asynchronous on that stream and never synchronises.  The
  *   caller owns all buffers; the library keeps no state between calls.
  * - Arguments are validated before any CUDA call, so a rejected call has no
@@ -106,6 +107,13 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype_t;
  *                cudaMallocAsync on `stream` and released on it.
  * q, k: [B][H][N][D]; v: [B][H][N][Dv]; o: [B][H][N][Dv] (written).  o must
  * not overlap q, k or v.  eps must be finite and >= 0.
+ * Defined on the pages "Linear Attention Mechanisms" (dileepadev.github.io):
+ * causal by "Recurrent Reformulation" (S_i, z_i and the read-out o_i), with
+ * the per-head decay of "Gating and Selective State Updates" (RetNet, weight
+ * gamma^(t-j)) on both S and z; non-causal by "The Kernel Trick for
+ * Attention" (S and z once over every key); eps as in the NumPy listing of
+ * "Linear Attention Mechanisms" (sadullah.online), "The linear attention
+ * trick".
  */
 LA_API la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
                        int B, int H, int N, int D, int Dv, int causal,
@@ -118,6 +126,10 @@ LA_API la_status_t la_forward(const void *q, const void *k, const void *v, void 
  * k: [B][H][N][D]; v: [B][H][N][Dv] (dtype); S: [B][H][D][Dv] fp32 and
  * z: [B][H][D] fp32 are overwritten.  S and z must not overlap k or v, nor
  * each other.
+ * Defined on the pages "Linear Attention Mechanisms" (dileepadev.github.io),
+ * "Recurrent Reformulation" (S_i and z_i of the causal recurrence at
+ * i = N - 1, the state the recurrent form carries into inference) and
+ * "Gating and Selective State Updates" (the decay weight gamma^(N-1-j)).
  */
 LA_API la_status_t la_prefill_state(const void *k, const void *v, float *S, float *z,
                              int B, int H, int N, int D, int Dv,
@@ -151,6 +163,11 @@ LA_API la_status_t la_forward_state(const void *q, const void *k, const void *v,
  * q, k: [B][H][D]; v, o: [B][H][Dv] (dtype); S: [B][H][D][Dv] fp32 and
  * z: [B][H][D] fp32 are read and rewritten.  No written buffer (S, z, o) may
  * overlap any other buffer; q, k and v may share memory.
+ * Defined on the pages "Linear Attention Mechanisms" (dileepadev.github.io),
+ * "Recurrent Reformulation" (one iteration of the recurrence: update with
+ * k, v, then read out with q) and "Practical Tradeoffs" (a fixed-size state
+ * per step at inference), with the decay of "Gating and Selective State
+ * Updates" on both S and z.
  */
 LA_API la_status_t la_decode_step(const void *q, const void *k, const void *v,
                            float *S, float *z, void *o, int B, int H, int D,

@@ -21,12 +21,16 @@ constexpr int kThreads = 256;
 constexpr int kTok = 32;            // tokens staged per tile
 constexpr int kSplitTokens = 4096;  // tokens per split of the reduction
 
-// grid (BH, nsplit); S_out/z_out indexed by (split * BH + bh).
+// The y extent of a grid is at most 65535; larger counts are strided.
+inline int grid_y(int64_t n) { return (int)(n < 1 ? 1 : (n > 65535 ? 65535 : n)); }
+
+// grid (BH, min(nsplit, 65535)); S_out/z_out indexed by (split * BH + bh).
 template <int D, int DV, bool DECAY, bool IDENT, typename T>
 __global__ void __launch_bounds__(kThreads)
     kv_partial_kernel(const T *__restrict__ k, const T *__restrict__ v,
                       float *__restrict__ S_out, float *__restrict__ z_out,
-                      int H, int N, int split_len, const __grid_constant__ Gammas gam) {
+                      int H, int N, int split_len, int nsplit,
+                      const __grid_constant__ Gammas gam) {
   constexpr int RD = D / 16, RE = DV / 16;
   __shared__ __align__(16) float fk[kTok][D];
   __shared__ __align__(16) float vs[kTok][DV];
@@ -36,61 +40,63 @@ __global__ void __launch_bounds__(kThreads)
   const int td = tid >> 4, te = tid & 15;
   const int64_t bh = blockIdx.x;
   const int64_t BH = gridDim.x;
-  const int sp = blockIdx.y;
   const int h = (int)(bh % H);
-  const int j0 = sp * split_len;
-  const int j1 = min(N, j0 + split_len);
   const T *kh = k + bh * (int64_t)N * D;
   const T *vh = v + bh * (int64_t)N * DV;
   const double gamma = DECAY ? (double)gam.g[h] : 1.0;
+  // splits beyond the grid's y extent (at most 65535) are taken in strides
+  for (int sp = blockIdx.y; sp < nsplit; sp += gridDim.y) {
+    const int64_t j0 = (int64_t)sp * split_len;
+    const int j1 = (int)min((int64_t)N, j0 + split_len);
 
-  float acc[RD][RE] = {};
-  float zacc[RD] = {};
-  for (int t0 = j0; t0 < j1; t0 += kTok) {
-    const int nv = min(kTok, j1 - t0);
-    if (DECAY && tid < kTok) {
-      // gamma^(N-1-j), in fp64 then rounded once
-      wt[tid] = tid < nv ? (float)pow(gamma, (double)(N - 1 - (t0 + tid))) : 0.f;
-    }
-    if (DECAY) __syncthreads();
-    for (int i = tid; i < kTok * D; i += kThreads) {
-      const int t = i / D, d = i % D;
-      float x = 0.f;
-      if (t < nv) {
-        x = feat_f32<IDENT>(io<T>::load(kh + (int64_t)(t0 + t) * D + d));
-        if (DECAY) x *= wt[t];
+    float acc[RD][RE] = {};
+    float zacc[RD] = {};
+    for (int t0 = (int)j0; t0 < j1; t0 += kTok) {
+      const int nv = min(kTok, j1 - t0);
+      if (DECAY && tid < kTok) {
+        // gamma^(N-1-j), in fp64 then rounded once
+        wt[tid] = tid < nv ? (float)pow(gamma, (double)(N - 1 - (t0 + tid))) : 0.f;
       }
-      fk[t][d] = x;
-    }
-    for (int i = tid; i < kTok * DV; i += kThreads) {
-      const int t = i / DV, e = i % DV;
-      vs[t][e] = t < nv ? io<T>::load(vh + (int64_t)(t0 + t) * DV + e) : 0.f;
-    }
-    __syncthreads();
-    for (int s = 0; s < nv; ++s) {
-      float a[RD], b[RE];
-#pragma unroll
-      for (int i = 0; i < RD; ++i) a[i] = fk[s][td * RD + i];
-#pragma unroll
-      for (int j = 0; j < RE; ++j) b[j] = vs[s][te * RE + j];
-#pragma unroll
-      for (int i = 0; i < RD; ++i) {
-#pragma unroll
-        for (int j = 0; j < RE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        zacc[i] += a[i];
+      if (DECAY) __syncthreads();
+      for (int i = tid; i < kTok * D; i += kThreads) {
+        const int t = i / D, d = i % D;
+        float x = 0.f;
+        if (t < nv) {
+          x = feat_f32<IDENT>(io<T>::load(kh + (int64_t)(t0 + t) * D + d));
+          if (DECAY) x *= wt[t];
+        }
+        fk[t][d] = x;
       }
+      for (int i = tid; i < kTok * DV; i += kThreads) {
+        const int t = i / DV, e = i % DV;
+        vs[t][e] = t < nv ? io<T>::load(vh + (int64_t)(t0 + t) * DV + e) : 0.f;
+      }
+      __syncthreads();
+      for (int s = 0; s < nv; ++s) {
+        float a[RD], b[RE];
+#pragma unroll
+        for (int i = 0; i < RD; ++i) a[i] = fk[s][td * RD + i];
+#pragma unroll
+        for (int j = 0; j < RE; ++j) b[j] = vs[s][te * RE + j];
+#pragma unroll
+        for (int i = 0; i < RD; ++i) {
+#pragma unroll
+          for (int j = 0; j < RE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          zacc[i] += a[i];
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
-  }
-  const int64_t u = (int64_t)sp * BH + bh;
-  float *So = S_out + u * (int64_t)D * DV;
+    const int64_t u = (int64_t)sp * BH + bh;
+    float *So = S_out + u * (int64_t)D * DV;
 #pragma unroll
-  for (int i = 0; i < RD; ++i)
+    for (int i = 0; i < RD; ++i)
 #pragma unroll
-    for (int j = 0; j < RE; ++j) So[(td * RD + i) * DV + te * RE + j] = acc[i][j];
-  if (te == 0) {
+      for (int j = 0; j < RE; ++j) So[(td * RD + i) * DV + te * RE + j] = acc[i][j];
+    if (te == 0) {
 #pragma unroll
-    for (int i = 0; i < RD; ++i) z_out[u * D + td * RD + i] = zacc[i];
+      for (int i = 0; i < RD; ++i) z_out[u * D + td * RD + i] = zacc[i];
+    }
   }
 }
 
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kThreads)
   out[i] = s;
 }
 
-// grid (BH, ceil(N / kRowsPerCta)).
+// grid (BH, min(ceil(N / kRowsPerCta), 65535)).
 constexpr int kRowTile = 64;
 constexpr int kRowsPerCta = 256;
 
@@ -127,39 +133,43 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = tid; i < D * DV; i += kThreads) Ss[i] = S[bh * D * DV + i];
   for (int i = tid; i < D; i += kThreads) zs[i] = z[bh * D + i];
 
-  const int r_begin = blockIdx.y * kRowsPerCta;
-  const int r_end = min(N, r_begin + kRowsPerCta);
-  for (int r0 = r_begin; r0 < r_end; r0 += kRowTile) {
-    const int nv = min(kRowTile, r_end - r0);
-    __syncthreads();
-    for (int i = tid; i < kRowTile * D; i += kThreads) {
-      const int t = i / D, d = i % D;
-      fq[t * (D + 1) + d] = t < nv ? feat_f32<IDENT>(io<T>::load(qh + (int64_t)(r0 + t) * D + d)) : 0.f;
-    }
-    __syncthreads();
-    float acc[RT][RE] = {};
-    float dn[RT] = {};
-    for (int d = 0; d < D; ++d) {
-      float b[RE];
+  // row blocks beyond the grid's y extent (at most 65535) are taken in strides
+  const int nblk = (N + kRowsPerCta - 1) / kRowsPerCta;
+  for (int blk = blockIdx.y; blk < nblk; blk += gridDim.y) {
+    const int r_begin = blk * kRowsPerCta;
+    const int r_end = min(N, r_begin + kRowsPerCta);
+    for (int r0 = r_begin; r0 < r_end; r0 += kRowTile) {
+      const int nv = min(kRowTile, r_end - r0);
+      __syncthreads();
+      for (int i = tid; i < kRowTile * D; i += kThreads) {
+        const int t = i / D, d = i % D;
+        fq[t * (D + 1) + d] = t < nv ? feat_f32<IDENT>(io<T>::load(qh + (int64_t)(r0 + t) * D + d)) : 0.f;
+      }
+      __syncthreads();
+      float acc[RT][RE] = {};
+      float dn[RT] = {};
+      for (int d = 0; d < D; ++d) {
+        float b[RE];
 #pragma unroll
-      for (int j = 0; j < RE; ++j) b[j] = Ss[d * DV + te * RE + j];
-      const float zd = zs[d];
+        for (int j = 0; j < RE; ++j) b[j] = Ss[d * DV + te * RE + j];
+        const float zd = zs[d];
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+          const float a = fq[(tt * RT + i) * (D + 1) + d];
+          dn[i] = fmaf(a, zd, dn[i]);
+#pragma unroll
+          for (int j = 0; j < RE; ++j) acc[i][j] = fmaf(a, b[j], acc[i][j]);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < RT; ++i) {
-        const float a = fq[(tt * RT + i) * (D + 1) + d];
-        dn[i] = fmaf(a, zd, dn[i]);
+        const int t = tt * RT + i;
+        if (t < nv) {
+          const float dd = dn[i] + eps;
 #pragma unroll
-        for (int j = 0; j < RE; ++j) acc[i][j] = fmaf(a, b[j], acc[i][j]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < RT; ++i) {
-      const int t = tt * RT + i;
-      if (t < nv) {
-        const float dd = dn[i] + eps;
-#pragma unroll
-        for (int j = 0; j < RE; ++j)
-          io<T>::store(oh + (int64_t)(r0 + t) * DV + te * RE + j, acc[i][j] / dd);
+          for (int j = 0; j < RE; ++j)
+            io<T>::store(oh + (int64_t)(r0 + t) * DV + te * RE + j, acc[i][j] / dd);
+        }
       }
     }
   }
@@ -173,10 +183,10 @@ cudaError_t kv_typed(const void *k, const void *v, float *S, float *z,
   const int64_t nS = (int64_t)BH * D * DV, nz = (int64_t)BH * D;
   float *So = nsplit == 1 ? S : part;
   float *zo = nsplit == 1 ? z : part + (int64_t)nsplit * nS;
-  dim3 grid((unsigned)BH, (unsigned)nsplit);
+  dim3 grid((unsigned)BH, (unsigned)grid_y(nsplit));
   kv_partial_kernel<D, DV, DECAY, IDENT, T><<<grid, kThreads, 0, s>>>(
       static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N,
-      kSplitTokens, g);
+      kSplitTokens, nsplit, g);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || nsplit == 1) return err;
   kv_reduce_kernel<<<(unsigned)((nS + kThreads - 1) / kThreads), kThreads, 0, s>>>(
@@ -216,7 +226,7 @@ cudaError_t apply_typed(const void *q, const float *S, const float *z, void *o,
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  dim3 grid((unsigned)BH, (unsigned)((N + kRowsPerCta - 1) / kRowsPerCta));
+  dim3 grid((unsigned)BH, (unsigned)grid_y((N + kRowsPerCta - 1) / kRowsPerCta));
   kern<<<grid, kThreads, smem, s>>>(static_cast<const T *>(q), S, z,
                                     static_cast<T *>(o), N, eps);
   return cudaGetLastError();
@@ -240,9 +250,9 @@ cudaError_t kv_typed_n(const void *k, const void *v, float *S, float *z, float *
   const int64_t nS = (int64_t)BH * D * DV, nz = (int64_t)BH * D;
   float *So = nsplit == 1 ? S : part;
   float *zo = nsplit == 1 ? z : part + (int64_t)nsplit * nS;
-  dim3 grid((unsigned)BH, (unsigned)nsplit);
+  dim3 grid((unsigned)BH, (unsigned)grid_y(nsplit));
   kv_partial_kernel<D, DV, DECAY, false, T><<<grid, kThreads, 0, s>>>(
-      static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N, split_len, g);
+      static_cast<const T *>(k), static_cast<const T *>(v), So, zo, H, N, split_len, nsplit, g);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || nsplit == 1) return err;
   kv_reduce_kernel<<<(unsigned)((nS + kThreads - 1) / kThreads), kThreads, 0, s>>>(

@@ -35,3 +35,17 @@ def state_error(S, S_ref):
     num = np.max(np.abs(S - S_ref), axis=ax)
     den = np.maximum(np.max(np.abs(S_ref), axis=ax), 1e-30)
     return float((num / den).max())
+
+
+# Worst error per checked quantity, {name: (error, tolerance)}; printed at the
+# end of the run (tests/conftest.py) so that the margin to each tolerance is
+# visible without -s.
+MARGINS = {}
+
+
+def record(name, err, tol):
+    """Keep the worst error of one checked quantity for the end-of-run report."""
+    err = float(err)
+    if name not in MARGINS or err > MARGINS[name][0]:
+        MARGINS[name] = (err, float(tol))
+    return err
