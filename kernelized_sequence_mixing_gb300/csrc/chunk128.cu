@@ -119,13 +119,24 @@ enum Bar : int {
   kDrain = 21,
 };
 
-// Part boundaries (in chunks): equal parts.  The CTA of part p > 0 runs
-// phase A over part p - 1 and then, once every earlier part's sum is
-// published, phase C over part p; part 0 runs phase C only.  Every part
-// p >= 2 waits for the sums of all earlier parts, so the slowest phase A
-// sets the start of its phase C: equal parts keep those equal.
-__host__ __device__ __forceinline__ int part_begin(int p, int P, int nch_all) {
-  return chunk_part_begin(p, P, nch_all);
+// Part boundaries (in chunks).  The CTA of part p > 0 runs phase A over
+// part p - 1 and then, once every earlier part's sum is published, phase C
+// over part p; part 0 runs phase C only.
+//
+// Relay split (n0 > 0): part 0 has n0 chunks and the later parts share the
+// rest equally.  Part 0 starts phase C at once, so it can take more chunks
+// than the others; to keep part 1 from paying a phase A over all of them,
+// the CTA of part 0 publishes its running state after its first m0 chunks
+// (a checkpoint), and part 1's phase A covers only chunks [m0, n0), the
+// state before part 1 being gamma^(C (n0 - m0)) times the checkpoint plus
+// that sum.  Sizes are chosen so that the checkpoint and part 1's phase A
+// land together and all parts end together.  n0 = 0: equal parts, no
+// checkpoint.
+__host__ __device__ __forceinline__ int part_begin(int p, int P, int nch_all, int n0) {
+  if (n0 <= 0 || P <= 1) return chunk_part_begin(p, P, nch_all);
+  if (p <= 0) return 0;
+  if (p >= P) return nch_all;
+  return n0 + chunk_part_begin(p - 1, P - 1, nch_all - n0);
 }
 
 struct Chunk128Params {
@@ -147,6 +158,10 @@ struct Chunk128Params {
   const float *gate_suf, *gate_part;
   const int *skip;
   int BH, H, N, P;
+  // relay split (see part_begin): chunks of part 0 and the checkpoint
+  // position (0, 0: equal parts); the checkpoint is record P - 1 of its
+  // (batch, head); flag P - 1 counts the state warps that have written it
+  int n0, m0;
   float eps;
   Gammas lg;  // log2(gamma) per head
 };
@@ -290,10 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   // the part: chunks [cb, cb + nch) of this (batch, head); phase A runs
   // over the previous part, chunks [cbA, cbA + nA)
   const int nch_all = (N + kC - 1) / kC;
-  const int cb = part_begin(part, P, nch_all);
-  const int nch = part_begin(part + 1, P, nch_all) - cb;
+  const bool relay = P > 1 && p.n0 > 0 && p.m0 > 0;
+  const int cb = part_begin(part, P, nch_all, p.n0);
+  const int nch = part_begin(part + 1, P, nch_all, p.n0) - cb;
   const bool hasA = part > 0;
-  const int cbA = hasA ? part_begin(part - 1, P, nch_all) : 0;
+  // part 1 of a relay split sums only the chunks of part 0 after the checkpoint
+  const int cbA = hasA ? (relay && part == 1 ? p.m0 : part_begin(part - 1, P, nch_all, p.n0)) : 0;
   const int nA = hasA ? cb - cbA : 0;
   const float lg = DECAY ? p.lg.g[bh % p.H] : 0.f;
   const bool final_state = p.S_out != nullptr && part == P - 1;
@@ -303,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
     WC = c < 1.f ? 1 : (c > 64.f ? 64 : static_cast<int>(c));
   }
   const int W = kC * WC;
-  auto phase_a_chunk = [&](int i) { return part == 1 ? i : nA - 1 - i; };
+  auto phase_a_chunk = [&](int i) { return part == 1 && !relay ? i : nA - 1 - i; };
   auto scale2 = [&](float e) -> uint32_t {  // gamma^e as a bf16 pair
     const float f = DECAY ? exp2f(e * lg) : 1.f;
     return pack_bf16x2(f, f);
@@ -314,8 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   // the chunks of parts 1, 2, ... last first, so that the tiles the owner of
   // that part reads first in its phase C are the most recent in L2; part 0
   // (read in phase C from time zero) goes first chunk first, ahead of its
-  // owner.  All 16 compute warps share the map: warp u maps rows
-  // 32 (u % 4) + lane, 16-byte chunks [4 (u / 4), + 4) of the row (box u / 8).
+  // owner, unless a checkpoint cuts it (then last first, like the others).
+  // All 16 compute warps share the map: warp u maps rows 32 (u % 4) + lane,
+  // 16-byte chunks [4 (u / 4), + 4) of the row (box u / 8).
   auto phase_a_map = [&](int u) {
     const int r = 32 * (u & 3) + lane, quarter = u >> 2;
     for (int i = 0; i < nA; ++i) {
@@ -347,8 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   // is published for the later parts that need it.  A_j, j < part - 1, was
   // published by the CTA of part j + 1 (a flag per record, release/acquire
   // at GPU scope; parts are started in part-major order by an atomic ticket,
-  // so every wait ends).  T = gamma^W S0 goes to tensor memory and, in
-  // bf16, to [T | z].
+  // so every wait ends).  With a relay split, part 1 adds part 0's checkpoint
+  // to its phase A before publishing A_0 (then the whole state before part
+  // 1).  T = gamma^W S0 goes to tensor memory and, in bf16, to [T | z].
   auto look_back = [&](int u) {
     const int qd = u & 3, g4 = u >> 2;
     const int d = 32 * qd + lane;
@@ -364,15 +383,50 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       tmem_ld32(tS, acc);
       if (zcol) accz = tmem_ld1(tZ);
       tmem_wait_ld();
-      if (part < P - 1) {  // A_(part-1) is read by the parts after this one
-        float *rec = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          __stcg(reinterpret_cast<float4 *>(rec) + (8 * g4 + q) * kD + d,
-                 make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
-        if (zcol) __stcg(rec + kD * kDV + d, accz);
-        __threadfence();
+    }
+    if (relay && part == 1) {
+      // the state before part 1: the checkpoint of part 0 (the state after
+      // its first m0 chunks, relative to token m0 C - 1), carried to token
+      // cb C - 1, plus this CTA's phase A over chunks [m0, cb)
+      if (tid == 0) {
+        const long long t0 = clock64();
+        const int *f = p.ws_flag + bh * P + P - 1;  // one count per state warp
+        while (ld_acquire_gpu(f) < 4) {
+          if (*abort_flag) break;
+          if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicAdd(p.timeouts, 1u);
+            break;
+          }
+          __nanosleep(32);
+        }
       }
+      named_sync(1, 512);
+      if (!*abort_flag) {
+        const float wk = DECAY ? exp2f(static_cast<float>((cb - p.m0) * kC) * lg) : 1.f;
+        const float *ck = p.rec + (static_cast<size_t>(bh) * P + P - 1) * kRec;
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __ldcg(reinterpret_cast<const float4 *>(ck) + (8 * g4 + q) * kD + d);
+        const float vz = zcol ? __ldcg(ck + kD * kDV + d) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          acc[4 * q] = fmaf(wk, v[q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(wk, v[q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(wk, v[q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(wk, v[q].w, acc[4 * q + 3]);
+        }
+        accz = fmaf(wk, vz, accz);
+      }
+    }
+    if (hasA && part < P - 1) {  // A_(part-1) is read by the parts after this one
+      float *rec = p.rec + (static_cast<size_t>(bh) * P + part - 1) * kRec;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        __stcg(reinterpret_cast<float4 *>(rec) + (8 * g4 + q) * kD + d,
+               make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+      if (zcol) __stcg(rec + kD * kDV + d, accz);
+      __threadfence();
     }
     named_sync(1, 512);
     if (hasA && part < P - 1 && tid == 0) st_release_gpu(p.ws_flag + bh * P + part - 1, 1);
@@ -401,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         if (GATED) wg *= __ldg(p.gate_part + (static_cast<size_t>(bh) * P + j + 1) * kD + d);
         const float wj =
             GATED ? wg
-                  : (DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1, P, nch_all)) * kC) * lg)
+                  : (DECAY ? exp2f(static_cast<float>((cb - part_begin(j + 1, P, nch_all, p.n0)) * kC) * lg)
                            : 1.f);
         const float *rec = p.rec + (static_cast<size_t>(bh) * P + j) * kRec;
         float4 v[8];
@@ -683,6 +737,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
         const float fr =
             GATED ? __ldg(p.gate_prod + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cb + i) * kD + d)
                   : gW;
+        if (relay && part == 0 && i == p.m0) {
+          // relay split, part 0 after m0 chunks: the checkpoint, T carried
+          // from the end of the window of chunk i - 1 back to token i C - 1;
+          // this warp's rows are written and fenced, then counted
+          float *ck = p.rec + (static_cast<size_t>(bh) * P + P - 1) * kRec;
+          const float fk = DECAY ? exp2f(static_cast<float>(((i - 1) % WC + 1) * kC - W) * lg) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < kDV / 32; ++cc) {
+            float x[32];
+            tmem_ld32(tT + 32 * cc, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(reinterpret_cast<float4 *>(ck) + (8 * cc + q) * kD + d,
+                     make_float4(fk * x[4 * q], fk * x[4 * q + 1], fk * x[4 * q + 2], fk * x[4 * q + 3]));
+          }
+          const float zd = tmem_ld1(tT + kDV);
+          tmem_wait_ld();
+          __stcg(ck + kD * kDV + d, fk * zd);
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(p.ws_flag + bh * P + P - 1, 1);
+        }
 #pragma unroll 1
         for (int cc = 0; cc < kDV / 32; cc += 2) {
           float x0[32], x1[32];
@@ -834,6 +911,31 @@ int num_sms128() {
   return v;
 }
 
+// Relay split (see part_begin) from a cost model in units of one phase-C
+// chunk: a phase-A chunk costs kPhaseARatio of one (it maps and multiplies
+// k and v only), and a part that waits for earlier sums starts kLookBack
+// chunks after they are published.  Part 0 runs n0 chunks from time 0; part
+// 1 sums n0 - m0 chunks of it while part 0 reaches its checkpoint m0; parts
+// 2.. sum the whole part before them, which takes as long when every later
+// part has n = n0 / (1 + ratio) - kLookBack chunks; all parts then end
+// together.
+constexpr double kPhaseARatio = 0.40;
+constexpr double kLookBack = 1.5;
+
+void relay_split(int P, int nch, int *n0, int *m0) {
+  *n0 = 0;
+  *m0 = 0;
+  if (P < 2) return;
+  const double r = kPhaseARatio;
+  int a = static_cast<int>((nch + (P - 1) * kLookBack) / (1.0 + (P - 1) / (1.0 + r)) + 0.5);
+  if (a > nch - (P - 1)) a = nch - (P - 1);  // every later part keeps a chunk
+  int m = static_cast<int>(r * a / (1.0 + r) + 0.5);
+  if (m > a - 1) m = a - 1;
+  if (a < 2 || m < 1) return;  // too short to gain: equal parts
+  *n0 = a;
+  *m0 = m;
+}
+
 size_t flag_bytes(int BH, int P) {
   const size_t flags = (static_cast<size_t>(BH) * P + 1) * sizeof(int);
   return (flags + 255) & ~static_cast<size_t>(255);
@@ -890,6 +992,7 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
   prm.S_out = S_out;
   prm.z_out = z_out;
   prm.lg = log2_gammas(g, p.H, p.decay);
+  relay_split(P, (p.N + kC - 1) / kC, &prm.n0, &prm.m0);
   if (P > 1) {
     if (!ws) return cudaErrorInvalidValue;
     // flags and ticket start at zero; the records need no initialisation

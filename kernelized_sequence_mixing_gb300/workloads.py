@@ -79,8 +79,11 @@ WORKLOADS = {
     # non-causal, bf16, B8 H16 N65536 D=Dv=64, seed 3
     "noncausal_bf16_n65536": Workload("noncausal_bf16_n65536", False, 8, 16,
                                       65536, 64, 64, torch.bfloat16, 0.5, 3),
-    # decode: 256 sequences x H32, D=Dv=128; prefill of 512 tokens (seed 4),
-    # then 1024 single-token steps with fresh inputs from seed 1000 + t
+    # the same at an eighth of the sequence length (the same CTA grid per
+    # pass, 537 MB of inputs and output, above the L2 size): the case for
+    # multi-pass counter captures
+    "noncausal_bf16_n8192": Workload("noncausal_bf16_n8192", False, 8, 16,
+                                     8192, 64, 64, torch.bfloat16, 0.5, 3),
     # gated (one gate per key feature and token), bf16, B2 H16 N16384
     # D=Dv=128, gates U[0.9, 1) from seed 5 + 1
     "gla_bf16_n16384": Workload("gla_bf16_n16384", True, 2, 16, 16384, 128,
@@ -99,6 +102,8 @@ WORKLOADS = {
     "decode_gated_bf16_h32": Workload("decode_gated_bf16_h32", True, 256, 32, 512, 128,
                                       128, torch.bfloat16, 0.5, 4, steps=1024,
                                       step_seed0=1000, gated=True),
+    # decode: 256 sequences x H32, D=Dv=128; prefill of 512 tokens (seed 4),
+    # then 1024 single-token steps with fresh inputs from seed 1000 + t
     "decode_bf16_h32": Workload("decode_bf16_h32", True, 256, 32, 512, 128,
                                 128, torch.bfloat16, 0.5, 4, steps=1024,
                                 step_seed0=1000),
