@@ -40,7 +40,7 @@ METRICS = {
     "decode_gated": "gated recurrent decode step tokens/s and % HBM roofline, 1×GB300",
     "gated": "gated linear-attn fwd tokens/s and % roofline (HBM, or fp32 ALU on CUDA cores), 1×GB300",
     "favor": "Performer (FAVOR+) causal linear-attn fwd tokens/s and % HBM roofline, 1×GB300",
-    "backward": "causal linear-attn bwd (dq, dk, dv) tokens/s and % fp32 ALU roofline, 1×GB300",
+    "backward": "causal linear-attn bwd (dq, dk, dv) tokens/s and % roofline (HBM on tensor cores, fp32 ALU on CUDA cores), 1×GB300",
 }
 
 
@@ -173,7 +173,7 @@ GATED_SOURCES = ("gla_simt.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 # sources of the Performer path (feature kernel, then the causal kernel)
 FAVOR_SOURCES = ("favor.cu", "chunk128.cu", "tc_common.cuh", "common.cuh")
 # sources of the backward pass
-BACKWARD_SOURCES = ("backward_simt.cu", "common.cuh")
+BACKWARD_SOURCES = ("backward_tc.cu", "chunk_tc.cu", "backward_simt.cu", "tc_common.cuh", "common.cuh")
 # sources of the decode step, the 64-token tensor-core kernel (causal with
 # D or Dv = 64; the non-causal sums and read-out with its part scan) and the
 # fp32 CUDA-core kernels
@@ -446,6 +446,7 @@ def run_ours(args, w):
 
     ws, rank, local = dist_env()
     gated_tc = False
+    bwd_tc = False
     final_state = bool(getattr(args, "final_state", False))
     if final_state and (w.steps or not w.causal or w.gated or w.favor_r or w.backward):
         raise SystemExit("--final-state applies to the causal forward workloads")
@@ -540,7 +541,8 @@ def run_ours(args, w):
         grads = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
         od = grads[2]
         ncopy = 1
-        launches_per_step = la.backward_launches(w.B, w.H, w.N, w.D, w.Dv)
+        launches_per_step = la.backward_launches(w.B, w.H, w.N, w.D, w.Dv, gamma=g, dtype=w.dtype)
+        bwd_tc = la.backward_kernel(w.B, w.H, w.N, w.D, w.Dv, gamma=g, dtype=w.dtype) == "tensor-core"
 
         def step():
             la.backward(qd, kd, vd, dod, eps=w.eps, dq=grads[0], dk=grads[1], dv=grads[2])
@@ -743,7 +745,7 @@ def run_ours(args, w):
         "metric": workload_metric(w), "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": compute_dtype(w, gated_tc),
+        "dtype": compute_dtype(w, gated_tc, bwd_tc),
         "data": "synthetic",
         "config": dict(workload_config(w), **({"final_state": "S [B][H][D][Dv] and z [B][H][D] "
                                                "fp32 written after the last token"}
@@ -755,7 +757,7 @@ def run_ours(args, w):
                            f"over {ncopy} input/output copies")),
         "roofline": roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src,
                                    tc_peak, traffic, launches_per_step,
-                                   gated_tc=bool(w.gated and gated_tc)),
+                                   gated_tc=bool(w.gated and gated_tc), bwd_tc=bwd_tc),
         "cpu_baseline": cpu,
         "e2e": None if e2e_s is None else {
             "value": tokens_rank * ws / e2e_s, "unit": "tokens/s",
@@ -881,12 +883,14 @@ def time_extra(la, name, dev, hbm_peak, quick):
     return entry
 
 
-def compute_dtype(w, gated_tc=False):
+def compute_dtype(w, gated_tc=False, bwd_tc=False):
     """The arithmetic type the timed path computes in: bf16 tensor-core
-    operands (fp32 accumulation) for the bf16 forward kernels, fp32 for the
-    CUDA-core paths (fp32 inputs, the decode steps' fp32 state update, the
-    CUDA-core gated form, the backward)."""
-    if w.backward or w.steps:
+    operands (fp32 accumulation) for the bf16 forward kernels and the
+    tensor-core backward, fp32 for the CUDA-core paths (fp32 inputs, the
+    decode steps' fp32 state update, the CUDA-core gated form and backward)."""
+    if w.backward:
+        return "bf16" if bwd_tc else "f32"
+    if w.steps:
         return "f32"
     if w.gated and not gated_tc:
         return "f32"
@@ -894,15 +898,16 @@ def compute_dtype(w, gated_tc=False):
 
 
 def roofline_entry(w, byts, flops, launch_ms, hbm_peak, peak_src, tc_peak, traffic,
-                   launches, gated_tc=False):
-    """HBM roofline for the forward and decode kernels; for the gated
-    CUDA-core kernel, the fp32 ALU roofline (its bound), with the HBM figure
-    beside it.  Timed over the whole step (all of its launches)."""
+                   launches, gated_tc=False, bwd_tc=False):
+    """HBM roofline for the forward, decode and tensor-core backward kernels;
+    for the gated and backward CUDA-core kernels, the fp32 ALU roofline
+    (their bound), with the HBM figure beside it.  Timed over the whole step
+    (all of its launches)."""
     achieved_gbs = byts / (launch_ms / 1e3) / 1e9
     tflops = flops / (launch_ms / 1e3) / 1e12
     hbm_src = (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                else "fallback")
-    if (w.gated and not w.steps and not gated_tc) or w.backward:
+    if (w.gated and not w.steps and not gated_tc) or (w.backward and not bwd_tc):
         return {"bound": "alu", "achieved": tflops, "peak": ALU_FP32_TFLOPS,
                 "unit": "TFLOP/s", "frac": tflops / ALU_FP32_TFLOPS, "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",

@@ -280,10 +280,16 @@ LA_API la_status_t la_forward_favor(const void *q, const void *k, const void *v,
  * "Recurrent Reformulation"; the forward it differentiates is la_forward's.
  * The library recomputes o and d itself (the caller keeps no forward
  * state).  q, k, dq, dk: [B][H][N][D]; v, dO, dv: [B][H][N][Dv]; all of
- * `dtype`; fp32 arithmetic on CUDA cores in a stream-ordered workspace of
- * B*H*N*(4D + 6Dv + 16)*4 bytes plus the per-part states of the sequence
- * split (cudaMallocAsync on `stream`).  No gradient may overlap an input or
- * another gradient.  Errors as la_forward.
+ * `dtype`.  For LA_BF16 with Dv = 64 and every gamma >= 0.35 the sums run on
+ * tcgen05 tensor cores (la_backward_kernel = 1): the forward's undivided
+ * numerators and normalisers, then three decayed causal products with bf16
+ * operands and fp32 accumulation (dq forward, dk and dv over token-reversed
+ * operands), in a stream-ordered workspace of about B*H*N*(8 D + 1412)
+ * bytes.  Otherwise fp32 arithmetic on CUDA cores in a stream-ordered
+ * workspace of B*H*N*(4D + 6Dv + 16)*4 bytes plus the per-part states of the
+ * sequence split.  Workspaces are taken with cudaMallocAsync on `stream`.
+ * No gradient may overlap an input or another gradient.  Errors as
+ * la_forward.
  */
 LA_API la_status_t la_backward(const void *q, const void *k, const void *v, const void *dO,
                                void *dq, void *dk, void *dv, int B, int H, int N, int D,
@@ -291,12 +297,24 @@ LA_API la_status_t la_backward(const void *q, const void *k, const void *v, cons
                                void *stream);
 
 /*
- * Number of kernels one la_backward call with these sizes launches (it
- * depends on how the sequence is split across the current device's SMs), 0
- * for an empty call, or a negative la_status_t (negated) for invalid sizes.
- * Host-only apart from reading the current device's SM count.
+ * Which kernels la_backward runs for these arguments: 1 = tcgen05 tensor
+ * cores (bf16, Dv = 64, D in {64, 128}, every gamma >= 0.35), 0 = fp32 CUDA
+ * cores, or a negative la_status_t (negated) for invalid arguments.  gamma
+ * as in la_backward (host array or NULL).  Host-only apart from reading the
+ * current device's SM count.
  */
-LA_API int la_backward_launches(int B, int H, int N, int D, int Dv);
+LA_API int la_backward_kernel(int B, int H, int N, int D, int Dv, const float *gamma,
+                              la_dtype_t dtype);
+
+/*
+ * Number of kernels one la_backward call with these arguments launches (on
+ * CUDA cores it depends on how the sequence is split across the current
+ * device's SMs), 0 for an empty call, or a negative la_status_t (negated)
+ * for invalid arguments.  Host-only apart from reading the current device's
+ * SM count.
+ */
+LA_API int la_backward_launches(int B, int H, int N, int D, int Dv, const float *gamma,
+                                la_dtype_t dtype);
 
 /*
  * Which kernel la_forward would run for a causal call with these arguments:

@@ -31,7 +31,7 @@ from . import workloads  # noqa: F401  (seeded input generators)
 __all__ = ["forward", "prefill_state", "decode_step", "forward_state",
            "forward_gated", "decode_gated", "favor_features", "forward_favor", "backward",
            "status_string",
-           "device_wait_timeouts", "causal_kernel",
+           "device_wait_timeouts", "causal_kernel", "backward_kernel",
            "load_library", "library_path", "LinAttnError", "workloads"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -90,8 +90,10 @@ def load_library() -> ctypes.CDLL:
             lib.la_backward.restype = I
             lib.la_gated_kernel.argtypes = [I, I, I, I, I, I, I]
             lib.la_gated_kernel.restype = I
-            lib.la_backward_launches.argtypes = [I, I, I, I, I]
+            lib.la_backward_launches.argtypes = [I, I, I, I, I, FP, I]
             lib.la_backward_launches.restype = I
+            lib.la_backward_kernel.argtypes = [I, I, I, I, I, FP, I]
+            lib.la_backward_kernel.restype = I
             lib.la_causal_kernel.argtypes = [I, I, I, I, I, FP, I]
             lib.la_causal_kernel.restype = I
             lib.la_wait_selftest.argtypes = [ctypes.c_longlong, ctypes.POINTER(I)]
@@ -477,13 +479,22 @@ def backward(q, k, v, do, gamma=None, eps=1e-6, dq=None, dk=None, dv=None):
     return dq, dk, dv
 
 
-def backward_launches(B, H, N, D, Dv) -> int:
-    """Kernels one backward() call with these sizes launches on the current
-    device."""
-    n = load_library().la_backward_launches(B, H, N, D, Dv)
+def backward_launches(B, H, N, D, Dv, gamma=None, dtype=torch.bfloat16) -> int:
+    """Kernels one backward() call with these arguments launches on the
+    current device."""
+    n = load_library().la_backward_launches(B, H, N, D, Dv, _gamma_arg(gamma, H), _DTYPES[dtype])
     if n < 0:
         raise LinAttnError("la_backward_launches", -n)
     return int(n)
+
+
+def backward_kernel(B, H, N, D, Dv, gamma=None, dtype=torch.bfloat16) -> str:
+    """Which kernels backward() runs: "tensor-core" (bf16, Dv = 64, every
+    decay >= 0.35) or "cuda-core".  Host-only query."""
+    code = load_library().la_backward_kernel(B, H, N, D, Dv, _gamma_arg(gamma, H), _DTYPES[dtype])
+    if code < 0:
+        raise LinAttnError("la_backward_kernel", -code)
+    return "tensor-core" if code == 1 else "cuda-core"
 
 
 def gated_kernel(B, H, N, D, Dv, dtype=torch.bfloat16, want_state=False) -> str:

@@ -151,7 +151,64 @@ struct ChunkParams {
   int BH, H, N, P, rec_parts;
   float eps;
   Gammas lg;  // log2(gamma) per head
+  // causal-mode epilogue in place of o = O[:, :Dv] / (O[:, Dv] + eps):
+  //   raw:  out_raw [B*H][N][Dv] fp32 = O[t, :Dv] and den_raw [B*H][N] fp32 =
+  //         O[t, Dv] (the undivided numerators and normalisers);
+  //   grad: grad_out [B*H][N][Dv] bf16 = O[t, :Dv] times phi'(x) elementwise,
+  //         x = grad_in (bf16 [B*H][N][Dv]) at the same row, or 1 when
+  //         grad_in is null; rev: row N - 1 - t of grad_out and grad_in
+  //         (the output of a product over token-reversed operands, stored in
+  //         token order).  phi'(x) = 1 for x > 0, e^x otherwise.
+  float *out_raw, *den_raw;
+  __nv_bfloat16 *grad_out;
+  const __nv_bfloat16 *grad_in;
+  int rev;
 };
+
+// One output half-row (64 columns, starting at column c0) of the causal
+// mode's epilogue: o = x / (den + eps) in bf16, or one of the raw and
+// gradient forms (ChunkParams).
+__device__ __forceinline__ void emit_half(const ChunkParams &p, size_t row, size_t grow, int DV, int c0,
+                                          const float *x, float den, float inv) {
+  if (p.out_raw) {
+    float4 *dst = reinterpret_cast<float4 *>(p.out_raw + row * DV + c0);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    if (c0 == 0) p.den_raw[row] = den;
+  } else if (p.grad_out) {
+    uint4 *dst = reinterpret_cast<uint4 *>(p.grad_out + grow * DV + c0);
+    const uint4 *src = p.grad_in ? reinterpret_cast<const uint4 *>(p.grad_in + grow * DV + c0) : nullptr;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float m[8];
+      if (src) {
+        const uint4 w = __ldg(src + q);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(wv[e] << 16), b = __uint_as_float(wv[e] & 0xffff0000u);
+          m[2 * e] = a > 0.f ? 1.f : __expf(a);
+          m[2 * e + 1] = b > 0.f ? 1.f : __expf(b);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m[e] = 1.f;
+      }
+      dst[q] = make_uint4(pack_bf16x2(x[8 * q] * m[0], x[8 * q + 1] * m[1]),
+                          pack_bf16x2(x[8 * q + 2] * m[2], x[8 * q + 3] * m[3]),
+                          pack_bf16x2(x[8 * q + 4] * m[4], x[8 * q + 5] * m[5]),
+                          pack_bf16x2(x[8 * q + 6] * m[6], x[8 * q + 7] * m[7]));
+    }
+  } else {
+    uint4 *dst = reinterpret_cast<uint4 *>(p.o + row * DV + c0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      dst[q] = make_uint4(pack_bf16x2(x[8 * q + 0] * inv, x[8 * q + 1] * inv),
+                          pack_bf16x2(x[8 * q + 2] * inv, x[8 * q + 3] * inv),
+                          pack_bf16x2(x[8 * q + 4] * inv, x[8 * q + 5] * inv),
+                          pack_bf16x2(x[8 * q + 6] * inv, x[8 * q + 7] * inv));
+  }
+}
 
 // phi and the row scales in place on NB boxes of 64 rows x 128 bytes.  Thread
 // tp (0..127) handles the 16-byte chunks tp + 128 m of every box, which lie in
@@ -717,7 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       const uint32_t tO = tmem_addr(tmem, 32 * w, L::kColO + b * NA);
       const int nv = min(kC, N - (cb + i) * kC);
       const bool row_ok = lane < 16 && t < nv;
-      __nv_bfloat16 *orow = p.o + (static_cast<size_t>(bh) * N + (cb + i) * kC + t) * DV;
+      // this thread's row of the output (and its place in token order for a
+      // product over token-reversed operands)
+      const int tok = (cb + i) * kC + t;
+      const size_t row = static_cast<size_t>(bh) * N + tok;
+      const size_t grow = static_cast<size_t>(bh) * N + (p.rev ? N - 1 - tok : tok);
       float x[64], dz[16];
       tmem_ld16(tO + DV, dz);
       tmem_ld32(tO, x);
@@ -729,13 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&O_free[b]);
       }
-      if (row_ok) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<uint4 *>(orow)[q] = make_uint4(
-              pack_bf16x2(x[8 * q + 0] * inv, x[8 * q + 1] * inv), pack_bf16x2(x[8 * q + 2] * inv, x[8 * q + 3] * inv),
-              pack_bf16x2(x[8 * q + 4] * inv, x[8 * q + 5] * inv), pack_bf16x2(x[8 * q + 6] * inv, x[8 * q + 7] * inv));
-      }
+      if (row_ok) emit_half(p, row, grow, DV, 0, x, dz[0], inv);
       if (DV == 128) {
         tmem_ld32(tO + 64, x);
         tmem_ld32(tO + 96, x + 32);
@@ -743,13 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&O_free[b]);
-        if (row_ok) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4 *>(orow + 64)[q] = make_uint4(
-                pack_bf16x2(x[8 * q + 0] * inv, x[8 * q + 1] * inv), pack_bf16x2(x[8 * q + 2] * inv, x[8 * q + 3] * inv),
-                pack_bf16x2(x[8 * q + 4] * inv, x[8 * q + 5] * inv), pack_bf16x2(x[8 * q + 6] * inv, x[8 * q + 7] * inv));
-        }
+        if (row_ok) emit_half(p, row, grow, DV, 64, x, dz[0], inv);
       }
     }
   } else if (warp >= kWarpS) {
@@ -1086,6 +1135,34 @@ cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int
   if (P > 1) {
     if (!ws) return cudaErrorInvalidValue;
     // flags and ticket start at zero; the records need no initialisation
+    const size_t fb = causal_flag_bytes(BH, P);
+    prm.ws_flag = static_cast<int *>(ws);
+    prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;
+    prm.rec = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + fb);
+    cudaError_t e = cudaMemsetAsync(ws, 0, (static_cast<size_t>(BH) * P + 1) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_mode<kCausal>(prm, p.decay, p.ident, p.D, p.Dv, BH * P, s);
+}
+
+cudaError_t launch_causal_chunk_epilogue(const Problem &p, const Gammas &g, void *ws, int P,
+                                         cudaStream_t s, const ChunkEpilogue &ep) {
+  if (!chunk_tc_supported(p, g) || !(ep.out_raw ? ep.den_raw != nullptr : ep.grad_out != nullptr))
+    return cudaErrorNotSupported;
+  const int BH = p.B * p.H;
+  ChunkParams prm = {};
+  if (!setup_params(&prm, p.q, p.k, p.v, BH, p.N, p.D, p.Dv, p.H, g, p.decay))
+    return cudaErrorNotSupported;
+  prm.out_raw = ep.out_raw;
+  prm.den_raw = ep.den_raw;
+  prm.grad_out = ep.out_raw ? nullptr : ep.grad_out;
+  prm.grad_in = ep.grad_in;
+  prm.rev = ep.rev;
+  prm.P = P;
+  prm.rec_parts = P;
+  prm.eps = p.eps;
+  if (P > 1) {
+    if (!ws) return cudaErrorInvalidValue;
     const size_t fb = causal_flag_bytes(BH, P);
     prm.ws_flag = static_cast<int *>(ws);
     prm.ws_ticket = prm.ws_flag + static_cast<size_t>(BH) * P;

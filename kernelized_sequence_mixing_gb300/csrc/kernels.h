@@ -1,5 +1,6 @@
 // Host-side launchers of the library's kernels (internal to the library).
 #pragma once
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,6 +54,20 @@ size_t chunk_causal_workspace_bytes(int BH, int P, int D, int Dv);
 Gammas log2_gammas(const Gammas &g, int H, bool decay);
 cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int P,
                                 cudaStream_t s);
+// The causal chunk kernel with another epilogue in place of o = numerators /
+// (normaliser + eps) (p.o unused): out_raw [B*H][N][Dv] and den_raw [B*H][N]
+// fp32, the undivided numerators and normalisers; or grad_out [B*H][N][Dv]
+// bf16, the numerators times phi'(grad_in) elementwise (factor 1 when
+// grad_in is null), at row N - 1 - t for rev (a product over token-reversed
+// operands stored back in token order).
+struct ChunkEpilogue {
+  float *out_raw, *den_raw;
+  __nv_bfloat16 *grad_out;
+  const __nv_bfloat16 *grad_in;
+  int rev;
+};
+cudaError_t launch_causal_chunk_epilogue(const Problem &p, const Gammas &g, void *ws, int P,
+                                         cudaStream_t s, const ChunkEpilogue &ep);
 // The causal kernel with 128-token chunks for D = Dv = 128 (chunk128.cu):
 // bf16, every decay >= 0.61; workspace (flags and inclusive states) for P
 // parts, 0 for one part.
@@ -157,5 +172,13 @@ size_t backward_workspace_bytes(int BH, int N, int D, int Dv);
 int backward_launches(int BH, int N, int D, int Dv);  // kernels one call launches
 cudaError_t launch_backward(const Problem &p, const void *dO, void *dq, void *dk, void *dv,
                             const Gammas &g, void *ws, cudaStream_t s);
+// The same on tensor cores (backward_tc.cu) for bf16, Dv = 64, D in {64,
+// 128} and the 64-token chunk kernel's decay envelope: the forward's
+// undivided n and d, a prep kernel, three gradient products.
+bool backward_tc_supported(const Problem &p, const Gammas &g);
+size_t backward_tc_workspace_bytes(int BH, int N, int D);
+int backward_tc_launches();
+cudaError_t launch_backward_tc(const Problem &p, const void *dO, void *dq, void *dk, void *dv,
+                               const Gammas &g, void *ws, cudaStream_t s);
 
 }  // namespace linattn

@@ -496,20 +496,35 @@ la_status_t la_backward(const void *q, const void *k, const void *v, const void 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Problem p{q, k, v, nullptr, B, H, N, D, Dv, decay, eps, dtype == LA_F32 ? kF32 : kBF16};
+  // tensor cores for bf16 with Dv = 64 inside the chunk kernel's decay
+  // envelope; the fp32 CUDA-core kernels otherwise
+  const bool tc = backward_tc_supported(p, g);
   void *ws = nullptr;
-  if (cudaMallocAsync(&ws, backward_workspace_bytes(B * H, N, D, Dv), s) != cudaSuccess)
-    return LA_ERR_CUDA;
-  const cudaError_t e = launch_backward(p, dO, dq, dk, dv, g, ws, s);
+  const size_t wsb = tc ? backward_tc_workspace_bytes(B * H, N, D) : backward_workspace_bytes(B * H, N, D, Dv);
+  if (cudaMallocAsync(&ws, wsb, s) != cudaSuccess) return LA_ERR_CUDA;
+  const cudaError_t e = tc ? launch_backward_tc(p, dO, dq, dk, dv, g, ws, s)
+                           : launch_backward(p, dO, dq, dk, dv, g, ws, s);
   const cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(ef);
 }
 
-int la_backward_launches(int B, int H, int N, int D, int Dv) {
-  const la_status_t st = check_sizes(B, H, N, D, Dv, LA_F32);
+int la_backward_kernel(int B, int H, int N, int D, int Dv, const float *gamma, la_dtype_t dtype) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
   if (st != LA_OK) return -static_cast<int>(st);
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return -static_cast<int>(st);
+  const Problem p{nullptr, nullptr, nullptr, nullptr, B, H, N > 0 ? N : 1, D, Dv, decay, 0.f,
+                  dtype == LA_F32 ? kF32 : kBF16};
+  return backward_tc_supported(p, g) ? 1 : 0;
+}
+
+int la_backward_launches(int B, int H, int N, int D, int Dv, const float *gamma, la_dtype_t dtype) {
+  const int path = la_backward_kernel(B, H, N, D, Dv, gamma, dtype);
+  if (path < 0) return path;
   if ((int64_t)B * H * N == 0) return 0;
-  return backward_launches(B * H, N, D, Dv);
+  return path == 1 ? backward_tc_launches() : backward_launches(B * H, N, D, Dv);
 }
 
 la_status_t la_wait_selftest(long long cycles, int *gave_up) {

@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
-              "la_backward", "la_backward_launches", "la_gated_kernel", "la_wait_selftest",
+              "la_backward", "la_backward_launches", "la_backward_kernel", "la_gated_kernel", "la_wait_selftest",
               "la_status_string", "la_causal_kernel",
               "la_device_wait_timeouts"):
         assert s in syms
@@ -262,13 +262,31 @@ def test_backward_launches_rejects_bad_sizes(lib):
     give the negated status, an empty call launches nothing.  (Valid sizes
     read the device's SM count, so they are left to the GPU tests.)"""
     L = lib.la_backward_launches
-    assert L(-1, 2, 8, 64, 64) == -INVALID
-    assert L(1, 2, 8, 0, 64) == -INVALID
-    assert L(1, 2, 8, 96, 64) == -UNSUPPORTED
-    assert L(1, 300, 8, 64, 64) == -UNSUPPORTED               # more heads than supported
-    assert L(1 << 16, 1 << 8, 1 << 8, 64, 64) == -UNSUPPORTED  # 2^32 tokens
-    assert L(0, 2, 8, 64, 64) == 0
-    assert L(1, 2, 0, 128, 128) == 0
+    L.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_int]
+    assert L(-1, 2, 8, 64, 64, None, F32) == -INVALID
+    assert L(1, 2, 8, 0, 64, None, F32) == -INVALID
+    assert L(1, 2, 8, 96, 64, None, F32) == -UNSUPPORTED
+    assert L(1, 300, 8, 64, 64, None, F32) == -UNSUPPORTED               # more heads than supported
+    assert L(1 << 16, 1 << 8, 1 << 8, 64, 64, None, F32) == -UNSUPPORTED  # 2^32 tokens
+    assert L(1, 2, 8, 64, 64, None, 7) == -INVALID                      # unknown dtype
+    assert L(1, 2, 8, 64, 64, (ctypes.c_float * 2)(0.5, 1.5), BF16) == -INVALID
+    assert L(0, 2, 8, 64, 64, None, F32) == 0
+    assert L(1, 2, 0, 128, 128, None, BF16) == 0
+
+
+def test_backward_kernel_dispatch(lib):
+    """Host-only: the tensor-core backward takes bf16 with Dv = 64 and every
+    decay inside the 64-token chunk kernel's envelope."""
+    K = lib.la_backward_kernel
+    K.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_int]
+    g = lambda *x: (ctypes.c_float * len(x))(*x)  # noqa: E731
+    assert K(4, 8, 4096, 64, 64, None, BF16) == 1
+    assert K(1, 2, 333, 128, 64, g(0.9, 1.0), BF16) == 1
+    assert K(1, 2, 333, 128, 64, g(0.35, 1.0), BF16) == 1
+    assert K(1, 2, 333, 128, 64, g(0.34, 1.0), BF16) == 0   # decay too strong
+    assert K(1, 2, 333, 64, 128, None, BF16) == 0           # Dv = 128
+    assert K(4, 8, 4096, 64, 64, None, F32) == 0            # fp32 inputs
+    assert K(1, 2, 8, 96, 64, None, BF16) == -UNSUPPORTED
 
 
 def test_causal_kernel_dispatch(lib):

@@ -9,9 +9,16 @@ The rounding error of an fp32 sum is bounded by the unit roundoff times the
 sum of |terms|, and a gradient row can be a near-total cancellation of large
 terms (dq of a single token: the output depends on q only through eps, so
 gt . v - c is almost exactly 0), so the error bound of a row scales with its
-T_i, not with its result.  fp32 inputs: 2e-4; bf16 inputs: 1e-2 (the inputs
-are widened exactly, the arithmetic is fp32 and the gradients are rounded
-once to bf16)."""
+T_i, not with its result.  fp32 inputs: 2e-4.  bf16 inputs on the fp32
+CUDA-core kernels: 1e-2 (the inputs are widened exactly, the arithmetic is
+fp32 and the gradients are rounded once to bf16).  bf16 inputs on the tensor
+cores: 2e-2, the bound the bf16 forward kernels are held to, for the same
+arithmetic (bf16 matrix-multiply operands, fp32 accumulation).  A term of a
+gradient sum there carries the bf16 roundings of its two mapped operands,
+the masked product P, the value operand and the output (up to six), plus
+the relative error of the normaliser d_i that gt_i = dO_i / d_i inherits
+from the forward product (up to four more): about 10 * 2^-9 = 2e-2 of the
+row's term scale when every rounding falls the same way."""
 import numpy as np
 import pytest
 import torch
@@ -21,6 +28,7 @@ from helpers import record, to_np
 pytestmark = pytest.mark.gpu
 
 BWD_TOL = {torch.float32: 2e-4, torch.bfloat16: 1e-2}
+BWD_TOL_TC = 2e-2  # bf16 operands on tensor cores (see the module docstring)
 
 
 @pytest.fixture(scope="module")
@@ -84,7 +92,17 @@ BWD_CASES = [
     (2, 2, 333, 128, 64, [0.9, 1.0]),
     (1, 3, 700, 128, 128, [0.5, 0.97, 0.999]),
     (1, 1, 1000, 64, 64, [0.0]),
+    # bf16 on tensor cores: several sequence parts per head (few heads, long
+    # sequences, ragged ends), the decay envelope's edge, D = 128
+    (1, 2, 3001, 64, 64, [0.35, 0.999]),
+    (1, 3, 2050, 128, 64, [1.0, 0.9, 0.5]),
+    (2, 3, 65, 64, 64, [0.97, 1.0, 0.6]),
 ]
+
+
+def expect_path(dtype, Dv, gammas):
+    tc = dtype == torch.bfloat16 and Dv == 64 and (gammas is None or min(gammas) >= 0.35)
+    return "tensor-core" if tc else "cuda-core"
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
@@ -94,6 +112,7 @@ def test_backward(la, bw, dtype, case):
     q, k, v, do = inputs(B, H, N, D, Dv, dtype, N + D + Dv)
     g = None if gl is None else torch.tensor([gl[h % len(gl)] for h in range(H)],
                                              dtype=torch.float32)
+    assert la.backward_kernel(B, H, N, D, Dv, gamma=g, dtype=dtype) == expect_path(dtype, Dv, gl)
     dq, dk, dv = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), gamma=g)
     torch.cuda.synchronize()
     gu = None if g is None else np.tile(g.numpy(), B).reshape(B, H)
@@ -105,10 +124,11 @@ def test_backward(la, bw, dtype, case):
                             None if gu is None else gu[b, h], 1e-6)
             for arr, t in zip(sizes, ts):
                 arr[b, h] = t
-    tol = BWD_TOL[dtype]
+    path = expect_path(dtype, Dv, gl)
+    tol = BWD_TOL_TC if path == "tensor-core" else BWD_TOL[dtype]
     for name, got, ref, sz in (("dq", dq, rq, sizes[0]), ("dk", dk, rk, sizes[1]),
                                ("dv", dv, rv, sizes[2])):
-        err = record(f"backward {name} {'fp32' if dtype == torch.float32 else 'bf16'}",
+        err = record(f"backward {name} {'fp32' if dtype == torch.float32 else 'bf16'} ({path})",
                      row_err(to_np(got), ref, sz), tol)
         assert err < tol, (name, err)
 
@@ -128,14 +148,15 @@ def test_backward_bf16_n4096_sampled_units(la, bw):
     launch configuration the benchmark times; whole units sampled."""
     from kernelized_sequence_mixing_gb300.workloads import WORKLOADS, workload_inputs, workload_upstream
     w = WORKLOADS["backward_bf16_n4096"]
+    assert la.backward_kernel(w.B, w.H, w.N, w.D, w.Dv, dtype=w.dtype) == "tensor-core"
     q, k, v = workload_inputs(w)
     do = workload_upstream(w)
     dq, dk, dv = la.backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), eps=w.eps)
     torch.cuda.synchronize()
-    for b, h in ((0, 0), (3, 5)):
+    for b, h in ((0, 0), (1, 2), (2, 7), (3, 5)):
         args = (to_np(q[b, h]), to_np(k[b, h]), to_np(v[b, h]), to_np(do[b, h]), None, w.eps)
         refs = bw.causal_backward(*args)
         for name, got, ref, sz in zip(("dq", "dk", "dv"), (dq, dk, dv), refs, term_sizes(*args)):
             err = record(f"backward_bf16_n4096 {name} (sampled units)",
-                         row_err(to_np(got[b, h]), ref, sz), 1e-2)
-            assert err < 1e-2, (b, h, name, err)
+                         row_err(to_np(got[b, h]), ref, sz), BWD_TOL_TC)
+            assert err < BWD_TOL_TC, (b, h, name, err)

@@ -55,7 +55,9 @@ def test_algorithmic_work_matches_the_hand_count(name, byts, flops):
 
 
 def test_every_workload_is_counted():
-    assert {n for n, _, _ in HAND} | {"causal_decay_bf16_n8192"} == set(WORKLOADS)
+    # the two smaller capture cases are not benchmarked
+    assert {n for n, _, _ in HAND} | {"causal_decay_bf16_n8192", "noncausal_bf16_n8192"} == \
+        set(WORKLOADS)
 
 
 def test_hbm_roofline_entry():
@@ -84,6 +86,10 @@ def test_alu_roofline_for_the_cuda_core_paths():
         r = bench.roofline_entry(WORKLOADS[name], 10**9, 0, 1.0, 2000.0, "fallback",
                                  1900.0, None, 1, gated_tc=True)
         assert r["bound"] == "hbm" and r["peak_source"] == "fallback"
+    # so is the tensor-core backward
+    r = bench.roofline_entry(WORKLOADS["backward_bf16_n4096"], 10**9, 0, 1.0, 2000.0,
+                             "measured", 1900.0, None, 5, bwd_tc=True)
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(0.5)
 
 
 @pytest.mark.parametrize("name,tc,dtype", [
@@ -94,11 +100,14 @@ def test_alu_roofline_for_the_cuda_core_paths():
     ("gla_bf16_n16384", True, "bf16"),
     ("gla_bf16_n16384", False, "f32"),
     ("backward_bf16_n4096", False, "f32"),
+    ("backward_bf16_n4096", True, "bf16"),
     ("decode_bf16_h32", False, "f32"),
     ("decode_gated_bf16_h32", False, "f32"),
 ])
 def test_compute_dtype(name, tc, dtype):
-    assert bench.compute_dtype(WORKLOADS[name], tc) == dtype
+    w = WORKLOADS[name]
+    got = bench.compute_dtype(w, bwd_tc=tc) if w.backward else bench.compute_dtype(w, tc)
+    assert got == dtype
 
 
 def test_metric_names():
@@ -152,7 +161,7 @@ def test_each_workload_hashes_the_sources_it_runs():
     assert src["decode_bf16_h32"] == src["decode_gated_bf16_h32"] == "decode.cu"
     assert src["gla_bf16_n16384"] == "gla_simt.cu"
     assert src["favor_bf16_n16384"] == "favor.cu"
-    assert src["backward_bf16_n4096"] == "backward_simt.cu"
+    assert src["backward_bf16_n4096"] == "backward_tc.cu"
     for w in WORKLOADS.values():
         for f in bench.workload_sources(w):
             assert os.path.exists(os.path.join(ROOT, "kernelized_sequence_mixing_gb300",
