@@ -179,7 +179,7 @@ BACKWARD_SOURCES = ("backward_tc.cu", "chunk_tc.cu", "backward_simt.cu", "tc_com
 # fp32 CUDA-core kernels
 DECODE_SOURCES = ("decode.cu", "common.cuh")
 CHUNK_TC_SOURCES = ("chunk_tc.cu", "tc_common.cuh", "common.cuh")
-NONCAUSAL_SOURCES = ("chunk_tc.cu", "part_scan.cu", "tc_common.cuh", "common.cuh")
+NONCAUSAL_SOURCES = ("noncausal_tc.cu", "part_scan.cu", "tc_common.cuh", "common.cuh")
 SIMT_SOURCES = ("causal_simt.cu", "common.cuh")
 NONCAUSAL_SIMT_SOURCES = ("kv_state_simt.cu", "common.cuh")
 

@@ -66,6 +66,13 @@ struct ChunkEpilogue {
   const __nv_bfloat16 *grad_in;
   int rev;
 };
+// Non-causal forward on tensor cores with persistent streaming kernels
+// (noncausal_tc.cu): bf16, D and Dv in {64, 128}, no decay.  A reduce pass
+// writes per-part [S | z] records (noncausal_tc_workspace_bytes()), a scan
+// sums them, an apply pass writes o.
+bool noncausal_tc_supported(const Problem &p);
+size_t noncausal_tc_workspace_bytes(const Problem &p);
+cudaError_t launch_noncausal_tc(const Problem &p, void *ws, cudaStream_t s);
 cudaError_t launch_causal_chunk_epilogue(const Problem &p, const Gammas &g, void *ws, int P,
                                          cudaStream_t s, const ChunkEpilogue &ep);
 // The causal kernel with 128-token chunks for D = Dv = 128 (chunk128.cu):

@@ -165,13 +165,11 @@ la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStrea
     return from_cuda(launch_causal_simt(p, g, s));
   }
   // Non-causal: reduce S, z per (b, h) into a stream-ordered workspace, then
-  // apply them to every query.
-  if (chunk_tc_supported(p, g)) {
-    const int P = chunk_state_parts(BH, N, D, Dv);
+  // apply them to every query (bf16: persistent tensor-core passes).
+  if (noncausal_tc_supported(p)) {
     void *ws = nullptr;
-    if (cudaMallocAsync(&ws, chunk_workspace_bytes(BH, P, D, Dv), s) != cudaSuccess)
-      return LA_ERR_CUDA;
-    cudaError_t e = launch_noncausal_chunk(p, ws, P, P, s);
+    if (cudaMallocAsync(&ws, noncausal_tc_workspace_bytes(p), s) != cudaSuccess) return LA_ERR_CUDA;
+    cudaError_t e = launch_noncausal_tc(p, ws, s);
     cudaError_t ef = cudaFreeAsync(ws, s);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(ef);

@@ -133,6 +133,13 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// One 32-byte store of eight 32-bit words to global memory (the address must
+// be 32-byte aligned): a whole sector per instruction and thread.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 // Prefetch a tile into L2 (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(

@@ -157,7 +157,7 @@ def test_each_workload_hashes_the_sources_it_runs():
     assert src["causal_decay_bf16_n16384"] == "chunk128.cu"
     assert src["causal_bf16_n4096"] == "chunk_tc.cu"
     assert src["causal_f32_n256"] == "causal_simt.cu"
-    assert src["noncausal_bf16_n65536"] == "chunk_tc.cu"
+    assert src["noncausal_bf16_n65536"] == "noncausal_tc.cu"
     assert src["decode_bf16_h32"] == src["decode_gated_bf16_h32"] == "decode.cu"
     assert src["gla_bf16_n16384"] == "gla_simt.cu"
     assert src["favor_bf16_n16384"] == "favor.cu"
