@@ -790,8 +790,11 @@ def time_extra(la, name, dev, hbm_peak, quick):
     """Time one more configuration in this process: warm-up, then CUDA events
     around each step on the launching stream; clocks sampled around it.
     Forward configurations run ``steps`` forward passes (rotating input
-    copies when the working set fits in L2); the decode configuration runs
-    its whole loop of single-token steps, each with fresh inputs."""
+    copies when the working set fits in L2), captured once in a CUDA graph
+    and replayed, so that a short step measures the GPU's work rather than
+    the host's call overhead; the decode configuration runs its whole loop
+    of single-token steps, each with fresh inputs, as plain launches (each
+    step is long enough to hide the host)."""
     import torch
     from kernelized_sequence_mixing_gb300.workloads import WORKLOADS
     w = WORKLOADS[name]
@@ -831,6 +834,22 @@ def time_extra(la, name, dev, hbm_peak, quick):
     for i in range(warm):
         run(i)
     torch.cuda.synchronize(dev)
+    graph = None
+    if not w.steps:
+        # one graph over a whole rotation of the input copies (at least
+        # `nsteps` launches); replayed until nsteps steps have run
+        per_graph = ncopy * max(1, -(-nsteps // ncopy)) if ncopy < nsteps else ncopy
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(per_graph):
+                    run(i)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            nsteps = per_graph
+        except RuntimeError:
+            graph = None
+            torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     roll = 0.0 if quick else 0.5
     if not quick:
@@ -845,14 +864,23 @@ def time_extra(la, name, dev, hbm_peak, quick):
         S.copy_(S0)
         z.copy_(z0)
         torch.cuda.synchronize(dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
-    ev[0].record(stream)
-    for i in range(nsteps):
-        run(i)
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(nsteps)]
-    total = ev[0].elapsed_time(ev[-1])
+    if graph is not None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        total = e0.elapsed_time(e1)
+        per = [total / nsteps]
+    else:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nsteps + 1)]
+        ev[0].record(stream)
+        for i in range(nsteps):
+            run(i)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(nsteps)]
+        total = ev[0].elapsed_time(ev[-1])
     t_end = time.perf_counter() + roll
     i = 0
     while time.perf_counter() < t_end:
@@ -869,6 +897,8 @@ def time_extra(la, name, dev, hbm_peak, quick):
                           "frac": gbs / hbm_peak, "algorithmic_bytes": byts,
                           "tflops": flops / (ms / 1e3) / 1e12},
              "clocks": clocks,
+             "timing": ("one CUDA graph of the steps, replayed between two events" if graph is not None
+                        else "CUDA events around each plain launch"),
              "inputs": "device-drawn from a seeded CUDA generator, same shapes and N(0,1) x "
                        f"{w.scale} distribution as the recipe"}
     if w.steps:

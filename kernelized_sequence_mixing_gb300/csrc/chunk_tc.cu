@@ -40,10 +40,8 @@
 //            rescaling T per chunk; T is multiplied by gamma^W once per
 //            window.  o_t = O[t, :Dv] / (O[t, Dv] + eps).
 //   state mode: phase A only, A_p stored for a scan over the parts
-//            (part_scan.cu): the final state of a prefill, or (gamma = 1) the
-//            sums of the non-causal form.
-//   apply mode: phase C with the inter-chunk product only, O = phi(q) [S | z],
-//            for the non-causal read-out.
+//            (part_scan.cu): the final state of a prefill.  (The bf16
+//            non-causal form has its own streaming passes, noncausal_tc.cu.)
 //
 // Every term of the token-by-token recurrence appears once; the regrouping
 // changes only the order of summation and the rounding of the MMA operands
@@ -83,12 +81,12 @@ constexpr int kWarpPhi = 12;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
 
-enum Mode : int { kCausal = 0, kState = 1, kApply = 2 };
+enum Mode : int { kCausal = 0, kState = 1 };
 constexpr int kMaxStages = 8;
 
 template <int D, int DV, int MODE>
 struct Lay {
-  static constexpr bool STATE = MODE == kState, APPLY = MODE == kApply;
+  static constexpr bool STATE = MODE == kState;
   static constexpr int KB = D / 64, VB = DV / 64;
   static constexpr int NA = DV + 16;  // columns of [V | 1], [T | z] and O
   // Stage layout by mode:
@@ -103,10 +101,10 @@ struct Lay {
   static constexpr int kOffK = STATE ? 0 : KB * kBox;
   static constexpr int kOffKlo = STATE ? KB * kBox : kOffQ;
   static constexpr int kOffV = STATE ? 2 * KB * kBox : kOffK + 2 * kBox;
-  static constexpr bool kOnesInStage = !APPLY && !(STATE && DV == 64);
+  static constexpr bool kOnesInStage = !(STATE && DV == 64);
   static constexpr int kOffOnes = kOffV + VB * kBox;  // in-stage ones box
   static constexpr int kStageBytes =
-      APPLY ? KB * kBox : (STATE ? kOffOnes + (kOnesInStage ? kBox : 0) : kOffOnes + kBox);
+      STATE ? kOffOnes + (kOnesInStage ? kBox : 0) : kOffOnes + kBox;
   static constexpr int kSharedBytes = STATE ? ((D == 64 ? kBox : 0) + (DV == 64 ? kBox : 0)) : 0;
   static constexpr int kPBytes = MODE == kCausal ? kC * 128 : 0;
   static constexpr int kSopAtom = D * 64;  // 32 columns of [T | z], 64-byte swizzle
@@ -126,10 +124,10 @@ struct Lay {
   static constexpr int kBytes = kOffMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   // tensor memory columns (fp32): A' (M = 64), T (M = 128), O double buffer
-  // (M = 64); state mode uses only T, apply mode only O, and allocates no more
+  // (M = 64); state mode uses only T, and allocates no more
   // than it uses (two apply CTAs can then share an SM)
-  static constexpr uint32_t kColA = 0, kColT = STATE ? 0 : 64, kColO = APPLY ? 0 : 64 + NA;
-  static constexpr uint32_t kTmemUsed = STATE ? NA : (APPLY ? 2 * NA : kColO + 2 * NA);
+  static constexpr uint32_t kColA = 0, kColT = STATE ? 0 : 64, kColO = 64 + NA;
+  static constexpr uint32_t kTmemUsed = STATE ? NA : kColO + 2 * NA;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
   static_assert(kTmemUsed <= 512, "tensor memory");
   static_assert(kStages >= 3, "stages");
@@ -142,8 +140,7 @@ struct ChunkParams {
   __nv_bfloat16 *o;
   // per-part records [B*H][rec_parts][D*Dv + D]: state mode writes A_p (S
   // rows, then z); causal mode A_(p-1) column-group-major (float4 of
-  // columns 4g..4g+3 of row d at g * D + d, then z); apply mode reads the
-  // sum in slot 0 of its (batch, head)
+  // columns 4g..4g+3 of row d at g * D + d, then z)
   float *rec;
   int *ws_flag;    // causal, P > 1: [B*H][P], 1 once A_p is published
   int *ws_ticket;  // causal, P > 1: part-major work counter
@@ -268,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   using L = Lay<D, DV, MODE>;
   constexpr int S = L::kStages;
   constexpr int NA = L::NA;
-  constexpr bool kPhaseC = MODE == kCausal || MODE == kApply;
+  constexpr bool kPhaseC = MODE == kCausal;
   constexpr size_t kRec = static_cast<size_t>(D) * DV + D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -537,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (lane == 0) {
         const bool phaseA = it < nA;
         const int row = (phaseA ? cbA + it : cb + it - nA) * kC;
-        const bool wq = !phaseA, wkv = phaseA || MODE != kApply;
+        const bool wq = !phaseA, wkv = true;
         uint8_t *st = sm + s * L::kStageBytes;
         mbar_arrive_expect_tx(&full[s], (wq ? L::KB * kBox : 0) + (wkv ? (L::KB + L::VB) * kBox : 0));
         if (wq)
@@ -661,7 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         s1 = 0;
         ph1 ^= 1;
       }
-      if (MODE == kApply && !warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) break;
       if (MODE == kCausal) {
         if (i + 1 < nch) {
           if (!warp_wait(&mapped[s1], ph1, abort_flag, p.timeouts)) break;
@@ -680,9 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       }
       // O = qh [T | z]  (M 64, N Dv + 16, K = D)
       if (!warp_wait(&O_free[b], (u & 1) ^ 1, abort_flag, p.timeouts)) break;
-      if (!warp_wait(S_full, MODE == kApply ? 0u : static_cast<uint32_t>(i & 1), abort_flag,
-                     p.timeouts))
-        break;
+      if (!warp_wait(S_full, static_cast<uint32_t>(i & 1), abort_flag, p.timeouts)) break;
       tc_fence_after();
       const uint32_t tO = tmem + L::kColO + b * NA;
       if (leader) {
@@ -728,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
       if (!warp_wait(&full[s], ph, abort_flag, p.timeouts)) break;
       const int nv = min(kC, N - (cb + i) * kC);
       uint8_t *st = sm + s * L::kStageBytes;
-      if (MODE != kApply) {
+      {
         // kh_s = gamma^(E - s) phi(k_s); rows past the sequence end are zero
         const int e0 = W - 1 - kC * (i % WC);
         uint32_t sc[4];
@@ -810,34 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
     uint8_t *sop = sm + L::kOffSop;
     constexpr int kAtom = L::kSopAtom;
     if (MODE == kState) phase_a_map(tid);
-    if (MODE == kApply) {
-      // [S | z] (the sum over all tokens, slot 0 of this (batch, head)) as the bf16 operand
-      const float *r0 = p.rec + static_cast<size_t>(bh) * p.rec_parts * kRec;
-      if (act) {
-#pragma unroll 1
-        for (int cc = 0; cc < DV / 32; ++cc) {
-          float x[32];
-          const float4 *src = reinterpret_cast<const float4 *>(r0 + d * DV + 32 * cc);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 v4 = __ldcg(src + q);
-            x[4 * q] = v4.x;
-            x[4 * q + 1] = v4.y;
-            x[4 * q + 2] = v4.z;
-            x[4 * q + 3] = v4.w;
-          }
-          put_sop32(sop, kAtom, cc, d, x);
-        }
-        float zz[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) zz[e] = 0.f;
-        zz[0] = __ldcg(r0 + D * DV + d);
-        put_sop16(sop, kAtom, DV / 32, d, zz);
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(S_full);
-    } else if (MODE == kState) {
+    if (MODE == kState) {
       // A_p = gamma^(e_p - E) T: T is scaled to the chunk-aligned end E of
       // the part; e_p = its last token (they differ only for a ragged end)
       const float corr = DECAY ? exp2f(-static_cast<float>(kC * nch - len) * lg) : 1.f;
@@ -1187,27 +1154,6 @@ cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *
   cudaError_t e = launch_mode<kState>(prm, decay, false, D, Dv, BH * P, s);
   if (e != cudaSuccess) return e;
   return launch_part_scan(prm.rec, BH, H, P, N, D, Dv, prm.lg, kScanFinal, S, z, s);
-}
-
-cudaError_t launch_noncausal_chunk(const Problem &p, void *ws, int Ps, int Pa, cudaStream_t s) {
-  Gammas ones;
-  for (int h = 0; h < kMaxHeads; ++h) ones.g[h] = 1.f;
-  if (p.decay || !chunk_tc_supported(p, ones) || !ws) return cudaErrorNotSupported;
-  const int BH = p.B * p.H;
-  ChunkParams prm = {};
-  if (!setup_params(&prm, p.q, p.k, p.v, BH, p.N, p.D, p.Dv, p.H, ones, false))
-    return cudaErrorNotSupported;
-  prm.o = static_cast<__nv_bfloat16 *>(p.o);
-  prm.eps = p.eps;
-  prm.rec = static_cast<float *>(ws);
-  prm.rec_parts = Ps;
-  prm.P = Ps;
-  cudaError_t e = launch_mode<kState>(prm, false, p.ident, p.D, p.Dv, BH * Ps, s);
-  if (e == cudaSuccess)
-    e = launch_part_scan(prm.rec, BH, p.H, Ps, p.N, p.D, p.Dv, prm.lg, kScanSum, nullptr, nullptr, s);
-  if (e != cudaSuccess) return e;
-  prm.P = Pa;
-  return launch_mode<kApply>(prm, false, p.ident, p.D, p.Dv, BH * Pa, s);
 }
 
 }  // namespace linattn

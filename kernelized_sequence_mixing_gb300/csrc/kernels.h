@@ -90,8 +90,6 @@ cudaError_t launch_causal_chunk128(const Problem &p, const Gammas &g, void *ws, 
 cudaError_t launch_prefill_chunk(const void *k, const void *v, float *S, float *z, int B, int H,
                                  int N, int D, int Dv, bool decay, const Gammas &g, void *ws,
                                  int P, cudaStream_t s);
-// Non-causal forward: sums over Ps parts, read-out over Pa parts.
-cudaError_t launch_noncausal_chunk(const Problem &p, void *ws, int Ps, int Pa, cudaStream_t s);
 
 // Scan over per-part records [BH][P][D*Dv + D] (part_scan.cu): kScanStarts
 // turns A_p into the state before part p in place; kScanFinal writes the
