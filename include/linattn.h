@@ -44,7 +44,9 @@
  * - stream is a cudaStream_t passed as void* (NULL = legacy default stream),
  *   so that this header needs no CUDA header to compile.
  *   Every call is asynchronous on that stream and never synchronises.  The
- *   caller owns all buffers; the library keeps no state between calls.
+ *   caller owns all buffers; the library keeps no state between calls
+ *   (except la_forward_host's copy streams and memory pool, and the
+ *   allocation-free entry point's fixed array, all per device).
  * - Arguments are validated before any CUDA call, so a rejected call has no
  *   side effect.  A launch failure returns LA_ERR_CUDA; an error raised while
  *   a kernel runs surfaces at the caller's next synchronisation.
@@ -119,6 +121,30 @@ LA_API la_status_t la_forward(const void *q, const void *k, const void *v, void 
                        int B, int H, int N, int D, int Dv, int causal,
                        const float *gamma, float eps, la_dtype_t dtype,
                        void *stream);
+
+/*
+ * la_forward on HOST buffers: q, k, v are read from host memory and o is
+ * written to host memory (same shapes, dtype and arguments as la_forward;
+ * no alignment requirement).  The heads are processed in groups (a run of
+ * heads of one batch entry each, about eight groups): a group's inputs are
+ * copied up on a copy stream the library owns, its forward runs on `stream`
+ * once they have landed, and its output is copied down on a second copy
+ * stream once the forward is done, so that uploads, kernels and downloads of
+ * different groups overlap.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister): pageable memory is correct but its
+ * copies do not overlap.  Device memory for the whole problem is a
+ * stream-ordered allocation on `stream` from a pool the library keeps per
+ * device, which holds released memory for the next call until the process
+ * exits (the two copy streams are kept likewise).  Asynchronous: o is complete once
+ * `stream` has been synchronised; the host buffers must stay valid until
+ * then.  The result equals la_forward's up to the order of summation (each
+ * group splits its sequences for its own size).  Errors as la_forward.
+ * Defined on the same pages as la_forward.
+ */
+LA_API la_status_t la_forward_host(const void *q, const void *k, const void *v, void *o,
+                                   int B, int H, int N, int D, int Dv, int causal,
+                                   const float *gamma, float eps, la_dtype_t dtype,
+                                   void *stream);
 
 /*
  * State after a causal pass over N tokens (the prefill of the decode loop):

@@ -67,6 +67,8 @@ def load_library() -> ctypes.CDLL:
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             FP = ctypes.POINTER(ctypes.c_float)
             lib.la_forward.argtypes = [P, P, P, P, I, I, I, I, I, I, FP, F, I, P]
+            lib.la_forward_host.argtypes = [P, P, P, P, I, I, I, I, I, I, FP, F, I, P]
+            lib.la_forward_host.restype = I
             lib.la_forward.restype = I
             lib.la_prefill_state.argtypes = [P, P, P, P, I, I, I, I, I, FP, I, P]
             lib.la_prefill_state.restype = I
@@ -224,23 +226,16 @@ def _step_qkv(fn, q, k, v):
     return B, H, D, v.shape[-1]
 
 
-def _to_device(t, dev):
-    if t.device.type == "cuda":
-        return t
-    if not t.is_pinned():
-        t = t.pin_memory()
-    return t.to(dev, non_blocking=True)
-
-
 def forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None,
             device=None):
     """Linear attention over whole sequences.
 
     q, k: [B, H, N, D]; v: [B, H, N, Dv]; all float32 or all bfloat16,
     contiguous.  CUDA tensors are used in place on the current stream; host
-    tensors are copied to ``device`` (default cuda:0), computed there and the
-    result copied back to host memory (pinned).  gamma: None, a float, or H
-    per-head decays in [0, 1] (causal only).  Returns o: [B, H, N, Dv].
+    tensors go through la_forward_host on ``device`` (default cuda:0), which
+    overlaps the copies with the kernels by groups of heads; the result is a
+    host tensor (pinned), complete when this returns.  gamma: None, a float,
+    or H per-head decays in [0, 1] (causal only).  Returns o: [B, H, N, Dv].
     """
     B, H, N, D, Dv = _qkv("forward", q, k, v)
     src = _one_device("forward", (("q", q), ("k", k), ("v", v), ("out", out)),
@@ -253,19 +248,21 @@ def forward(q, k, v, causal=True, gamma=None, eps=1e-6, out=None,
     dt = _dtype_code(q)
     g = _gamma_arg(gamma, H)
     with torch.cuda.device(dev):
-        qd, kd, vd = (_to_device(t, dev) for t in (q, k, v))
-        od = out if (out is not None and not host) else torch.empty(
+        if host:
+            qh, kh, vh = (t if t.is_pinned() else t.pin_memory() for t in (q, k, v))
+            res = out if out is not None else torch.empty(
+                (B, H, N, Dv), dtype=q.dtype, pin_memory=True)
+            _check("la_forward_host", lib.la_forward_host(
+                _ptr(qh), _ptr(kh), _ptr(vh), _ptr(res), B, H, N, D, Dv,
+                1 if causal else 0, g, float(eps), dt, _stream(dev)))
+            torch.cuda.current_stream(dev).synchronize()
+            return res
+        od = out if out is not None else torch.empty(
             (B, H, N, Dv), dtype=q.dtype, device=dev)
         _check("la_forward", lib.la_forward(
-            _ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), B, H, N, D, Dv,
+            _ptr(q), _ptr(k), _ptr(v), _ptr(od), B, H, N, D, Dv,
             1 if causal else 0, g, float(eps), dt, _stream(dev)))
-        if not host:
-            return od
-        res = out if out is not None else torch.empty(
-            od.shape, dtype=od.dtype, pin_memory=True)
-        res.copy_(od, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
-        return res
+        return od
 
 
 def prefill_state(k, v, gamma=None, S=None, z=None):

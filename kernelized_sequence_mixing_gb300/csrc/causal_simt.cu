@@ -81,20 +81,31 @@ __global__ void __launch_bounds__(kThreads)
   for (int c0 = 0; c0 < N; c0 += kC) {
     const int nv = min(kC, N - c0);
     // 1. phi(q), phi(k) transposed into shared memory; v slice.  Rows past
-    //    the end of the sequence are zero.
-    for (int i = tid; i < kC * D; i += kThreads) {
-      const int t = i / D, d = i % D;
-      float xq = 0.f, xk = 0.f;
-      if (t < nv) {
-        xq = feat_f32<IDENT>(io<T>::load(qh + (int64_t)(c0 + t) * D + d));
-        xk = feat_f32<IDENT>(io<T>::load(kh + (int64_t)(c0 + t) * D + d));
+    //    the end of the sequence are zero.  Every load of the chunk is issued
+    //    before any is used, so the chunk pays one memory latency, not one
+    //    per loop step.
+    {
+      constexpr int kQK = kC * D / kThreads, kV = kC * kDvs / kThreads;
+      float xq[kQK], xk[kQK], xv[kV];
+#pragma unroll
+      for (int it = 0; it < kQK; ++it) {
+        const int i = tid + it * kThreads, t = i / D, d = i % D;
+        xq[it] = t < nv ? io<T>::load(qh + (int64_t)(c0 + t) * D + d) : 0.f;
+        xk[it] = t < nv ? io<T>::load(kh + (int64_t)(c0 + t) * D + d) : 0.f;
       }
-      fqT[d * kLd + t] = xq;
-      fkT[d * kLd + t] = xk;
-    }
-    for (int i = tid; i < kC * kDvs; i += kThreads) {
-      const int t = i / kDvs, e = i % kDvs;
-      vs[i] = t < nv ? io<T>::load(vh + (int64_t)(c0 + t) * DV + e0 + e) : 0.f;
+#pragma unroll
+      for (int it = 0; it < kV; ++it) {
+        const int i = tid + it * kThreads, t = i / kDvs, e = i % kDvs;
+        xv[it] = t < nv ? io<T>::load(vh + (int64_t)(c0 + t) * DV + e0 + e) : 0.f;
+      }
+#pragma unroll
+      for (int it = 0; it < kQK; ++it) {
+        const int i = tid + it * kThreads, t = i / D, d = i % D;
+        fqT[d * kLd + t] = t < nv ? feat_f32<IDENT>(xq[it]) : 0.f;
+        fkT[d * kLd + t] = t < nv ? feat_f32<IDENT>(xk[it]) : 0.f;
+      }
+#pragma unroll
+      for (int it = 0; it < kV; ++it) vs[tid + it * kThreads] = xv[it];
     }
     __syncthreads();
 

@@ -6,6 +6,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
 #include "../../include/linattn.h"
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -59,6 +62,9 @@ la_status_t from_cuda(cudaError_t e) {
 }
 
 la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStream_t s);
+la_status_t run_forward_host(const void *q, const void *k, const void *v, void *o, int B, int H,
+                             int N, int D, int Dv, int causal, const Gammas &g, float eps, Dtype dt,
+                             cudaStream_t s);
 
 }  // namespace
 
@@ -125,6 +131,28 @@ la_status_t la_forward(const void *q, const void *k, const void *v, void *o,
   return run_forward(p, g, causal, static_cast<cudaStream_t>(stream));
 }
 
+la_status_t la_forward_host(const void *q, const void *k, const void *v, void *o,
+                            int B, int H, int N, int D, int Dv, int causal,
+                            const float *gamma, float eps, la_dtype_t dtype,
+                            void *stream) {
+  la_status_t st = check_sizes(B, H, N, D, Dv, dtype);
+  if (st != LA_OK) return st;
+  if (!isfinite(eps) || eps < 0.f) return LA_ERR_INVALID_ARG;
+  Gammas g;
+  bool decay = false;
+  if ((st = load_gammas(gamma, H, &g, &decay)) != LA_OK) return st;
+  if (!causal && decay) return LA_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)B * H * N;
+  if (rows == 0) return LA_OK;
+  if (!q || !k || !v || !o) return LA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t nqk = (size_t)rows * D * es, nv = (size_t)rows * Dv * es;
+  if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv))
+    return LA_ERR_INVALID_ARG;
+  return run_forward_host(q, k, v, o, B, H, N, D, Dv, causal, g, eps, dtype == LA_F32 ? kF32 : kBF16,
+                          static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"
 
 namespace {
@@ -188,6 +216,148 @@ la_status_t run_forward(const Problem &p, const Gammas &g, int causal, cudaStrea
   cudaError_t ef = cudaFreeAsync(ws, s);
   if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(ef);
+}
+
+// Copy streams of the current device for la_forward_host, created once and
+// kept until the process exits.
+bool copy_streams(cudaStream_t *up, cudaStream_t *down) {
+  constexpr int kMaxDev = 64;
+  static cudaStream_t ups[kMaxDev] = {}, downs[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ups[dev]) {
+    cudaStream_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaStreamDestroy(a);
+      return false;
+    }
+    ups[dev] = a;
+    downs[dev] = b;
+  }
+  *up = ups[dev];
+  *down = downs[dev];
+  return true;
+}
+
+// The device-memory pool of la_forward_host's buffers on the current
+// device: created once, it keeps released memory for the next call (a
+// release threshold of "never"), so that a call does not map its buffers
+// anew each time.
+cudaMemPool_t host_path_pool() {
+  constexpr int kMaxDev = 64;
+  static cudaMemPool_t pools[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
+// Host buffers in, host buffer out, in groups of heads: group g's inputs go
+// up on one copy stream, its forward runs on `s` once they have landed, its
+// output comes down on a second copy stream once the forward is done, so
+// that the uploads, the kernels and the downloads of different groups
+// overlap.  A group is a run of heads of one batch entry (so each keeps its
+// decays); device buffers for the whole problem are stream-ordered
+// allocations on `s` from the library's pool, released on `s` after the
+// last download.
+la_status_t run_forward_host(const void *q, const void *k, const void *v, void *o, int B, int H,
+                             int N, int D, int Dv, int causal, const Gammas &g, float eps, Dtype dt,
+                             cudaStream_t s) {
+  cudaStream_t up = nullptr, down = nullptr;
+  if (!copy_streams(&up, &down)) return LA_ERR_CUDA;
+  cudaMemPool_t pool = host_path_pool();
+  if (!pool) return LA_ERR_CUDA;
+  const size_t es = dt == kF32 ? 4 : 2;
+  const size_t head_qk = (size_t)N * D * es, head_v = (size_t)N * Dv * es;
+  const size_t nqk = (size_t)B * H * head_qk, nvv = (size_t)B * H * head_v;
+  // about eight groups: enough to overlap, few enough that each forward
+  // still spreads over the SMs
+  const int groups_target = 8;
+  int hs = (B * H + groups_target - 1) / groups_target;
+  if (hs > H) hs = H;
+  if (hs < 1) hs = 1;
+  const int gpb = (H + hs - 1) / hs;  // groups per batch entry
+  const int G = B * gpb;
+  uint8_t *dbuf = nullptr;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&dbuf), 2 * nqk + 2 * nvv, pool, s) != cudaSuccess)
+    return LA_ERR_CUDA;
+  uint8_t *dq = dbuf, *dk = dq + nqk, *dv = dk + nqk, *dout = dv + nvv;
+  std::vector<cudaEvent_t> ev(2 * G + 2, nullptr);
+  la_status_t st = LA_OK;
+  for (auto &e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) st = LA_ERR_CUDA;
+  cudaEvent_t ev_alloc = ev[2 * G], ev_done = ev[2 * G + 1];
+  auto ok = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == LA_OK) st = LA_ERR_CUDA;
+    return st == LA_OK;
+  };
+  if (st == LA_OK && ok(cudaEventRecord(ev_alloc, s)) && ok(cudaStreamWaitEvent(up, ev_alloc, 0)) &&
+      ok(cudaStreamWaitEvent(down, ev_alloc, 0))) {
+    auto range = [&](int gi, int *b, int *h0, int *nh) {
+      *b = gi / gpb;
+      *h0 = (gi % gpb) * hs;
+      *nh = H - *h0 < hs ? H - *h0 : hs;
+    };
+    // uploads, in group order
+    for (int gi = 0; gi < G && st == LA_OK; ++gi) {
+      int b, h0, nh;
+      range(gi, &b, &h0, &nh);
+      const size_t u0 = (size_t)b * H + h0;
+      ok(cudaMemcpyAsync(dq + u0 * head_qk, static_cast<const uint8_t *>(q) + u0 * head_qk, nh * head_qk,
+                         cudaMemcpyHostToDevice, up));
+      ok(cudaMemcpyAsync(dk + u0 * head_qk, static_cast<const uint8_t *>(k) + u0 * head_qk, nh * head_qk,
+                         cudaMemcpyHostToDevice, up));
+      ok(cudaMemcpyAsync(dv + u0 * head_v, static_cast<const uint8_t *>(v) + u0 * head_v, nh * head_v,
+                         cudaMemcpyHostToDevice, up));
+      ok(cudaEventRecord(ev[gi], up));
+    }
+    // each group's forward once its inputs are on the device, then its download
+    for (int gi = 0; gi < G && st == LA_OK; ++gi) {
+      int b, h0, nh;
+      range(gi, &b, &h0, &nh);
+      const size_t u0 = (size_t)b * H + h0;
+      if (!ok(cudaStreamWaitEvent(s, ev[gi], 0))) break;
+      Gammas gg;
+      for (int h = 0; h < kMaxHeads; ++h) gg.g[h] = h < nh ? g.g[h0 + h] : 1.f;
+      bool gdecay = false;
+      for (int h = 0; h < nh; ++h) gdecay = gdecay || gg.g[h] != 1.f;
+      Problem pg{dq + u0 * head_qk, dk + u0 * head_qk, dv + u0 * head_v, dout + u0 * head_v, 1, nh, N,
+                 D, Dv, gdecay, eps, dt};
+      const la_status_t fs = run_forward(pg, gg, causal, s);
+      if (fs != LA_OK) {
+        st = fs;
+        break;
+      }
+      if (!ok(cudaEventRecord(ev[G + gi], s)) || !ok(cudaStreamWaitEvent(down, ev[G + gi], 0))) break;
+      ok(cudaMemcpyAsync(static_cast<uint8_t *>(o) + u0 * head_v, dout + u0 * head_v, nh * head_v,
+                         cudaMemcpyDeviceToHost, down));
+    }
+  }
+  // the caller's stream waits for every download before the buffers are
+  // released (and before its own later work)
+  if (ev_done && cudaEventRecord(ev_done, down) == cudaSuccess) cudaStreamWaitEvent(s, ev_done, 0);
+  if (cudaFreeAsync(dbuf, s) != cudaSuccess && st == LA_OK) st = LA_ERR_CUDA;
+  for (auto &e : ev)
+    if (e) cudaEventDestroy(e);  // released once the work they mark is done
+  return st;
 }
 
 }  // namespace

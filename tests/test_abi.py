@@ -34,7 +34,7 @@ def declared_symbols():
 
 def test_header_declares_entry_points():
     syms = declared_symbols()
-    for s in ("la_forward", "la_forward_state", "la_prefill_state", "la_decode_step",
+    for s in ("la_forward", "la_forward_host", "la_forward_state", "la_prefill_state", "la_decode_step",
               "la_forward_gated", "la_decode_gated", "la_favor_features", "la_forward_favor",
               "la_backward", "la_backward_launches", "la_backward_kernel", "la_gated_kernel", "la_wait_selftest",
               "la_status_string", "la_causal_kernel",
@@ -303,3 +303,22 @@ def test_causal_kernel_dispatch(lib):
     assert K(1, 1, 256, 96, 64, None, BF16) == -UNSUPPORTED
     assert K(1, 2, 256, 64, 64, g(1.5, 1.0), BF16) == -INVALID
     assert K(256, 256, 1, 64, 64, None, BF16) == 1          # one-dimensional grid
+
+
+def test_forward_host_rejects_bad_arguments(lib):
+    """Host-only: la_forward_host validates like la_forward before any CUDA
+    call (host pointers need no alignment)."""
+    F = lib.la_forward_host
+    F.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_float,
+                                                               ctypes.c_int, ctypes.c_void_p]
+    q, k, v, o = (A + i * STEP for i in range(4))
+
+    def call(p=(q, k, v, o), B=1, H=2, N=8, D=64, Dv=64, causal=1, g=None, eps=1e-6, dt=BF16):
+        return F(*p, B, H, N, D, Dv, causal, g, eps, dt, None)
+
+    assert call(p=(q, k, v, None)) == INVALID
+    assert call(p=(q, k, v, q)) == INVALID                   # o aliases q
+    assert call(eps=float("nan")) == INVALID
+    assert call(causal=0, g=(ctypes.c_float * 2)(0.5, 1.0)) == INVALID
+    assert call(D=96) == UNSUPPORTED
+    assert call(B=0, p=(None,) * 4) == OK                    # empty: nothing to do

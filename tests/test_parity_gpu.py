@@ -206,12 +206,43 @@ def test_causal_empty_and_host_buffers(la, ora):
     q, k, v = gen(1, 2, 0, 64, 64, torch.bfloat16, 1)
     o = la.forward(q.cuda(), k.cuda(), v.cuda())
     assert o.shape == (1, 2, 0, 64)
-    # host tensors: copied in, computed on the GPU, copied back
+    # host tensors (la_forward_host: groups of heads whose copies overlap the
+    # kernels): the oracle's result within tolerance, and the device path's
     q, k, v = gen(1, 2, 300, 64, 128, torch.bfloat16, 2)
     o_host = la.forward(q, k, v, gamma=[0.9, 1.0])
     o_dev = la.forward(q.cuda(), k.cuda(), v.cuda(), gamma=[0.9, 1.0])
     assert o_host.device.type == "cpu"
-    assert torch.equal(o_host, o_dev.cpu())
+    ref = ora.causal(to_np(q), to_np(k), to_np(v), gamma=[0.9, 1.0])
+    assert max_row_error(to_np(o_host), ref) < 2e-2
+    assert max_row_error(to_np(o_host), to_np(o_dev)) < 2e-2
+
+
+# Host buffers through la_forward_host: several batch entries and head
+# groups, decays per head (each group keeps its own), causal and non-causal,
+# both dtypes; pinned inputs and a pinned output buffer as the benchmark's
+# end-to-end leg passes them.
+HOST_CASES = [
+    # (B, H, N, D, Dv, dtype, causal, gammas)
+    (2, 16, 1000, 128, 128, torch.bfloat16, True, "retnet"),
+    (3, 5, 777, 64, 64, torch.bfloat16, False, None),
+    (2, 3, 300, 64, 128, torch.float32, True, "mix"),
+]
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=lambda c: "x".join(map(str, c[:5])) + ("c" if c[6] else "n"))
+def test_forward_host_buffers(la, ora, case):
+    B, H, N, D, Dv, dtype, causal, gk = case
+    q, k, v = gen(B, H, N, D, Dv, dtype, seed=B + H + N)
+    g = gammas_for(H, gk)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    out = torch.empty((B, H, N, Dv), dtype=dtype, pin_memory=True)
+    o = la.forward(qh, kh, vh, causal=causal, gamma=g, out=out)
+    assert o.data_ptr() == out.data_ptr() and o.device.type == "cpu"
+    gn = None if g is None else g.numpy()
+    ref = (ora.causal(to_np(q), to_np(k), to_np(v), gamma=gn) if causal else
+           ora.noncausal(to_np(q), to_np(k), to_np(v)))
+    err = record(f"host buffers {dtype_name(dtype)}", max_row_error(to_np(o), ref), TOL[dtype])
+    assert err < TOL[dtype], err
 
 
 def test_causal_repeatable(la):
