@@ -433,27 +433,35 @@ __global__ void __launch_bounds__(kThreadsNc) noncausal_tc_kernel(const __grid_c
   if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
+// Dynamic shared memory of a pass, and the whole of the SM's unified memory
+// as shared memory (left to itself, the driver may size the carveout for
+// one CTA and so keep the second CTA of a pass that plans two per SM off
+// the SM).
+template <typename K>
+cudaError_t nc_set_attributes(K kern, int smem) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
 template <int D, int DV, int PASS, bool IDENT>
 int nc_grid() {
-  // CTAs that run at once on the device: one or two per SM by the plan,
-  // fewer if registers do not allow it (the occupancy calculator)
+  // CTAs that run at once on the device: one or two per SM by the plan (the
+  // shared-memory plan, at most 256 tensor-memory columns and 320 threads of
+  // at most 102 registers each let two share an SM).  The passes have no
+  // waits between CTAs, so a grid larger than what fits only runs longer.
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
-  using L = NcLay<D, DV, PASS>;
-  int per = L::kTwoPerSm ? 2 : 1, occ = 0;
-  auto kern = noncausal_tc_kernel<D, DV, PASS, IDENT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsNc, L::kAlloc) == cudaSuccess &&
-      occ >= 1 && occ < per)
-    per = occ;
-  return sms * per;
+  return sms * (NcLay<D, DV, PASS>::kTwoPerSm ? 2 : 1);
 }
 
 // Parts per (batch, head) for `slots` resident CTAs: the number of whole
-// waves of equal items times the tiles of an item, plus a small cost per
-// part (a record to write and scan in the reduce pass).
+// waves of equal items times the tiles of an item, plus a cost per part in
+// tiles (the reduce pass: a record to write and scan; the apply pass: at
+// each new item the pipeline drains while [S | z] is replaced).
 int nc_parts(int BH, int ntile, int slots, double per_part) {
   int best = 1;
   double best_t = 1e300;
@@ -476,7 +484,7 @@ template <int D, int DV, int PASS, bool IDENT>
 cudaError_t nc_launch(const NcParams &prm, int grid, cudaStream_t s) {
   auto kern = noncausal_tc_kernel<D, DV, PASS, IDENT>;
   const int smem = NcLay<D, DV, PASS>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = nc_set_attributes(kern, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreadsNc, smem, s>>>(prm);
   return cudaGetLastError();
@@ -492,8 +500,8 @@ NcPlan nc_plan(int BH, int N) {
   NcPlan pl;
   pl.gr = nc_grid<D, DV, kReduce, IDENT>();
   pl.ga = nc_grid<D, DV, kApply, IDENT>();
-  pl.Pr = nc_parts(BH, ntile, pl.gr, 0.05);
-  pl.Pa = nc_parts(BH, ntile, pl.ga, 0.0);
+  pl.Pr = nc_parts(BH, ntile, pl.gr, 0.5);
+  pl.Pa = nc_parts(BH, ntile, pl.ga, 3.0);
   const long long ir = static_cast<long long>(BH) * pl.Pr, ia = static_cast<long long>(BH) * pl.Pa;
   if (ir < pl.gr) pl.gr = static_cast<int>(ir);
   if (ia < pl.ga) pl.ga = static_cast<int>(ia);
