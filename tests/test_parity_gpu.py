@@ -261,6 +261,11 @@ NONCAUSAL_SMALL = [
     (2, 1, 4096, 128, 64),
     (1, 2, 4097, 128, 128),
     (1, 1, 10000, 64, 64),
+    # more (batch, head) work items than resident CTAs: a CTA's later items
+    # belong to other heads (the persistent passes replace [S | z] and start
+    # a new record mid-loop), with a ragged last tile
+    (8, 80, 333, 64, 64),
+    (4, 90, 129, 128, 128),
 ]
 
 
