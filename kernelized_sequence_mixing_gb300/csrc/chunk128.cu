@@ -524,17 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           tma_load_3d(dst + kKBox, map, 64, row, bh, &fullb[sl]);
         }
         issued = c + 1;
-        // L2 prefetch of the tile two ring chunks ahead (its load waits for a slot)
-        const int cp = c + 2;
-        if (cp < n) {
+        // During phase A, an L2 prefetch of the next ring chunk (its load
+        // waits for a slot).  Phase C prefetches nothing: with every CTA
+        // streaming, a prefetch only adds L2 traffic ahead of a load that is
+        // already queued.
+        const int cp = c + 1;
+        if (lane != 2 && c < nA && cp < n) {
           const int rowp = ring_row(cp);
-          if (lane == 1) {
-            tma_prefetch_3d(map, 0, rowp, bh);
-            tma_prefetch_3d(map, 64, rowp, bh);
-          } else {
-            tma_prefetch_3d(map, 0, rowp, bh);
-            tma_prefetch_3d(map, 64, rowp, bh);
-          }
+          tma_prefetch_3d(map, 0, rowp, bh);
+          tma_prefetch_3d(map, 64, rowp, bh);
         }
       }
       if (*abort_flag) {  // let every issued copy land before the CTA exits
