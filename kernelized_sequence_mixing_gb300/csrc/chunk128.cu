@@ -200,21 +200,22 @@ __device__ __forceinline__ void map_row4(uint8_t *box, int r, int c0, uint32_t s
 }
 
 // Per-feature factors on chunks [c0, c0 + 4) of row r of a box (features
-// 8 (c0 + c) + j of the box, factors F[8 c + j]); a row past the sequence end
-// becomes 0.
-__device__ __forceinline__ void map_row4_feat(uint8_t *box, int r, int c0, const float *F,
+// 8 (c0 + c) + j of the box, factor 8 c + j held by lane 8 c + j of the warp
+// in f_lane); a row past the sequence end becomes 0.  All 32 lanes call it.
+__device__ __forceinline__ void map_row4_feat(uint8_t *box, int r, int c0, float f_lane,
                                               bool valid) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint4 *ptr = reinterpret_cast<uint4 *>(box + sw128_off(r, 16 * (c0 + c)));
     uint4 x = *ptr;
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = __shfl_sync(0xffffffffu, f_lane, 8 * c + j);
     if (valid) {
-      const float4 f0 = *reinterpret_cast<const float4 *>(F + 8 * c);
-      const float4 f1 = *reinterpret_cast<const float4 *>(F + 8 * c + 4);
-      x.x = feat_scale_bf16x2<true>(x.x, pack_bf16x2(f0.x, f0.y));
-      x.y = feat_scale_bf16x2<true>(x.y, pack_bf16x2(f0.z, f0.w));
-      x.z = feat_scale_bf16x2<true>(x.z, pack_bf16x2(f1.x, f1.y));
-      x.w = feat_scale_bf16x2<true>(x.w, pack_bf16x2(f1.z, f1.w));
+      x.x = feat_scale_bf16x2<true>(x.x, pack_bf16x2(f[0], f[1]));
+      x.y = feat_scale_bf16x2<true>(x.y, pack_bf16x2(f[2], f[3]));
+      x.z = feat_scale_bf16x2<true>(x.z, pack_bf16x2(f[4], f[5]));
+      x.w = feat_scale_bf16x2<true>(x.w, pack_bf16x2(f[6], f[7]));
     } else {
       x = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -336,16 +337,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   // 16-byte chunks [4 (u / 4), + 4) of the row (box u / 8).
   auto phase_a_map = [&](int u) {
     const int r = 32 * (u & 3) + lane, quarter = u >> 2;
+    // gated: k-hat already carries the gates up to its chunk's end; the
+    // later chunks of the previous part add their products, feature by
+    // feature.  Lane l holds factor l of this warp's 32 features, loaded one
+    // chunk ahead so that the load is not on the chunk's critical path.
+    auto gate_factor = [&](int i) {
+      const int ia = phase_a_chunk(i);
+      return __ldg(p.gate_suf + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cbA + ia) * kD +
+                   64 * (quarter >> 1) + 32 * (quarter & 1) + lane);
+    };
+    float f_next = GATED && nA > 0 ? gate_factor(0) : 0.f;
     for (int i = 0; i < nA; ++i) {
       const int sl = i & 1, ia = phase_a_chunk(i);
+      const float f_lane = f_next;
+      if (GATED && i + 1 < nA) f_next = gate_factor(i + 1);
       if (!warp_wait(&bar[kKFull + sl], (i >> 1) & 1, abort_flag, p.timeouts)) break;
       const int nv = min(kC, N - (cbA + ia) * kC);
       if (GATED) {
-        // k-hat already carries the gates up to its chunk's end; the later
-        // chunks of the previous part add their products, feature by feature
-        const float *F = p.gate_suf + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cbA + ia) * kD +
-                         64 * (quarter >> 1) + 32 * (quarter & 1);
-        map_row4_feat(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), F,
+        map_row4_feat(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), f_lane,
                       r < nv);
       } else {
         const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
@@ -720,21 +729,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       mbar_arrive(&bar[kTFree]);
       mbar_arrive(&bar[kSFull]);
     }
+    // gated: row d of T times the gate product of chunk i before chunk i;
+    // each is loaded one chunk ahead, off the chunk's critical path
+    auto gate_row = [&](int i) {
+      return __ldg(p.gate_prod + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cb + i) * kD + d);
+    };
+    float fr_next = GATED && nch > 1 ? gate_row(1) : gW;
     for (int i = 1; i <= nch; ++i) {
       // (1) after T += kh^T [V | 1] of chunk i-1 and once O = qh [T | z] of
       // chunk i-1 has read the old copy, publish bf16 [T | z] for chunk i
       // (rescaled when chunk i opens a new decay window)
       if (i < nch) {
+        const float fr = fr_next;
+        if (GATED && i + 1 < nch) fr_next = gate_row(i + 1);
         if (!warp_wait(&bar[kTReady], static_cast<uint32_t>((i - 1 + (hasA ? 1 : 0)) & 1), abort_flag,
                        p.timeouts) ||
             !warp_wait(&bar[kInterDone], static_cast<uint32_t>((i - 1) & 1), abort_flag, p.timeouts))
           break;
         tc_fence_after();
         const bool rebase = (DECAY && (i % WC == 0)) || GATED;
-        // gated: row d of T times the gate product of chunk i
-        const float fr =
-            GATED ? __ldg(p.gate_prod + (static_cast<size_t>(bh) * ((N + kC - 1) / kC) + cb + i) * kD + d)
-                  : gW;
         if (relay && part == 0 && i == p.m0) {
           // relay split, part 0 after m0 chunks: the checkpoint, T carried
           // from the end of the window of chunk i - 1 back to token i C - 1;
@@ -758,23 +771,38 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
           __syncwarp();
           if (lane == 0) atomicAdd(p.ws_flag + bh * P + P - 1, 1);
         }
+        if (GATED) {
+          // every chunk rebases: one 32-column tile at a time keeps the
+          // scaled copy within the register budget
 #pragma unroll 1
-        for (int cc = 0; cc < kDV / 32; cc += 2) {
-          float x0[32], x1[32];
-          tmem_ld32(tT + 32 * cc, x0);
-          tmem_ld32(tT + 32 * cc + 32, x1);
-          tmem_wait_ld();
-          if (rebase) {
+          for (int cc = 0; cc < kDV / 32; ++cc) {
+            float x0[32];
+            tmem_ld32(tT + 32 * cc, x0);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              x0[e] *= fr;
-              x1[e] *= fr;
-            }
+            for (int e = 0; e < 32; ++e) x0[e] *= fr;
             tmem_st32(tT + 32 * cc, x0);
-            tmem_st32(tT + 32 * cc + 32, x1);
+            put_sop32(sop, kSopAtom, cc, d, x0);
           }
-          put_sop32(sop, kSopAtom, cc, d, x0);
-          put_sop32(sop, kSopAtom, cc + 1, d, x1);
+        } else {
+#pragma unroll 1
+          for (int cc = 0; cc < kDV / 32; cc += 2) {
+            float x0[32], x1[32];
+            tmem_ld32(tT + 32 * cc, x0);
+            tmem_ld32(tT + 32 * cc + 32, x1);
+            tmem_wait_ld();
+            if (rebase) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                x0[e] *= fr;
+                x1[e] *= fr;
+              }
+              tmem_st32(tT + 32 * cc, x0);
+              tmem_st32(tT + 32 * cc + 32, x1);
+            }
+            put_sop32(sop, kSopAtom, cc, d, x0);
+            put_sop32(sop, kSopAtom, cc + 1, d, x1);
+          }
         }
         {
           float x0[16];

@@ -118,16 +118,15 @@ __device__ __forceinline__ float scan_prod_rev(float x, int lane) {
   return x;
 }
 
-// grid: x = (batch, head) * Pg + part, y = Dv / 32; Pg = P - 1 for the state
-// pass (the last part needs no record), P for the output pass.
+// One (batch, head, part) and 32-column slice of Dv: vb = (batch, head) * Pg
+// + part, the slice blockIdx.y; Pg = P - 1 for the state pass (the last part
+// needs no record), P for the output pass.
 template <int D, int DV, int PASS, typename T>
-__global__ void __launch_bounds__(kThreads, 2)
-    gla_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
-                    const T *__restrict__ v, const float *__restrict__ a,
-                    T *__restrict__ o, float *__restrict__ rec,
-                    float *__restrict__ S_out, float *__restrict__ z_out, int N,
-                    int P, int Pg, float eps, const int *__restrict__ only_if) {
-  if (only_if && *only_if == 0) return;  // uniform: the tensor-core form ran
+__device__ __forceinline__ void gla_simt_block(const T *__restrict__ q, const T *__restrict__ k,
+                                               const T *__restrict__ v, const float *__restrict__ a,
+                                               T *__restrict__ o, float *__restrict__ rec,
+                                               float *__restrict__ S_out, float *__restrict__ z_out,
+                                               int N, int P, int Pg, float eps, int vb) {
   constexpr int NG = D / 64;  // feature groups of 8 per warp
   constexpr int RD = D / 32;  // state rows per thread
   extern __shared__ float4 smem4[];
@@ -145,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float *redz = red + 2 * kWarps * kDvs;         // [2][kWarps]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bh = blockIdx.x / Pg, part = blockIdx.x % Pg;
+  const int bh = vb / Pg, part = vb % Pg;
   const int e0 = blockIdx.y * kDvs;
   const int nch = (N + kC - 1) / kC;
   const int cb = part_chunk(part, P, nch), ce = part_chunk(part + 1, P, nch);
@@ -472,23 +471,44 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// grid: x strides over the nvb = (batch, head) * Pg blocks of
+// gla_simt_block, y = Dv / 32.  Behind the tensor-core form (only_if set)
+// the grid is one wave, so that it costs one wave of early exits when that
+// form covered every chunk.
+template <int D, int DV, int PASS, typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+    gla_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
+                    const T *__restrict__ v, const float *__restrict__ a,
+                    T *__restrict__ o, float *__restrict__ rec,
+                    float *__restrict__ S_out, float *__restrict__ z_out, int N,
+                    int P, int Pg, float eps, int nvb, const int *__restrict__ only_if) {
+  if (only_if && *only_if == 0) return;  // uniform: the tensor-core form ran
+  for (int vb = blockIdx.x; vb < nvb; vb += gridDim.x) {
+    gla_simt_block<D, DV, PASS, T>(q, k, v, a, o, rec, S_out, z_out, N, P, Pg, eps, vb);
+    __syncthreads();  // shared memory is reused by the next block
+  }
+}
+
 // In place over the records of one (batch, head): record p becomes the state
 // after part p, S_after(p) = g_p (.) S_after(p-1) + A_p (rows scaled by g_p).
-// grid: x = (batch, head), y = blocks over the D*Dv + D state entries.
+// grid: x strides over the BH (batch, head) pairs, y = blocks over the
+// D*Dv + D state entries.
 template <int D, int DV>
-__global__ void __launch_bounds__(256) gla_scan_kernel(float *__restrict__ rec, int P,
+__global__ void __launch_bounds__(256) gla_scan_kernel(float *__restrict__ rec, int P, int BH,
                                                       const int *__restrict__ only_if) {
   if (only_if && *only_if == 0) return;
   constexpr size_t R = record_floats<D, DV>();
   const int i = blockIdx.y * blockDim.x + threadIdx.x;
   if (i >= D * DV + D) return;
   const int d = i < D * DV ? i / DV : i - D * DV;
-  float *r = rec + static_cast<size_t>(blockIdx.x) * (P - 1) * R;
-  float carry = 0.f;
-  for (int p = 0; p < P - 1; ++p) {
-    float *rp = r + p * R;
-    carry = fmaf(rp[D * DV + D + d], carry, rp[i]);
-    rp[i] = carry;
+  for (int bh = blockIdx.x; bh < BH; bh += gridDim.x) {
+    float *r = rec + static_cast<size_t>(bh) * (P - 1) * R;
+    float carry = 0.f;
+    for (int p = 0; p < P - 1; ++p) {
+      float *rp = r + p * R;
+      carry = fmaf(rp[D * DV + D + d], carry, rp[i]);
+      rp[i] = carry;
+    }
   }
 }
 
@@ -515,16 +535,25 @@ cudaError_t gla_typed(const Problem &p, const float *a, float *ws, int P, float 
   const T *q = static_cast<const T *>(p.q), *k = static_cast<const T *>(p.k),
           *v = static_cast<const T *>(p.v);
   T *o = static_cast<T *>(p.o);
+  // behind the tensor-core form: grids of one wave (two CTAs per SM of the
+  // passes, eight of the scan), strided over the blocks
+  const long long sms = num_sms_gla();
+  auto cap = [&](long long nblocks, long long per_wave) {
+    return static_cast<unsigned>(only_if && nblocks > per_wave ? per_wave : nblocks);
+  };
+  const int ys = DV / kDvs, yscan = (D * DV + D + 255) / 256;
+  const long long pass_wave = (2 * sms + ys - 1) / ys, scan_wave = (8 * sms + yscan - 1) / yscan;
   if (P > 1) {
-    kst<<<dim3((unsigned)(BH * (P - 1)), DV / kDvs), kThreads, smem, s>>>(
-        q, k, v, a, o, ws, nullptr, nullptr, p.N, P, P - 1, p.eps, only_if);
+    const int nvb = BH * (P - 1);
+    kst<<<dim3(cap(nvb, pass_wave), ys), kThreads, smem, s>>>(q, k, v, a, o, ws, nullptr, nullptr, p.N,
+                                                              P, P - 1, p.eps, nvb, only_if);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    gla_scan_kernel<D, DV><<<dim3((unsigned)BH, (D * DV + D + 255) / 256), 256, 0, s>>>(ws, P,
-                                                                                      only_if);
+    gla_scan_kernel<D, DV><<<dim3(cap(BH, scan_wave), yscan), 256, 0, s>>>(ws, P, BH, only_if);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  kout<<<dim3((unsigned)(BH * P), DV / kDvs), kThreads, smem, s>>>(
-      q, k, v, a, o, ws, S_out, z_out, p.N, P, P, p.eps, only_if);
+  const int nvb = BH * P;
+  kout<<<dim3(cap(nvb, pass_wave), ys), kThreads, smem, s>>>(q, k, v, a, o, ws, S_out, z_out, p.N, P, P,
+                                                             p.eps, nvb, only_if);
   return cudaGetLastError();
 }
 
@@ -547,15 +576,36 @@ cudaError_t gla_shape(const Problem &p, const float *a, float *ws, int P, float 
 // for s <= t, and the state carried from the previous chunk enters token t
 // as qh_t . (gate product) S.  A chunk whose gate product falls below 2^-93
 // in some feature (r_t could leave the bf16 range) sets *hard.
-// grid: (batch, head) x 128-token chunks, 64 threads; thread j owns
-// features 2j and 2j + 1 (4-byte bf16 pairs and 8-byte gate pairs, so every
-// warp access is a full 128-byte line).
+// phi for operands rounded to bf16 next: __expf's error (a few fp32 ulp at
+// the inputs' scale) is far below bf16's 2^-8 spacing, and it avoids the
+// accurate expf's range reduction (branches and FMAs that held this
+// HBM-bound kernel to about 0.8 of its bandwidth)
+__device__ __forceinline__ float phi_bf16_operand(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// With P > 1 parts per (batch, head) (the part split of the 128-token
+// kernel), the block that finishes the last chunk of a part also writes that
+// part's gate tables: per chunk c of part q, gsuf[c] = the product of gp over
+// the chunks after c in q, and gpart[q] = the product of gp over q.  Each
+// block publishes its gp behind a fence and counts itself in done[bh * P + q]
+// (zero at launch); the block whose count completes the part reads the
+// others' gp from L2.  Nothing waits.
+// grid: B*H*chunks blocks of 64 threads; thread j owns features 2j, 2j + 1
+// and walks the chunk's tokens from the last, loading kT tokens before it
+// computes and stores the first of them, so that each warp keeps kT rows of
+// reads in flight (eight gave 0.89 of the copy bandwidth; wider accesses per
+// thread with fewer warps were slower).
 __global__ void __launch_bounds__(64)
     gla_tc_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                        const float *__restrict__ a, __nv_bfloat16 *__restrict__ qh,
                        __nv_bfloat16 *__restrict__ kh, float *__restrict__ gp,
-                       int *__restrict__ hard, int N) {
-  constexpr int kD128 = 128, kC128 = 128;
+                       float *__restrict__ gsuf, float *__restrict__ gpart,
+                       unsigned *__restrict__ done, int *__restrict__ hard, int N, int P) {
+  constexpr int kD128 = 128, kC128 = 128, kT = 8;
   const int j = threadIdx.x;
   const int nch = (N + kC128 - 1) / kC128;
   const int64_t bh = blockIdx.x / nch;
@@ -563,21 +613,62 @@ __global__ void __launch_bounds__(64)
   const int c0 = c * kC128, nv = min(kC128, N - c0);
   const int64_t base = (bh * N + c0) * kD128 + 2 * j;
   float r0 = 1.f, r1 = 1.f;
-#pragma unroll 8
-  for (int t = nv - 1; t >= 0; --t) {
-    const int64_t off = base + static_cast<int64_t>(t) * kD128;
-    const float2 xq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(q + off));
-    const float2 xk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(k + off));
-    const float2 ga = *reinterpret_cast<const float2 *>(a + off);
-    *reinterpret_cast<__nv_bfloat162 *>(qh + off) =
-        __floats2bfloat162_rn(phi_f32(xq.x) / r0, phi_f32(xq.y) / r1);
-    *reinterpret_cast<__nv_bfloat162 *>(kh + off) =
-        __floats2bfloat162_rn(phi_f32(xk.x) * r0, phi_f32(xk.y) * r1);
-    r0 *= ga.x;
-    r1 *= ga.y;
+  for (int t0 = nv - 1; t0 >= 0; t0 -= kT) {
+    uint32_t wq[kT], wk[kT];
+    float2 ga[kT];
+#pragma unroll
+    for (int u = 0; u < kT; ++u) {
+      if (t0 - u < 0) break;
+      const int64_t off = base + static_cast<int64_t>(t0 - u) * kD128;
+      wq[u] = __ldcs(reinterpret_cast<const unsigned int *>(q + off));
+      wk[u] = __ldcs(reinterpret_cast<const unsigned int *>(k + off));
+      ga[u] = __ldcs(reinterpret_cast<const float2 *>(a + off));
+    }
+#pragma unroll
+    for (int u = 0; u < kT; ++u) {
+      if (t0 - u < 0) break;
+      const int64_t off = base + static_cast<int64_t>(t0 - u) * kD128;
+      const float q0 = __uint_as_float(wq[u] << 16), q1 = __uint_as_float(wq[u] & 0xffff0000u);
+      const float k0 = __uint_as_float(wk[u] << 16), k1 = __uint_as_float(wk[u] & 0xffff0000u);
+      // r stays within [2^-93, 1] on every chunk not flagged hard, where the
+      // fast divide is within 2 ulp of fp32 before the bf16 rounding
+      __stcs(reinterpret_cast<unsigned int *>(qh + off),
+             bf16x2_bits(__fdividef(phi_bf16_operand(q0), r0), __fdividef(phi_bf16_operand(q1), r1)));
+      __stcs(reinterpret_cast<unsigned int *>(kh + off),
+             bf16x2_bits(phi_bf16_operand(k0) * r0, phi_bf16_operand(k1) * r1));
+      r0 *= ga[u].x;
+      r1 *= ga[u].y;
+    }
   }
   *reinterpret_cast<float2 *>(gp + (bh * nch + c) * kD128 + 2 * j) = make_float2(r0, r1);
   if (!(r0 >= 0x1p-93f) || !(r1 >= 0x1p-93f)) *hard = 1;
+  if (P <= 1) return;
+  // the part of chunk c: the first nch % P parts have one chunk more
+  const int base_n = nch / P, rem = nch % P;
+  const int part = c < rem * (base_n + 1) ? c / (base_n + 1) : rem + (c - rem * (base_n + 1)) / base_n;
+  const int cb = chunk_part_begin(part, P, nch), ce = chunk_part_begin(part + 1, P, nch);
+  __shared__ unsigned last;
+  __threadfence();
+  __syncthreads();
+  if (j == 0) last = atomicAdd(done + bh * P + part, 1u) == static_cast<unsigned>(ce - cb - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  float s0 = 1.f, s1 = 1.f;
+  for (int c1 = ce - 1; c1 >= cb; c1 -= kT) {
+    float2 g[kT];
+#pragma unroll
+    for (int u = 0; u < kT; ++u)
+      if (c1 - u >= cb) g[u] = __ldcg(reinterpret_cast<const float2 *>(gp + (bh * nch + c1 - u) * kD128 + 2 * j));
+#pragma unroll
+    for (int u = 0; u < kT; ++u)
+      if (c1 - u >= cb) {
+        *reinterpret_cast<float2 *>(gsuf + (bh * nch + c1 - u) * kD128 + 2 * j) = make_float2(s0, s1);
+        s0 *= g[u].x;
+        s1 *= g[u].y;
+      }
+  }
+  *reinterpret_cast<float2 *>(gpart + (bh * P + part) * kD128 + 2 * j) = make_float2(s0, s1);
 }
 
 }  // namespace
@@ -620,31 +711,14 @@ cudaError_t launch_gla_simt(const Problem &p, const float *a, void *ws, int P, f
                          : gla_shape<__nv_bfloat16>(p, a, w, P, S_out, z_out, only_if, s);
 }
 
-// The gate tables of the part split (P parts of the 128-token kernel): per
-// chunk c of part q, gsuf[c] = product of gp over the chunks after c in q;
-// gpart[q] = product of gp over q.  grid: (batch, head) x P, thread d owns
-// feature d.
-__global__ void __launch_bounds__(128)
-    gla_tc_tables_kernel(const float *__restrict__ gp, float *__restrict__ gsuf,
-                         float *__restrict__ gpart, int N, int P) {
-  constexpr int kD128 = 128;
-  const int d = threadIdx.x;
-  const int nch = (N + 127) / 128;
-  const int64_t bh = blockIdx.x / P;
-  const int q = static_cast<int>(blockIdx.x % P);
-  const int cb = chunk_part_begin(q, P, nch), ce = chunk_part_begin(q + 1, P, nch);
-  float suf = 1.f;
-  for (int c = ce - 1; c >= cb; --c) {
-    const size_t i = (static_cast<size_t>(bh) * nch + c) * kD128 + d;
-    gsuf[i] = suf;
-    suf *= gp[i];
-  }
-  gpart[(static_cast<size_t>(bh) * P + q) * kD128 + d] = suf;
-}
-
 bool gla_tc_supported(const Problem &p) {
   return p.dtype == kBF16 && p.D == 128 && p.Dv == 128 && p.N > 0 &&
          static_cast<long long>(p.B) * p.H >= 8;
+}
+
+// the hard flag and the per-(batch, head, part) chunk counts of the prep kernel
+static size_t gla_tc_header_bytes(int BH, int P) {
+  return (sizeof(int) + sizeof(unsigned) * static_cast<size_t>(BH) * P + 255) & ~static_cast<size_t>(255);
 }
 
 size_t gla_tc_workspace_bytes(int BH, int N) {
@@ -652,7 +726,8 @@ size_t gla_tc_workspace_bytes(int BH, int N) {
   const size_t nch = (static_cast<size_t>(N) + 127) / 128;
   const int P = chunk128_parts(BH, N);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return 256 + 2 * up(rows * 128 * 2) + 2 * up(static_cast<size_t>(BH) * nch * 128 * 4) +
+  // [hard flag, per-part chunk counts][qh][kh][gp][gsuf][gpart][chunk kernel]
+  return gla_tc_header_bytes(BH, P) + 2 * up(rows * 128 * 2) + 2 * up(static_cast<size_t>(BH) * nch * 128 * 4) +
          up(static_cast<size_t>(BH) * P * 128 * 4) + up(chunk128_workspace_bytes(BH, P));
 }
 
@@ -663,27 +738,26 @@ cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream
   const size_t rows = static_cast<size_t>(BH) * p.N;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   uint8_t *w = static_cast<uint8_t *>(ws);
+  const int P = chunk128_parts(BH, p.N);
+  const size_t hdr = gla_tc_header_bytes(BH, P);
   int *hard = reinterpret_cast<int *>(w);
-  __nv_bfloat16 *qh = reinterpret_cast<__nv_bfloat16 *>(w + 256);
-  __nv_bfloat16 *kh = reinterpret_cast<__nv_bfloat16 *>(w + 256 + up(rows * 128 * 2));
+  unsigned *done = reinterpret_cast<unsigned *>(w + sizeof(int));
+  __nv_bfloat16 *qh = reinterpret_cast<__nv_bfloat16 *>(w + hdr);
+  __nv_bfloat16 *kh = reinterpret_cast<__nv_bfloat16 *>(w + hdr + up(rows * 128 * 2));
   const int nch = (p.N + 127) / 128;
   const size_t ntab = up(static_cast<size_t>(BH) * nch * 128 * 4);
-  const int P = chunk128_parts(BH, p.N);
-  float *gp = reinterpret_cast<float *>(w + 256 + 2 * up(rows * 128 * 2));
+  float *gp = reinterpret_cast<float *>(w + hdr + 2 * up(rows * 128 * 2));
   float *gsuf = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(gp) + ntab);
   float *gpart = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(gsuf) + ntab);
   void *cws = reinterpret_cast<uint8_t *>(gpart) + up(static_cast<size_t>(BH) * P * 128 * 4);
-  cudaError_t e = cudaMemsetAsync(hard, 0, sizeof(int), s);
+  cudaError_t e = cudaMemsetAsync(w, 0, sizeof(int) + sizeof(unsigned) * static_cast<size_t>(BH) * P, s);
   if (e != cudaSuccess) return e;
+  // one block per (batch, head, chunk); the gate tables come from the block
+  // that completes each part
   gla_tc_prep_kernel<<<(unsigned)(static_cast<long long>(BH) * nch), 64, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), a, qh, kh,
-      gp, hard, p.N);
+      gp, gsuf, gpart, done, hard, p.N, P);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (P > 1) {
-    gla_tc_tables_kernel<<<(unsigned)(static_cast<long long>(BH) * P), 128, 0, s>>>(gp, gsuf, gpart,
-                                                                                   p.N, P);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   Problem pf = p;
   pf.q = qh;
   pf.k = kh;
