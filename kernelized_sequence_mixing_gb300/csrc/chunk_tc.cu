@@ -562,42 +562,45 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
         mbar_wait_drain(&full[c % S], (c / S) & 1);
     }
   } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer (warp-wide loop, lane 0 issues) ----------------
-    const bool leader = lane == 0;
-    constexpr uint32_t ID_A = idesc_bf16(64, 64, false, false);
-    constexpr uint32_t ID_DS = idesc_bf16(128, NA, true, true);
-    constexpr uint32_t ID_O = idesc_bf16(64, NA, false, true);
-    constexpr uint64_t kStageU = L::kStageBytes >> 4;
-    const uint32_t base = smem_u32(sm);
-    // q, k: K-major (K = d); kh^T: MN-major (M = d, K = tokens); [V | 1]:
-    // MN-major (N = value column, K = tokens); P: K-major; [T | z]: MN-major
-    // (N = value column, K = d).  Variants differ in the start address only.
-    const uint64_t dq0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
-    const uint64_t dk0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
-    // kh^T (its low parts) and [V | 1]: the second atom (zero box, ones box)
-    // is in the stage at the next box, except where it is a shared copy
-    const uint64_t dkt0 = smem_desc(base + L::kOffK, kBox, 1024, kSw128);
-    const uint64_t dktlo0 = smem_desc(base + L::kOffKlo, (MODE == kCausal && D == 64) ? 2 * kBox : kBox, 1024, kSw128);
-    const uint64_t dv0 = smem_desc(base + L::kOffV, kBox, 1024, kSw128);
-    // state mode, per stage: start address field as usual, LBO to the shared box
-    auto desc_state = [&](int st, int off, bool shared, int shared_off) {
-      const uint32_t a = base + st * L::kStageBytes + off;
-      return smem_desc(a, shared ? base + shared_off - a : kBox, 1024, kSw128);
-    };
-    const uint64_t dp0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
-    const uint64_t dsop0 = smem_desc(base + L::kOffSop, L::kSopAtom, 512, kSw64);
-    const uint32_t tA = tmem + L::kColA, tT = tmem + L::kColT;
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    // phase A: T = kh^T [V | 1] over the part
-    for (int i = 0; i < nA; ++i) {
-      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (leader) {
+    // ---------------- MMA issuer: lane 0 alone ----------------
+    // One thread waits and issues: a warp-wide loop paid a vote and a
+    // reconvergence around every wait and every issue, which kept the tensor
+    // pipe idle most of each chunk (its own MMAs need about 850 cycles of a
+    // chunk's 2700 at D = Dv = 64).
+    if (lane == 0) {
+      constexpr uint32_t ID_A = idesc_bf16(64, 64, false, false);
+      constexpr uint32_t ID_DS = idesc_bf16(128, NA, true, true);
+      constexpr uint32_t ID_O = idesc_bf16(64, NA, false, true);
+      constexpr uint64_t kStageU = L::kStageBytes >> 4;
+      const uint32_t base = smem_u32(sm);
+      // q, k: K-major (K = d); kh^T: MN-major (M = d, K = tokens); [V | 1]:
+      // MN-major (N = value column, K = tokens); P: K-major; [T | z]: MN-major
+      // (N = value column, K = d).  Variants differ in the start address only.
+      const uint64_t dq0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
+      const uint64_t dk0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
+      // kh^T (its low parts) and [V | 1]: the second atom (zero box, ones box)
+      // is in the stage at the next box, except where it is a shared copy
+      const uint64_t dkt0 = smem_desc(base + L::kOffK, kBox, 1024, kSw128);
+      const uint64_t dktlo0 = smem_desc(base + L::kOffKlo, (MODE == kCausal && D == 64) ? 2 * kBox : kBox, 1024, kSw128);
+      const uint64_t dv0 = smem_desc(base + L::kOffV, kBox, 1024, kSw128);
+      // state mode, per stage: start address field as usual, LBO to the shared box
+      auto desc_state = [&](int st, int off, bool shared, int shared_off) {
+        const uint32_t a = base + st * L::kStageBytes + off;
+        return smem_desc(a, shared ? base + shared_off - a : kBox, 1024, kSw128);
+      };
+      const uint64_t dp0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
+      const uint64_t dsop0 = smem_desc(base + L::kOffSop, L::kSopAtom, 512, kSw64);
+      const uint32_t tA = tmem + L::kColA, tT = tmem + L::kColT;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      // phase A: T = kh^T [V | 1] over the part
+      for (int i = 0; i < nA; ++i) {
+        if (!mbar_wait(&mapped[s], ph, abort_flag, p.timeouts)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * kStageU;
         if (MODE == kState) {
           const uint64_t dk = desc_state(s, L::kOffK, D == 64, L::kOffZero);
@@ -614,26 +617,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
             mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      __syncwarp();
-      if (++s == S) {
-        s = 0;
-        ph ^= 1;
+      if (ok && hasA) {
+        mma_commit(T_ready);
       }
-    }
-    if (ok && hasA) {
-      if (leader) mma_commit(T_ready);
-      __syncwarp();
-    }
-    // phase C.  Iteration i issues chunk i+1's A' first, then chunk i's
-    // [dS | dz], inter- and intra-chunk MMAs, so the P warps turn A'_(i+1)
-    // into P while the tensor pipe works on chunk i: every wait below has
-    // about a chunk of queued work in front of it.  (A' has one buffer: the
-    // P warps have read A'_i long before A'_(i+1) is issued.)
-    auto issue_a = [&](int j, int st) -> bool {  // A'_j = qh kh^T (M 64 t, N 64 s, K = D)
-      if (!warp_wait(A_free, (j & 1) ^ 1, abort_flag, p.timeouts)) return false;
-      tc_fence_after();
-      if (leader) {
+      // phase C.  Iteration i issues chunk i+1's A' first, then chunk i's
+      // [dS | dz], inter- and intra-chunk MMAs, so the P warps turn A'_(i+1)
+      // into P while the tensor pipe works on chunk i: every wait below has
+      // about a chunk of queued work in front of it.  (A' has one buffer: the
+      // P warps have read A'_i long before A'_(i+1) is issued.)
+      auto issue_a = [&](int j, int st) -> bool {  // A'_j = qh kh^T (M 64 t, N 64 s, K = D)
+        if (!mbar_wait(A_free, (j & 1) ^ 1, abort_flag, p.timeouts)) return false;
+        tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(st) * kStageU;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -641,71 +640,57 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
           mma_bf16(tA, dq0 + off, dk0 + off, ID_A, kk > 0 ? 1u : 0u);
         }
         mma_commit(A_full);
+        return true;
+      };
+      if (ok && kPhaseC && nch > 0 && MODE == kCausal) {
+        if (!mbar_wait(&mapped[s], ph, abort_flag, p.timeouts) || !issue_a(0, s)) ok = false;
       }
-      __syncwarp();
-      return true;
-    };
-    if (ok && kPhaseC && nch > 0 && MODE == kCausal) {
-      if (!warp_wait(&mapped[s], ph, abort_flag, p.timeouts) || !issue_a(0, s)) ok = false;
-    }
-    for (int i = 0; ok && kPhaseC && i < nch; ++i) {
-      const int b = i & 1;
-      const uint32_t u = static_cast<uint32_t>(i >> 1);
-      const uint64_t so = static_cast<uint64_t>(s) * kStageU;
-      int s1 = s + 1;
-      uint32_t ph1 = ph;
-      if (s1 == S) {
-        s1 = 0;
-        ph1 ^= 1;
-      }
-      if (MODE == kCausal) {
-        if (i + 1 < nch) {
-          if (!warp_wait(&mapped[s1], ph1, abort_flag, p.timeouts)) break;
-          if (!issue_a(i + 1, s1)) break;
-          // T += kh^T [V | 1]: not needed after the last chunk
-          if (!warp_wait(T_free, i & 1, abort_flag, p.timeouts)) break;
-          tc_fence_after();
-          if (leader) {
+      for (int i = 0; ok && kPhaseC && i < nch; ++i) {
+        const int b = i & 1;
+        const uint32_t u = static_cast<uint32_t>(i >> 1);
+        const uint64_t so = static_cast<uint64_t>(s) * kStageU;
+        int s1 = s + 1;
+        uint32_t ph1 = ph;
+        if (s1 == S) {
+          s1 = 0;
+          ph1 ^= 1;
+        }
+        if (MODE == kCausal) {
+          if (i + 1 < nch) {
+            if (!mbar_wait(&mapped[s1], ph1, abort_flag, p.timeouts)) break;
+            if (!issue_a(i + 1, s1)) break;
+            // T += kh^T [V | 1]: not needed after the last chunk
+            if (!mbar_wait(T_free, i & 1, abort_flag, p.timeouts)) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kC / 16; ++kk)
               mma_bf16(tT, dkt0 + so + kk * 128, dv0 + so + kk * 128, ID_DS, 1u);
             mma_commit(T_ready);
           }
-          __syncwarp();
         }
-      }
-      // O = qh [T | z]  (M 64, N Dv + 16, K = D)
-      if (!warp_wait(&O_free[b], (u & 1) ^ 1, abort_flag, p.timeouts)) break;
-      if (!warp_wait(S_full, static_cast<uint32_t>(i & 1), abort_flag, p.timeouts)) break;
-      tc_fence_after();
-      const uint32_t tO = tmem + L::kColO + b * NA;
-      if (leader) {
+        // O = qh [T | z]  (M 64, N Dv + 16, K = D)
+        if (!mbar_wait(&O_free[b], (u & 1) ^ 1, abort_flag, p.timeouts)) break;
+        if (!mbar_wait(S_full, static_cast<uint32_t>(i & 1), abort_flag, p.timeouts)) break;
+        tc_fence_after();
+        const uint32_t tO = tmem + L::kColO + b * NA;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16(tO, dq0 + so + (kk >> 2) * (kBox >> 4) + (kk & 3) * 2, dsop0 + kk * 64, ID_O,
                    kk > 0 ? 1u : 0u);
         if (MODE == kCausal) mma_commit(S_free);
-      }
-      __syncwarp();
-      if (MODE == kCausal) {
-        // O += P [V | 1]  (M 64, N Dv + 16, K 64 tokens)
-        if (!warp_wait(P_full, i & 1, abort_flag, p.timeouts)) break;
-        tc_fence_after();
-        if (leader) {
+        if (MODE == kCausal) {
+          // O += P [V | 1]  (M 64, N Dv + 16, K 64 tokens)
+          if (!mbar_wait(P_full, i & 1, abort_flag, p.timeouts)) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kC / 16; ++kk) mma_bf16(tO, dp0 + kk * 2, dv0 + so + kk * 128, ID_O, 1u);
         }
-      }
-      if (leader) {
         mma_commit(&O_full[b]);
         mma_commit(&empty[s]);
+        s = s1;
+        ph = ph1;
       }
-      __syncwarp();
-      s = s1;
-      ph = ph1;
-    }
-    // every MMA issued has completed before TMEM is released
-    if (leader) {
+      // every MMA issued has completed before TMEM is released
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
