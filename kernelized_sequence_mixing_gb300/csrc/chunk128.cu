@@ -302,6 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int part = item[0], bh = item[1];
+  // identity features without decay or gates (Performer features): the
+  // phase-C k map would multiply every row by one (rows past the sequence
+  // end are already zero from the copy's bounds), so it is skipped.  (The
+  // gated mode's and phase A's maps are kept: skipping them made ptxas spill
+  // in the per-chunk loops.)
+  constexpr bool kMapK = !(IDENT && !DECAY && !GATED);
 
   // the part: chunks [cb, cb + nch) of this (batch, head); phase A runs
   // over the previous part, chunks [cbA, cbA + nA)
@@ -675,8 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int jw = i % WC;  // chunk within its decay window
       // kh_s = gamma^(E - s) phi(k_s), rows past the sequence end zero
       if (!warp_wait(&bar[kKFull + sl], (c >> 1) & 1, abort_flag, p.timeouts)) break;
-      map_row<IDENT>(sm + kOffK + sl * kKSlot + h * kKBox, r,
-              r < nv ? scale2(static_cast<float>(W - 1 - kC * jw - r)) : 0u);
+      if (kMapK)
+        map_row<IDENT>(sm + kOffK + sl * kKSlot + h * kKBox, r,
+                       r < nv ? scale2(static_cast<float>(W - 1 - kC * jw - r)) : 0u);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_cnt(&bar[kKMapped + sl], 2);
