@@ -302,12 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int part = item[0], bh = item[1];
-  // identity features without decay or gates (Performer features): the
-  // phase-C k map would multiply every row by one (rows past the sequence
-  // end are already zero from the copy's bounds), so it is skipped.  (The
-  // gated mode's and phase A's maps are kept: skipping them made ptxas spill
-  // in the per-chunk loops.)
-  constexpr bool kMapK = !(IDENT && !DECAY && !GATED);
+  // identity features without per-row decay (Performer features, gated
+  // k-hat): the phase-C k map would multiply every row by one (rows past the
+  // sequence end are already zero from the copy's bounds), so it is skipped;
+  // the gated mode keeps the call for rows past the end (a no-op at run time
+  // on full chunks: without it ptxas spilled in the per-chunk loops).  Phase
+  // A's map is kept for the same reason.
+  constexpr bool kMapK = !(IDENT && !DECAY);
 
   // the part: chunks [cb, cb + nch) of this (batch, head); phase A runs
   // over the previous part, chunks [cbA, cbA + nA)
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       const int jw = i % WC;  // chunk within its decay window
       // kh_s = gamma^(E - s) phi(k_s), rows past the sequence end zero
       if (!warp_wait(&bar[kKFull + sl], (c >> 1) & 1, abort_flag, p.timeouts)) break;
-      if (kMapK)
+      if (kMapK || GATED && r >= nv)
         map_row<IDENT>(sm + kOffK + sl * kKSlot + h * kKBox, r,
                        r < nv ? scale2(static_cast<float>(W - 1 - kC * jw - r)) : 0u);
       fence_async_smem();
