@@ -304,10 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
   const int part = item[0], bh = item[1];
   // identity features without per-row decay (Performer features, gated
   // k-hat): the phase-C k map would multiply every row by one (rows past the
-  // sequence end are already zero from the copy's bounds), so it is skipped;
-  // the gated mode keeps the call for rows past the end (a no-op at run time
-  // on full chunks: without it ptxas spilled in the per-chunk loops).  Phase
-  // A's map is kept for the same reason.
+  // sequence end are already zero from the copy's bounds), so it is skipped,
+  // in phase A too; the call stays for rows past the end (a no-op at run
+  // time on full chunks: without it ptxas spilled in the per-chunk loops).
   constexpr bool kMapK = !(IDENT && !DECAY);
 
   // the part: chunks [cb, cb + nch) of this (batch, head); phase A runs
@@ -363,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk128_kernel(const __grid_cons
       if (GATED) {
         map_row4_feat(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), f_lane,
                       r < nv);
-      } else {
+      } else if (kMapK || r >= nv) {
         const uint32_t sc = r < nv ? scale2(static_cast<float>(kC * (nA - ia) - 1 - r)) : 0u;
         map_row4<IDENT>(sm + kOffK + sl * kKSlot + (quarter >> 1) * kKBox, r, 4 * (quarter & 1), sc);
       }
