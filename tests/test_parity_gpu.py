@@ -98,13 +98,15 @@ def test_causal_small(la, ora, dtype, gkind, shape):
 # CTAs) and rescales its state once per decay window.  Many heads give one
 # part per head and windows of one chunk (gamma = 0.35 / 0.5) or several
 # (0.9, 0.99); fewer heads give several multi-chunk parts, so the state
-# crosses parts and windows (20 heads x 64 chunks: 5 parts of 12-13 chunks).
+# crosses parts and windows (20 heads x 64 chunks: 5 parts of 12-13 chunks,
+# skewed toward the front; 16 heads x 128 chunks: 7 skewed parts of 15-22).
 CAUSAL_PARTS = [
     # (B, H, N, D, Dv, gammas)
     (8, 76, 700, 64, 64, [0.35, 0.5, 0.9, 0.99]),
     (2, 100, 2560, 64, 64, [0.5, 0.9, 0.99, 1.0]),
     (1, 40, 1500, 128, 128, [0.6, 0.97, 1.0, 0.85]),
     (2, 10, 4096, 128, 64, [0.5, 0.35, 0.9, 0.999, 1.0]),
+    (1, 16, 8192, 64, 64, [0.4, 0.8, 0.95, 1.0]),
 ]
 
 
