@@ -567,15 +567,6 @@ cudaError_t gla_shape(const Problem &p, const float *a, float *ws, int P, float 
   return cudaErrorNotSupported;
 }
 
-// The operands of the gated tensor-core form (D = 128): per 128-token chunk
-// and feature d, with the suffix products r_t = a_(t+1) ... a_(last token of
-// the chunk),
-//   qh_t = phi(q_t) / r_t,   kh_t = phi(k_t) r_t   (bf16),
-// and the chunk's gate product a_(first) ... a_(last) (fp32), so that within
-// a chunk qh_t . kh_s = sum_d phi(q_t)[d] phi(k_s)[d] prod_(u=s+1..t) a_u[d]
-// for s <= t, and the state carried from the previous chunk enters token t
-// as qh_t . (gate product) S.  A chunk whose gate product falls below 2^-93
-// in some feature (r_t could leave the bf16 range) sets *hard.
 // phi for operands rounded to bf16 next: __expf's error (a few fp32 ulp at
 // the inputs' scale) is far below bf16's 2^-8 spacing, and it avoids the
 // accurate expf's range reduction (branches and FMAs that held this
@@ -587,6 +578,15 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
+// The operands of the gated tensor-core form (D = 128): per 128-token chunk
+// and feature d, with the suffix products r_t = a_(t+1) ... a_(last token of
+// the chunk),
+//   qh_t = phi(q_t) / r_t,   kh_t = phi(k_t) r_t   (bf16),
+// and the chunk's gate product a_(first) ... a_(last) (fp32), so that within
+// a chunk qh_t . kh_s = sum_d phi(q_t)[d] phi(k_s)[d] prod_(u=s+1..t) a_u[d]
+// for s <= t, and the state carried from the previous chunk enters token t
+// as qh_t . (gate product) S.  A chunk whose gate product falls below 2^-93
+// in some feature (r_t could leave the bf16 range) sets *hard.
 // With P > 1 parts per (batch, head) (the part split of the 128-token
 // kernel), the block that finishes the last chunk of a part also writes that
 // part's gate tables: per chunk c of part q, gsuf[c] = the product of gp over
