@@ -846,25 +846,26 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
           tc_fence_after();
           const bool rebase = DECAY && (i % WC == 0);
           if (!warp_wait(S_free, static_cast<uint32_t>((i - 1) & 1), abort_flag, p.timeouts)) break;
+          // two 32-column tiles at a time, or one where the decay rescale is
+          // compiled in (two spilled there)
+          constexpr int kTiles = DECAY ? 1 : 2;
 #pragma unroll 1
-          for (int cc = 0; cc < DV / 32; cc += 2) {
-            float x0[32], x1[32];
-            tmem_ld32(tT + 32 * cc, x0);
-            tmem_ld32(tT + 32 * cc + 32, x1);
+          for (int cc = 0; cc < DV / 32; cc += kTiles) {
+            float x[kTiles][32];
+#pragma unroll
+            for (int u = 0; u < kTiles; ++u) tmem_ld32(tT + 32 * (cc + u), x[u]);
             tmem_wait_ld();
             if (rebase) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                x0[e] *= gW;
-                x1[e] *= gW;
+              for (int u = 0; u < kTiles; ++u) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[u][e] *= gW;
+                tmem_st32(tT + 32 * (cc + u), x[u]);
               }
-              tmem_st32(tT + 32 * cc, x0);
-              tmem_st32(tT + 32 * cc + 32, x1);
             }
-            if (act) {
-              put_sop32(sop, kAtom, cc, d, x0);
-              put_sop32(sop, kAtom, cc + 1, d, x1);
-            }
+            if (act)
+#pragma unroll
+              for (int u = 0; u < kTiles; ++u) put_sop32(sop, kAtom, cc + u, d, x[u]);
           }
           {
             float x0[16];
