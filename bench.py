@@ -74,7 +74,8 @@ NCU_TRAFFIC = {
 # the other configurations of the method, timed in the same process as the
 # default workload and reported in its line under "workloads"
 EXTRA_WORKLOADS = ("causal_f32_n256", "causal_bf16_n4096", "noncausal_bf16_n65536",
-                   "decode_bf16_h32")
+                   "decode_bf16_h32", "gla_bf16_n16384", "favor_bf16_n16384",
+                   "backward_bf16_n4096")
 
 
 # ---------------------------------------------------------------------------
@@ -801,6 +802,7 @@ def time_extra(la, name, dev, hbm_peak, quick):
     gen = torch.Generator(device=dev)
     gen.manual_seed(w.seed)
     stream = torch.cuda.current_stream(dev)
+    gated_tc = bwd_tc = False  # the tensor-core forms, where the workload has one
     if w.steps:
         _, kp, vp = device_inputs(w, gen, dev)
         S, z = la.prefill_state(kp, vp, gamma=w.gamma())
@@ -819,14 +821,36 @@ def time_extra(la, name, dev, hbm_peak, quick):
     else:
         q, k, v = device_inputs(w, gen, dev)
         od = torch.empty((w.B, w.H, w.N, w.Dv), dtype=w.dtype, device=dev)
-        step_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, od))
+        # the gated forward's fp32 gates U[gate_lo, 1), the Performer's
+        # directions, the backward's upstream gradient N(0, 1) and its
+        # three gradients
+        extra = []
+        if w.gated:
+            extra = [torch.rand((w.B, w.H, w.N, w.D), generator=gen, device=dev) * (1.0 - w.gate_lo)
+                     + w.gate_lo]
+            gated_tc = la.gated_kernel(w.B, w.H, w.N, w.D, w.Dv, w.dtype) == "tensor-core"
+        elif w.backward:
+            extra = [torch.randn((w.B, w.H, w.N, w.Dv), generator=gen, device=dev).to(w.dtype),
+                     torch.empty_like(q), torch.empty_like(k)]
+            bwd_tc = la.backward_kernel(w.B, w.H, w.N, w.D, w.Dv, dtype=w.dtype) == "tensor-core"
+        if w.favor_r:
+            from kernelized_sequence_mixing_gb300.workloads import favor_matrix
+            Wd = favor_matrix(w.favor_r, w.D, w.seed + 2, True, w.dtype).to(dev)
+        step_bytes = sum(t.numel() * t.element_size() for t in [q, k, v, od] + extra)
         ncopy = 1 if step_bytes > L2_BYTES else -(-2 * L2_BYTES // step_bytes)
-        copies = [(q, k, v, od)] + [(q.clone(), k.clone(), v.clone(), torch.empty_like(od))
-                                    for _ in range(ncopy - 1)]
+        copies = [[q, k, v, od] + extra] + [[t.clone() for t in [q, k, v, od] + extra]
+                                            for _ in range(ncopy - 1)]
 
         def run(i):
-            qc, kc, vc, oc = copies[i % ncopy]
-            la.forward(qc, kc, vc, causal=w.causal, gamma=w.gamma(), eps=w.eps, out=oc)
+            c = copies[i % ncopy]
+            if w.gated:
+                la.forward_gated(c[0], c[1], c[2], c[4], eps=w.eps, out=c[3])
+            elif w.favor_r:
+                la.forward_favor(c[0], c[1], c[2], Wd, causal=w.causal, eps=w.eps, out=c[3])
+            elif w.backward:
+                la.backward(c[0], c[1], c[2], c[4], eps=w.eps, dq=c[5], dk=c[6], dv=c[3])
+            else:
+                la.forward(c[0], c[1], c[2], causal=w.causal, gamma=w.gamma(), eps=w.eps, out=c[3])
         nsteps = 20 if w.N * w.B * w.H >= (1 << 22) else 100
         warm = 5
         byts, flops = algorithmic_work(w)
@@ -891,7 +915,7 @@ def time_extra(la, name, dev, hbm_peak, quick):
     ms = total / nsteps
     gbs = byts / (ms / 1e3) / 1e9
     entry = {"ms_per_step": ms, "value": tokens / (ms / 1e3), "unit": "tokens/s",
-             "steps": nsteps, "dtype": compute_dtype(w),
+             "steps": nsteps, "dtype": compute_dtype(w, gated_tc, bwd_tc),
              "config": workload_config(w),
              "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                           "frac": gbs / hbm_peak, "algorithmic_bytes": byts,
