@@ -573,6 +573,15 @@ cudaError_t gla_shape(const Problem &p, const float *a, float *ws, int P, float 
 // HBM-bound kernel to about 0.8 of its bandwidth)
 __device__ __forceinline__ float phi_bf16_operand(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
+// barrier 1 or 2 (the block's first or second 64-thread half), with
+// immediate ids so that only those barriers are reserved
+__device__ __forceinline__ void half_sync(int half) {
+  if (half == 0)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 64;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
@@ -594,22 +603,28 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 // block publishes its gp behind a fence and counts itself in done[bh * P + q]
 // (zero at launch); the block whose count completes the part reads the
 // others' gp from L2.  Nothing waits.
-// grid: B*H*chunks blocks of 64 threads; thread j owns features 2j, 2j + 1
-// and walks the chunk's tokens from the last, loading kT tokens before it
-// computes and stores the first of them, so that each warp keeps kT rows of
-// reads in flight (eight gave 0.89 of the copy bandwidth; wider accesses per
-// thread with fewer warps were slower).
-__global__ void __launch_bounds__(64)
+// grid: ceil(B*H*chunks / 2) blocks of 128 threads, two chunks per block
+// (64 threads each, synchronised by their own named barrier); thread j of a
+// chunk owns features 2j, 2j + 1 and walks the chunk's tokens from the last,
+// loading kT tokens before it computes and stores the first of them, so that
+// each warp keeps kT rows of reads in flight (eight gave 0.89 of the copy
+// bandwidth; wider accesses per thread with fewer warps were slower, and
+// blocks of one chunk 3% slower than of two).
+__global__ void __launch_bounds__(128)
     gla_tc_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                        const float *__restrict__ a, __nv_bfloat16 *__restrict__ qh,
                        __nv_bfloat16 *__restrict__ kh, float *__restrict__ gp,
                        float *__restrict__ gsuf, float *__restrict__ gpart,
-                       unsigned *__restrict__ done, int *__restrict__ hard, int N, int P) {
+                       unsigned *__restrict__ done, int *__restrict__ hard, int N, int P,
+                       long long items) {
   constexpr int kD128 = 128, kC128 = 128, kT = 8;
-  const int j = threadIdx.x;
+  const int half = threadIdx.x >> 6;  // chunk of the block, and its barrier
+  const long long item = static_cast<long long>(blockIdx.x) * 2 + half;
+  if (item >= items) return;  // the second chunk of the last block: whole half
+  const int j = threadIdx.x & 63;
   const int nch = (N + kC128 - 1) / kC128;
-  const int64_t bh = blockIdx.x / nch;
-  const int c = static_cast<int>(blockIdx.x % nch);
+  const int64_t bh = item / nch;
+  const int c = static_cast<int>(item % nch);
   const int c0 = c * kC128, nv = min(kC128, N - c0);
   const int64_t base = (bh * N + c0) * kD128 + 2 * j;
   float r0 = 1.f, r1 = 1.f;
@@ -647,12 +662,12 @@ __global__ void __launch_bounds__(64)
   const int base_n = nch / P, rem = nch % P;
   const int part = c < rem * (base_n + 1) ? c / (base_n + 1) : rem + (c - rem * (base_n + 1)) / base_n;
   const int cb = chunk_part_begin(part, P, nch), ce = chunk_part_begin(part + 1, P, nch);
-  __shared__ unsigned last;
+  __shared__ unsigned last[2];
   __threadfence();
-  __syncthreads();
-  if (j == 0) last = atomicAdd(done + bh * P + part, 1u) == static_cast<unsigned>(ce - cb - 1);
-  __syncthreads();
-  if (!last) return;
+  half_sync(half);
+  if (j == 0) last[half] = atomicAdd(done + bh * P + part, 1u) == static_cast<unsigned>(ce - cb - 1);
+  half_sync(half);
+  if (!last[half]) return;
   __threadfence();
   float s0 = 1.f, s1 = 1.f;
   for (int c1 = ce - 1; c1 >= cb; c1 -= kT) {
@@ -752,11 +767,12 @@ cudaError_t launch_gla_tc(const Problem &p, const float *a, void *ws, cudaStream
   void *cws = reinterpret_cast<uint8_t *>(gpart) + up(static_cast<size_t>(BH) * P * 128 * 4);
   cudaError_t e = cudaMemsetAsync(w, 0, sizeof(int) + sizeof(unsigned) * static_cast<size_t>(BH) * P, s);
   if (e != cudaSuccess) return e;
-  // one block per (batch, head, chunk); the gate tables come from the block
-  // that completes each part
-  gla_tc_prep_kernel<<<(unsigned)(static_cast<long long>(BH) * nch), 64, 0, s>>>(
+  // two (batch, head, chunk) items per block; the gate tables come from the
+  // item that completes each part
+  const long long items = static_cast<long long>(BH) * nch;
+  gla_tc_prep_kernel<<<(unsigned)((items + 1) / 2), 128, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), a, qh, kh,
-      gp, gsuf, gpart, done, hard, p.N, P);
+      gp, gsuf, gpart, done, hard, p.N, P, items);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   Problem pf = p;
   pf.q = qh;
