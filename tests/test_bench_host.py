@@ -244,3 +244,24 @@ def test_oracle_timing_counts_tokens_across_heads():
                     step_seed0=1000)
     units_tokens, times, _ = bench.time_oracle_decode(d, 16, 1)
     assert units_tokens == 16 / 8 and len(times) == 1
+
+
+def test_extra_workloads_cover_every_kind_beside_the_main_line():
+    """The configurations timed beside the default line: each a defined
+    workload other than the default, with positive algorithmic work, and
+    together every kind of step (short causal, fp32, non-causal, decode,
+    gated, Performer, backward)."""
+    extras = bench.EXTRA_WORKLOADS
+    assert len(set(extras)) == len(extras)
+    assert bench.DEFAULT_WORKLOAD not in extras
+    for name in extras:
+        w = WORKLOADS[name]
+        byts, flops = bench.decode_work(w) if w.steps else bench.algorithmic_work(w)
+        assert byts > 0 and flops > 0, name
+    ws = [WORKLOADS[n] for n in extras]
+    assert any(w.dtype == torch.float32 for w in ws)
+    assert any(not w.causal for w in ws)
+    assert any(w.steps for w in ws)
+    assert any(w.gated for w in ws)
+    assert any(w.favor_r for w in ws)
+    assert any(w.backward for w in ws)
