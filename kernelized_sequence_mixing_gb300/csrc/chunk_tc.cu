@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_tc_kernel(const __grid_cons
   // more chunks (a later part starts phase C later: its look-back waits for
   // more records, and part 0 has no phase A); for P = 4, 64 chunks split 17,
   // 17, 15, 15, about 3% faster than equal parts.  Every part keeps
-  // pbase - (P - 1) / 2 >= 1 chunks, as P <= sqrt(0.43 chunks) (chunk_parts).
+  // pbase - (P - 1) / 2 >= 1 chunks: the host sets p.skew only then.
   const bool skew = MODE == kCausal && p.skew && pbase >= 8;
   auto part_begin = [&](int q) { return q * pbase + min(q, prem) + (skew ? q * (P - q) / 2 : 0); };
   const int cb = part_begin(part);
@@ -1099,7 +1099,11 @@ cudaError_t launch_causal_chunk(const Problem &p, const Gammas &g, void *ws, int
   prm.P = P;
   prm.rec_parts = P;
   prm.eps = p.eps;
-  prm.skew = 1;
+  // skewed parts only while the last part keeps a chunk: the skew moves its
+  // start (P - 1) / 2 chunks later (true of every part count chunk_parts
+  // gives; a caller's larger P falls back to equal parts)
+  const int nch_all = (p.N + kC - 1) / kC;
+  prm.skew = P >= 1 && nch_all / P - (P - 1) / 2 >= 1;
   if (P > 1) {
     if (!ws) return cudaErrorInvalidValue;
     // flags and ticket start at zero; the records need no initialisation
