@@ -365,6 +365,44 @@ def test_state_in_continues_sequence(oracle_mod):
     assert rel_err(o_tail, o_full[23:]) < 1e-13
 
 
+def test_decode_step_closed_forms(oracle_mod):
+    """gamma = 0 forgets the carried state: S' = phi(k) v^T, z' = phi(k) and
+    o = v a / (a + eps) with a = phi(q).phi(k), whatever (S, z) held; v = 0
+    leaves S' = gamma S exactly (the update adds phi(k) 0^T)."""
+    D, Dv, eps = 5, 3, 0.25
+    q, k, v = rng_inputs(23, 1, D, Dv)
+    rng = np.random.default_rng(24)
+    S0 = rng.uniform(0.5, 2.0, (D, Dv))
+    z0 = rng.uniform(0.5, 2.0, D)
+    o, S, z = oracle_mod.decode_step(q[0], k[0], v[0], S0.copy(), z0.copy(),
+                                     gamma=0.0, eps=eps)
+    fq, fk = phi_np(q[0]), phi_np(k[0])
+    a = float(fq @ fk)
+    assert rel_err(o, v[0].astype(np.float64) * (a / (a + eps))) < 1e-14
+    assert rel_err(S, np.outer(fk, v[0])) < 1e-15 and rel_err(z, fk) < 1e-15
+    _, S, _ = oracle_mod.decode_step(q[0], k[0], np.zeros(Dv, np.float32),
+                                     S0.copy(), z0.copy(), gamma=0.75, eps=eps)
+    assert np.array_equal(S, 0.75 * S0)
+
+
+@pytest.mark.parametrize("gamma", [1.0, 0.8])
+def test_one_token_continuation_equals_decode_step(oracle_mod, gamma):
+    """A causal pass over one token that starts from a given (S, z) and a
+    decode step on the same (S, z) are the same recurrence step, reached
+    through different entry points."""
+    N, D, Dv = 12, 4, 6
+    q, k, v = rng_inputs(25, N + 1, D, Dv)
+    _, S, z = oracle_mod.causal(q[:N], k[:N], v[:N], gamma=gamma,
+                                return_state=True)
+    o_c, S_c, z_c = oracle_mod.causal(q[N:], k[N:], v[N:], gamma=gamma,
+                                      state=(S.copy(), z.copy()),
+                                      return_state=True)
+    o_d, S_d, z_d = oracle_mod.decode_step(q[N], k[N], v[N], S.copy(),
+                                           z.copy(), gamma=gamma)
+    assert rel_err(o_c[0], o_d) < 1e-15
+    assert rel_err(S_c, S_d) < 1e-15 and rel_err(z_c, z_d) < 1e-15
+
+
 def test_empty_sequence(oracle_mod):
     q = np.zeros((0, 4), np.float32)
     v = np.zeros((0, 3), np.float32)

@@ -60,6 +60,23 @@ def test_zero_directions_give_the_gaussian_closed_form():
     assert np.allclose(f, np.broadcast_to(ref, f.shape), rtol=1e-15, atol=0)
 
 
+def test_one_direction_fixes_each_feature_to_its_row():
+    """W zero but for row j = c e_m: feature j is exp(c x_m - |x|^2/2)/sqrt(r)
+    and every other feature exp(-|x|^2/2)/sqrt(r), so feature j belongs to
+    row j of W.  D = r, so that a transposed W gives wrong values rather than
+    a shape error."""
+    r = D = 6
+    x = np.random.default_rng(31).normal(size=(5, D))
+    base = np.exp(-0.5 * (x * x).sum(1)) / np.sqrt(r)
+    for j, m, c in ((0, 3, 0.7), (4, 1, -1.3), (5, 5, 0.4)):
+        W = np.zeros((r, D))
+        W[j, m] = c
+        f = fv.favor_features(x, W)
+        ref = np.repeat(base[:, None], r, axis=1)
+        ref[:, j] = base * np.exp(c * x[:, m])
+        assert np.allclose(f, ref, rtol=1e-14, atol=0)
+
+
 def test_many_features_approach_softmax_attention():
     """With many random features, non-causal Performer attention approaches
     exact softmax attention softmax(q k^T) V (eps = 0)."""
