@@ -50,6 +50,7 @@ class LinAttnError(RuntimeError):
 
 
 def library_path() -> str:
+    """Path of the in-tree liblinattn.so that load_library() opens."""
     return _LIB_PATH
 
 
@@ -109,6 +110,7 @@ def load_library() -> ctypes.CDLL:
 
 
 def status_string(code: int) -> str:
+    """The library's text for a status code (la_status_string)."""
     return load_library().la_status_string(int(code)).decode()
 
 
